@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Throughput of the INT8 NCxHWx<32> Conv2d fprop path on GB300.
+
+One step = one i8c_plan_run (fp16 filter staging kernel + the tcgen05
+implicit-GEMM kernel) over one batch of the synthetic workload, inputs
+resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--all]
+  python bench.py --impl reference ...   # the CPU oracle, timed on the host
+
+With N > 1 (torchrun) every rank runs an independent replica on its own
+GPU (the convolution has no exchange step): value = work of all ranks /
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "INT8 conv fprop TOPS (1 GB300) and % of dense INT8 tensor-core roofline"
+DEFAULT_WORKLOAD = "n8c256h56k256r3s1"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_TENSOR_TFLOPS = 1900.0
+
+
+def ops_of(wl) -> int:
+    # 2*N*K*P*Q*C*R*S with P, Q from the library (not the oracle)
+    import int8_implicit_gemm_gb300 as ext
+    P, Q = ext.i8c_output_size(wl.shape_tuple())
+    return 2 * wl.N * wl.K * P * Q * wl.C * wl.R * wl.S
+
+
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        # kind::f16 (fp16 operands) runs at the bf16 rate: nominal ratio 1.
+        return float(d["bf16_tflops"]), "of measured (bf16 burst cuBLAS; fp16 kind::f16 at the same nominal rate)"
+    except Exception:
+        return FALLBACK_TENSOR_TFLOPS, "of fallback (1.9 PFLOP/s bf16; fp16 at the same nominal rate)"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int8_implicit_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(workload: str):
+    """Per-launch DRAM bytes of the convolution kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "conv_fprop_tc_dram_traffic.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    entry = d.get("workloads", {}).get(workload)
+    return None if entry is None else entry.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(name)
+            except Exception:
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_rate(wl, budget_s: float, max_images: int | None = None):
+    """Time the CPU oracle (as it stands) on the first images of the workload
+    until about budget_s seconds of work are done.  Returns (TOPS, cores, sample)."""
+    import oracle
+    x = wl.activations_nchw()
+    f = wl.filters_kcrs()
+    shape = list(wl.shape_tuple())
+    orc = oracle.Oracle()
+    P, Q = orc.out_size(wl.shape_tuple())
+    cores = os.cpu_count() or 1
+    n_img, done_ops, elapsed = 1, 0, 0.0
+    limit = wl.N if max_images is None else min(wl.N, max_images)
+    while True:
+        shape[0] = n_img
+        t0 = time.perf_counter()
+        orc.conv2d_fprop(x[:n_img], f, tuple(shape), wl.alpha, threads=cores)
+        dt = time.perf_counter() - t0
+        done_ops = 2 * n_img * wl.K * P * Q * wl.C * wl.R * wl.S
+        elapsed = dt
+        if dt >= budget_s / 4 or n_img >= limit:
+            break
+        n_img = min(limit, n_img * 4 if dt < budget_s / 16 else n_img * 2)
+    sample = f"{n_img} of {wl.N} images, all {wl.K} output channels ({done_ops / 2:.3g} multiply-adds)"
+    return done_ops / elapsed / 1e12, cores, sample, elapsed
+
+
+def run_ours(args, wl, rank, world):
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    shape = wl.shape_tuple()
+    P, Q = ext.i8c_output_size(shape)
+    ops = ops_of(wl)
+    x_bytes = wl.N * wl.C * wl.H * wl.W
+    f_bytes = wl.K * wl.C * wl.R * wl.S
+    y_bytes = wl.N * wl.K * P * Q
+
+    # seeded inputs, packed on the device by the library's layout kernels
+    x_nchw = torch.from_numpy(wl.activations_nchw()).cuda()
+    f_kcrs = torch.from_numpy(wl.filters_kcrs()).cuda()
+    x0 = torch.empty(x_bytes, dtype=torch.int8, device="cuda")
+    f0 = torch.empty(f_bytes, dtype=torch.int8, device="cuda")
+    ext.i8c_pack_nchw_to_ncxhwx32(x_nchw, x0, wl.N, wl.C, wl.H, wl.W)
+    ext.i8c_pack_kcrs_to_cxrskx32(f_kcrs, f0, wl.K, wl.C, wl.R, wl.S)
+    del x_nchw, f_kcrs
+    # rotate distinct buffer sets so that the sets together exceed L2
+    set_bytes = x_bytes + f_bytes + y_bytes
+    nsets = max(1, min(64, math.ceil(2 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(nsets):
+        xi = x0 if i == 0 else x0.clone()
+        fi = f0 if i == 0 else f0.clone()
+        sets.append((xi, fi, torch.empty(y_bytes, dtype=torch.int8, device="cuda")))
+    plan = ext.Plan(shape, timing_events=max(1, args.steps))
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        xi, fi, yi = sets[i % nsets]
+        plan.run(xi, fi, yi, wl.alpha, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    assert plan.status(stream) == 0
+    plan.kernel_time()  # discard warm-up launches
+
+    clocks = ClockSampler(dev) if (rank == 0 and not args.no_clocks) else None
+    if clocks:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = ext.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    launches = ext.launch_count() - launches0
+    total_ms = ev0.elapsed_time(ev1)
+    kern_ms, kern_n = plan.kernel_time()
+    clock_rec = clocks.stop() if clocks else None
+    st = plan.status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {ext.status_string(st)}")
+
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    ms_per_step = total_ms / args.steps
+    value = world * ops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the C-ABI on pinned host buffers: H2D of x and f,
+    # the run, D2H of y, every step
+    plan_h = ext.Plan(shape, host_staging=True)
+    xh = x0.cpu().pin_memory()
+    fh = f0.cpu().pin_memory()
+    yh = torch.empty(y_bytes, dtype=torch.int8).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        plan_h.run_host(xh, fh, yh, wl.alpha, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        plan_h.run_host(xh, fh, yh, wl.alpha, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert plan_h.status(stream) == 0
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    plan_h.destroy()
+
+    peak, peak_note = tensor_peak()
+    kern_avg_ms = kern_ms / max(1, kern_n)
+    achieved = ops / (kern_avg_ms * 1e-3) / 1e12
+    traffic = dram_traffic(wl.name)
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "s8 in/out; s8 x s8 products on fp16 tensor-core operands, fp32 chunks flushed to exact s32",
+        "data": "synthetic (seeded xoshiro256**, uniform/normal int8 per workload)",
+        "config": {"workload": wl.name, "shape": dict(zip(
+            ["N", "C", "H", "W", "K", "R", "S", "pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w"], shape)),
+            "P": P, "Q": Q, "alpha": wl.alpha,
+            "l2": f"{nsets} rotating input/output sets, {nsets * set_bytes / 2**20:.0f} MiB total > 129 MiB L2",
+            "plan": {k: plan.info[k] for k in ("block_m", "block_n", "num_tiles", "num_ctas", "num_chunks",
+                                              "chunk_slices", "acc_buffers", "smem_bytes")},
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "conv_fprop_tc_kernel", "kernel_ms": round(kern_avg_ms, 6),
+                     "note": f"int8 ops (2*N*K*P*Q*C*R*S) per launch / CUDA-event duration; peak {peak_note}"},
+        "e2e": {"value": round(ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS", "ms_per_step": round(e2e_ms, 6),
+                "h2d_bytes_per_step": x_bytes + f_bytes, "d2h_bytes_per_step": y_bytes,
+                "path": "i8c_plan_run_host on pinned host buffers"},
+        "gpu_launches": launches,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if clock_rec is not None:
+        result["clocks"] = clock_rec
+    plan.destroy()
+    if args.all and rank == 0:
+        result["all_workloads"] = {w.name: bench_one_quick(w) for w in synth.WORKLOADS}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, cores, sample, el = cpu_oracle_rate(wl, args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(v, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+                                  "sample": sample, "seconds": round(el, 2)}
+    return result
+
+
+def bench_one_quick(wl, steps=50, warmup=5):
+    """Device time per step and conv-kernel roofline fraction for one workload."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = wl.shape_tuple()
+    P, Q = ext.i8c_output_size(shape)
+    ops = ops_of(wl)
+    xb, fb, yb = wl.N * wl.C * wl.H * wl.W, wl.K * wl.C * wl.R * wl.S, wl.N * wl.K * P * Q
+    nsets = max(1, min(64, math.ceil(2 * L2_BYTES / (xb + fb + yb))))
+    g = torch.Generator(device="cuda").manual_seed(wl.x_seed)
+    sets = [(torch.randint(-128, 128, (xb,), dtype=torch.int8, device="cuda", generator=g),
+             torch.randint(-128, 128, (fb,), dtype=torch.int8, device="cuda", generator=g),
+             torch.empty(yb, dtype=torch.int8, device="cuda")) for _ in range(nsets)]
+    plan = ext.Plan(shape, timing_events=steps)
+    s = torch.cuda.current_stream()
+    for i in range(warmup):
+        plan.run(*sets[i % nsets], wl.alpha, s)
+    torch.cuda.synchronize()
+    plan.kernel_time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(steps):
+        plan.run(*sets[i % nsets], wl.alpha, s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    assert plan.status(s) == 0
+    kms, kn = plan.kernel_time()
+    peak, _ = tensor_peak()
+    step_ms = e0.elapsed_time(e1) / steps
+    kern = kms / max(1, kn)
+    plan.destroy()
+    return {"ms_per_step": round(step_ms, 6), "TOPS": round(ops / (step_ms * 1e-3) / 1e12, 2),
+            "kernel_ms": round(kern, 6), "kernel_TOPS": round(ops / (kern * 1e-3) / 1e12, 2),
+            "frac": round(ops / (kern * 1e-3) / 1e12 / peak, 4), "block_n": plan.info["block_n"]}
+
+
+def run_reference(args, wl, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample
+    (the first image of the workload), timed on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    x = wl.activations_nchw()
+    f = wl.filters_kcrs()
+    orc = oracle.Oracle()
+    P, Q = orc.out_size(wl.shape_tuple())
+    shape = list(wl.shape_tuple())
+    shape[0] = 1
+    cores = os.cpu_count() or 1
+    step_ops = 2 * wl.K * P * Q * wl.C * wl.R * wl.S
+    for _ in range(args.warmup):
+        orc.conv2d_fprop(x[:1], f, tuple(shape), wl.alpha, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.conv2d_fprop(x[:1], f, tuple(shape), wl.alpha, threads=cores)
+    dt = time.perf_counter() - t0
+    v = step_ops * args.steps / dt / 1e12
+    sample = f"1 of {wl.N} images per step, all {wl.K} output channels"
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8 (int64 accumulation)",
+            "data": "synthetic", "config": {"workload": wl.name},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS_BY_NAME))
+    ap.add_argument("--all", action="store_true", help="also time every workload (quick, device time only)")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work for cpu_baseline")
+    args = ap.parse_args()
+    args.steps = max(1, args.steps)
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = synth.WORKLOADS_BY_NAME[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, wl, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, wl, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

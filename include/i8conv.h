@@ -1,0 +1,197 @@
+/*
+ * i8conv -- INT8 Conv2d forward propagation (fprop) on one GB300 (sm_103a).
+ *
+ * The operation is the one configured in the CUTLASS issue "How to optimize
+ * cutlass int8 fprop2d kernel with NCxHWx interleaved layout" (section "CUTLASS
+ * Kernel Configuration"): DefaultConv2dFprop with int8 activations in
+ * NCxHWx<32>, int8 filters in CxRSKx<32>, int8 outputs in NCxHWx<32>, an int32
+ * accumulator and the LinearCombinationClamp epilogue with alpha-only scaling:
+ *
+ *     acc[n][k][p][q] = sum_{c,r,s} x[n][c][p*stride_h - pad_h + r*dil_h]
+ *                                         [q*stride_w - pad_w + s*dil_w] * f[k][c][r][s]
+ *     y[n][k][p][q]   = clamp(rint(alpha * (float)acc), -128, 127)
+ *
+ * with zero padding, P = floor((H + 2*pad_h - dil_h*(R-1) - 1)/stride_h) + 1
+ * and Q likewise (the output-size formula of the POPCORNBENCH l1_p80 trace,
+ * first analysis paragraph).  (float)acc rounds to nearest even, the product
+ * is one fp32 multiply, rint rounds half to even.  Results are bit-exact.
+ *
+ * Memory layouts (all int8, all dense, no padding between elements):
+ *   NCxHWx<32>: element (n, c, h, w) at (((n*C/32 + c/32)*H + h)*W + w)*32 + c%32
+ *   CxRSKx<32>: element (k, c, r, s) at ((((c/32)*R + r)*S + s)*K + k)*32 + c%32
+ *   NCHW / KCRS: the plain row-major orders (used only by the pack helpers).
+ * The CxRSKx<32> formula is our reading of the layout's name by analogy with
+ * NCxHWx<32>; the pack/unpack helpers below define it.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned
+ *     (the configuration's 16/16 alignment), and inputs never alias outputs.
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and returns
+ *     immediately; results are valid once the stream reaches that point.
+ *   - No entry point throws; each returns an i8c_status.  Argument errors are
+ *     detected on the host before anything is enqueued.  Errors raised while a
+ *     kernel runs (a bounded wait that ran out) are recorded in a per-plan
+ *     device status word read by i8c_plan_status().
+ *   - There is no CPU fallback: without a usable CUDA device the calls fail
+ *     with I8C_ERR_CUDA / I8C_ERR_NO_DEVICE.
+ */
+#ifndef I8CONV_H_
+#define I8CONV_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  I8C_OK = 0,
+  I8C_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad option   */
+  I8C_ERR_UNSUPPORTED = 2,   /* C or K not a multiple of 32, empty output     */
+  I8C_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned       */
+  I8C_ERR_OVERFLOW_RISK = 4, /* C*R*S*128*128 could exceed int32, or a size
+                                overflows 32-bit indexing                      */
+  I8C_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed             */
+  I8C_ERR_TIMEOUT = 6,       /* a kernel's bounded wait ran out (device side) */
+  I8C_ERR_NO_DEVICE = 7      /* no CUDA device, or not an sm_103 device       */
+} i8c_status;
+
+/* Convolution geometry.  Padding, stride and dilation are per axis (h, w);
+ * the same padding is applied on both sides of an axis, as in nn.Conv2d. */
+typedef struct {
+  int32_t N, C, H, W; /* batch, input channels, input height and width   */
+  int32_t K, R, S;    /* output channels, filter height and width         */
+  int32_t pad_h, pad_w, stride_h, stride_w, dil_h, dil_w;
+} i8c_conv_shape;
+
+/* Plan options.  Zero-initialise for defaults. */
+typedef struct {
+  int32_t block_n;           /* output channels per tile: 0 = auto, else 32, 64, 128 or 256   */
+  int32_t num_ctas;          /* persistent CTAs: 0 = one per SM                                */
+  int32_t max_chunk_slices;  /* K-slices (32 channels each) per exact fp32 chunk: 0 = 32      */
+  int32_t wait_timeout_us;   /* device-side bounded waits: 0 = 2,000,000 us                     */
+  int32_t host_staging;      /* 1 = allocate device staging buffers for i8c_plan_run_host     */
+  int32_t debug_flags;       /* test hooks, see I8C_DEBUG_*; 0 in production                  */
+  int32_t timing_events;     /* > 0: bracket each convolution kernel with CUDA events (keeps
+                                the last timing_events launches) for i8c_plan_kernel_time;
+                                for benchmarks, not for use under graph capture               */
+} i8c_options;
+
+/* debug_flags: make the activation producers skip their first arrival, so
+ * the MMA warp's bounded wait runs out and the kernel reports
+ * I8C_ERR_TIMEOUT without faulting or hanging.  Used by the failure tests. */
+#define I8C_DEBUG_SKIP_FIRST_ARRIVE 1
+
+typedef struct i8c_plan i8c_plan;
+
+/* Read-only facts about a plan (for benchmarks and tests). */
+typedef struct {
+  int32_t P, Q;              /* output height and width                        */
+  int64_t M;                 /* GEMM rows: N*P*Q                               */
+  int32_t gemm_n, gemm_k;    /* GEMM columns (K) and reduction length (C*R*S)  */
+  int32_t block_m, block_n;  /* tile shape                                     */
+  int32_t num_tiles;         /* M-tiles x N-tiles                              */
+  int32_t num_ctas;          /* persistent grid size                           */
+  int32_t num_chunks;        /* exact fp32 chunks per tile                     */
+  int32_t chunk_slices;      /* K-slices per chunk                             */
+  int32_t acc_buffers;       /* tensor-memory accumulator buffers              */
+  int32_t smem_bytes;        /* dynamic shared memory per CTA                  */
+  int32_t kernels_per_run;   /* kernel launches enqueued by one i8c_plan_run   */
+  int64_t ops;               /* 2*N*K*P*Q*C*R*S                                 */
+  int64_t workspace_bytes;   /* device memory owned by the plan                */
+} i8c_plan_info;
+
+/* Output height P and width Q for a shape (formula above).  Returns
+ * I8C_ERR_INVALID_ARG for non-positive sizes or negative padding and
+ * I8C_ERR_UNSUPPORTED when the dilated filter does not fit (P or Q < 1). */
+i8c_status i8c_output_size(const i8c_conv_shape* shape, int32_t* P, int32_t* Q);
+
+/* The argument check of the checked entry points (the CUTLASS Python API's
+ * supports(), host-latency tutorial, "Bypassing argument checks"):
+ * positive sizes, C % 32 == 0, K % 32 == 0, P, Q >= 1, C*R*S*16384 < 2^31
+ * (so no int32 accumulator can overflow and saturating accumulation is moot),
+ * and every tensor small enough for 32-bit element offsets per image plane. */
+i8c_status i8c_supported(const i8c_conv_shape* shape);
+
+/* Checked one-shot convolution: validates, then runs on `stream` using a
+ * plan cached per (shape, device).  The first call for a shape creates the
+ * plan (allocates and may synchronise the device); later calls do not.
+ *   x: NCxHWx<32> int8 [N][C/32][H][W][32], read-only
+ *   f: CxRSKx<32> int8 [C/32][R][S][K][32], read-only
+ *   y: NCxHWx<32> int8 [N][K/32][P][Q][32], written */
+i8c_status i8c_conv2d_fprop(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape,
+                            float alpha, cudaStream_t stream);
+
+/* As i8c_conv2d_fprop, but writes the int32 accumulators instead of the
+ * epilogue result: acc is [N][K/32][P][Q][32] int32 (same interleave).
+ * For parity checks of the contraction alone. */
+i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, const i8c_conv_shape* shape,
+                                cudaStream_t stream);
+
+/* Compile-once / run-many (host-latency tutorial, "Compiling once"): a plan
+ * holds the validated shape, the tile schedule, the filter staging buffer
+ * and a device status word, allocated on the current device.  `opts` may be
+ * NULL.  The plan must be used on that device and destroyed by the caller. */
+i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts, i8c_plan** plan);
+
+/* Unchecked run (host-latency tutorial, "Bypassing argument checks"): no
+ * shape validation (only null and 16-byte alignment checks, since a
+ * misaligned vector access would otherwise fault the device), no
+ * allocation, no synchronisation, so it
+ * can be captured in a CUDA graph (tutorial section "CUDA Graphs").  Runs
+ * sharing one plan must be serialised on one stream: they share the plan's
+ * filter staging buffer. */
+i8c_status i8c_plan_run(const i8c_plan* plan, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
+                        cudaStream_t stream);
+
+/* Unchecked run that writes int32 accumulators (layout as in _acc above). */
+i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t* f, int32_t* acc,
+                            cudaStream_t stream);
+
+/* End-to-end run on HOST buffers: copies x and f from host memory into the
+ * plan's staging buffers, runs, and copies y back, all on `stream`.  The plan
+ * must have been created with host_staging = 1.  Pinned (page-locked) host
+ * memory makes the copies asynchronous; the caller synchronises `stream`
+ * before reading y. */
+i8c_status i8c_plan_run_host(const i8c_plan* plan, const int8_t* x_host, const int8_t* f_host, int8_t* y_host,
+                             float alpha, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns (and clears) the plan's device status
+ * word: I8C_OK, or I8C_ERR_TIMEOUT if a bounded wait in a kernel ran out. */
+i8c_status i8c_plan_status(const i8c_plan* plan, cudaStream_t stream);
+
+i8c_status i8c_plan_get_info(const i8c_plan* plan, i8c_plan_info* info);
+
+/* With timing_events > 0: synchronises on the last recorded event, returns
+ * the summed device time (ms) of the convolution-kernel launches recorded
+ * since the previous call and their count, and starts a new window.  Only
+ * the last timing_events launches are kept. */
+i8c_status i8c_plan_kernel_time(const i8c_plan* plan, double* total_ms, int64_t* launches);
+
+/* Frees the plan's device memory.  Synchronises the device first. */
+i8c_status i8c_plan_destroy(i8c_plan* plan);
+
+/* Layout helpers (device, byte permutations, not part of the timed path).
+ * C (resp. K for filters) must be a multiple of 32 where it is interleaved. */
+i8c_status i8c_pack_nchw_to_ncxhwx32(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,
+                                     cudaStream_t stream);
+i8c_status i8c_unpack_ncxhwx32_to_nchw(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,
+                                       cudaStream_t stream);
+i8c_status i8c_pack_kcrs_to_cxrskx32(const int8_t* src, int8_t* dst, int32_t K, int32_t C, int32_t R, int32_t S,
+                                     cudaStream_t stream);
+i8c_status i8c_unpack_cxrskx32_to_kcrs(const int8_t* src, int8_t* dst, int32_t K, int32_t C, int32_t R, int32_t S,
+                                       cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* i8c_status_string(i8c_status status);
+
+/* Number of kernel launches this library has enqueued in this process
+ * (all entry points, all devices).  For launch accounting in benchmarks. */
+int64_t i8c_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I8CONV_H_ */

@@ -1,0 +1,245 @@
+"""Python binding of ``libi8conv.so`` (INT8 NCxHWx<32> Conv2d fprop on GB300).
+
+A thin ctypes layer: argument marshalling only, every step of the
+convolution runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams.  The function names match the C entry points declared in
+``include/i8conv.h``; ``Plan`` wraps the plan handle.
+
+There is no fallback: if the library is missing this module raises at import
+time, and without a GB300 the calls fail with ``I8ConvError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libi8conv.so")
+
+# status codes (include/i8conv.h)
+I8C_OK = 0
+I8C_ERR_INVALID_ARG = 1
+I8C_ERR_UNSUPPORTED = 2
+I8C_ERR_MISALIGNED = 3
+I8C_ERR_OVERFLOW_RISK = 4
+I8C_ERR_CUDA = 5
+I8C_ERR_TIMEOUT = 6
+I8C_ERR_NO_DEVICE = 7
+I8C_DEBUG_SKIP_FIRST_ARRIVE = 1
+
+
+class I8ConvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+class ConvShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("N", "C", "H", "W", "K", "R", "S", "pad_h", "pad_w",
+                 "stride_h", "stride_w", "dil_h", "dil_w")]
+
+    @classmethod
+    def of(cls, shape) -> "ConvShape":
+        if isinstance(shape, ConvShape):
+            return shape
+        if isinstance(shape, dict):
+            return cls(*[int(shape[n]) for n, _ in cls._fields_])
+        return cls(*[int(v) for v in shape])
+
+    def astuple(self):
+        return tuple(getattr(self, n) for n, _ in self._fields_)
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("block_n", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("max_chunk_slices", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
+                ("host_staging", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
+                ("timing_events", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_int32), ("Q", ctypes.c_int32), ("M", ctypes.c_int64),
+                ("gemm_n", ctypes.c_int32), ("gemm_k", ctypes.c_int32),
+                ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("num_tiles", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("num_chunks", ctypes.c_int32), ("chunk_slices", ctypes.c_int32),
+                ("acc_buffers", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("kernels_per_run", ctypes.c_int32), ("ops", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def asdict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run int8_implicit_gemm_gb300/build_lib.py "
+                          "(or __graft_entry__.build()) first -- there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    S = ctypes.POINTER(ConvShape)
+    sig = {
+        "i8c_output_size": [S, ctypes.POINTER(I32), ctypes.POINTER(I32)],
+        "i8c_supported": [S],
+        "i8c_conv2d_fprop": [P, P, P, S, F, P],
+        "i8c_conv2d_fprop_acc": [P, P, P, S, P],
+        "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
+        "i8c_plan_run": [P, P, P, P, F, P],
+        "i8c_plan_run_acc": [P, P, P, P, P],
+        "i8c_plan_run_host": [P, P, P, P, F, P],
+        "i8c_plan_status": [P, P],
+        "i8c_plan_get_info": [P, ctypes.POINTER(PlanInfo)],
+        "i8c_plan_kernel_time": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
+        "i8c_plan_destroy": [P],
+        "i8c_pack_nchw_to_ncxhwx32": [P, P, I32, I32, I32, I32, P],
+        "i8c_unpack_ncxhwx32_to_nchw": [P, P, I32, I32, I32, I32, P],
+        "i8c_pack_kcrs_to_cxrskx32": [P, P, I32, I32, I32, I32, P],
+        "i8c_unpack_cxrskx32_to_kcrs": [P, P, I32, I32, I32, I32, P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.i8c_status_string.argtypes = [ctypes.c_int]
+    lib.i8c_status_string.restype = ctypes.c_char_p
+    lib.i8c_launch_count.argtypes = []
+    lib.i8c_launch_count.restype = I64
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.i8c_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != I8C_OK:
+        raise I8ConvError(status, where)
+
+
+def _ptr(t) -> int:
+    """Raw address of a tensor's data (torch tensor) or of a numpy array."""
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    return t.ctypes.data
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def launch_count() -> int:
+    return int(lib.i8c_launch_count())
+
+
+def i8c_output_size(shape):
+    P, Q = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib.i8c_output_size(ctypes.byref(ConvShape.of(shape)), ctypes.byref(P), ctypes.byref(Q)),
+           "i8c_output_size")
+    return P.value, Q.value
+
+
+def i8c_supported(shape) -> int:
+    """Status code of the argument check (0 = supported)."""
+    return lib.i8c_supported(ctypes.byref(ConvShape.of(shape)))
+
+
+def i8c_conv2d_fprop(x, f, y, shape, alpha: float, stream=None) -> None:
+    _check(lib.i8c_conv2d_fprop(_ptr(x), _ptr(f), _ptr(y), ctypes.byref(ConvShape.of(shape)),
+                                ctypes.c_float(alpha), _stream(stream)), "i8c_conv2d_fprop")
+
+
+def i8c_conv2d_fprop_acc(x, f, acc, shape, stream=None) -> None:
+    _check(lib.i8c_conv2d_fprop_acc(_ptr(x), _ptr(f), _ptr(acc), ctypes.byref(ConvShape.of(shape)),
+                                    _stream(stream)), "i8c_conv2d_fprop_acc")
+
+
+def i8c_pack_nchw_to_ncxhwx32(src, dst, N, C, H, W, stream=None) -> None:
+    _check(lib.i8c_pack_nchw_to_ncxhwx32(_ptr(src), _ptr(dst), N, C, H, W, _stream(stream)), "pack")
+
+
+def i8c_unpack_ncxhwx32_to_nchw(src, dst, N, C, H, W, stream=None) -> None:
+    _check(lib.i8c_unpack_ncxhwx32_to_nchw(_ptr(src), _ptr(dst), N, C, H, W, _stream(stream)), "unpack")
+
+
+def i8c_pack_kcrs_to_cxrskx32(src, dst, K, C, R, S, stream=None) -> None:
+    _check(lib.i8c_pack_kcrs_to_cxrskx32(_ptr(src), _ptr(dst), K, C, R, S, _stream(stream)), "pack")
+
+
+def i8c_unpack_cxrskx32_to_kcrs(src, dst, K, C, R, S, stream=None) -> None:
+    _check(lib.i8c_unpack_cxrskx32_to_kcrs(_ptr(src), _ptr(dst), K, C, R, S, _stream(stream)), "unpack")
+
+
+class Plan:
+    """A validated convolution plan on the current CUDA device (i8c_plan_*)."""
+
+    def __init__(self, shape, block_n=0, num_ctas=0, max_chunk_slices=0, wait_timeout_us=0,
+                 host_staging=False, debug_flags=0, timing_events=0):
+        self.shape = ConvShape.of(shape)
+        opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(bool(host_staging)), debug_flags,
+                       timing_events)
+        h = ctypes.c_void_p()
+        _check(lib.i8c_plan_create(ctypes.byref(self.shape), ctypes.byref(opts), ctypes.byref(h)),
+               "i8c_plan_create")
+        self.handle = h
+        info = PlanInfo()
+        _check(lib.i8c_plan_get_info(self.handle, ctypes.byref(info)), "i8c_plan_get_info")
+        self.info = info.asdict()
+
+    def run(self, x, f, y, alpha: float, stream=None) -> None:
+        _check(lib.i8c_plan_run(self.handle, _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha), _stream(stream)),
+               "i8c_plan_run")
+
+    def run_acc(self, x, f, acc, stream=None) -> None:
+        _check(lib.i8c_plan_run_acc(self.handle, _ptr(x), _ptr(f), _ptr(acc), _stream(stream)), "i8c_plan_run_acc")
+
+    def run_host(self, x_host, f_host, y_host, alpha: float, stream=None) -> None:
+        _check(lib.i8c_plan_run_host(self.handle, _ptr(x_host), _ptr(f_host), _ptr(y_host), ctypes.c_float(alpha),
+                                     _stream(stream)), "i8c_plan_run_host")
+
+    def kernel_time(self):
+        """(summed ms, launches) of the convolution kernels timed since the last call."""
+        ms, n = ctypes.c_double(), ctypes.c_int64()
+        _check(lib.i8c_plan_kernel_time(self.handle, ctypes.byref(ms), ctypes.byref(n)), "i8c_plan_kernel_time")
+        return ms.value, n.value
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return (and clear) the device status word."""
+        return lib.i8c_plan_status(self.handle, _stream(stream))
+
+    def destroy(self) -> None:
+        if self.handle:
+            _check(lib.i8c_plan_destroy(self.handle), "i8c_plan_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                lib.i8c_plan_destroy(self.handle)
+        except Exception:
+            pass
+
+
+def output_nbytes(shape) -> int:
+    s = ConvShape.of(shape)
+    P, Q = i8c_output_size(s)
+    return s.N * s.K * P * Q
+
+
+def conv2d_fprop(x, f, shape, alpha: float, out=None, stream=None):
+    """Convenience wrapper: allocate the NCxHWx<32> int8 output with torch and run."""
+    import torch
+    s = ConvShape.of(shape)
+    P, Q = i8c_output_size(s)
+    if out is None:
+        out = torch.empty((s.N, s.K // 32, P, Q, 32), dtype=torch.int8, device=x.device)
+    i8c_conv2d_fprop(x, f, out, s, alpha, stream)
+    return out

@@ -1,0 +1,477 @@
+// Host side of the C-ABI: argument checks, plans, the filter tensor map, and
+// launches.  See include/i8conv.h for the contract of each entry point.
+#include <cudaTypedefs.h>
+
+#include <array>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/i8conv.h"
+#include "internal.h"
+
+using i8c::ConvParams;
+
+struct i8c_plan {
+  i8c_conv_shape shape;
+  int P, Q;
+  int64_t M;
+  int device;
+  int block_n, num_n_tiles, num_m_tiles, num_tiles, num_ctas;
+  int num_slices, chunk_slices, num_chunks, acc_buffers;
+  uint32_t tmem_cols;
+  int smem_bytes;
+  uint64_t timeout_ns;
+  int debug_flags;
+  uint16_t* f16;   // fp16 copy of the filter, [C/32][R][S][K][32]
+  int* status;     // device status word
+  CUtensorMap tmap;
+  int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
+  size_t x_bytes, f_bytes, y_bytes;
+  int64_t workspace_bytes;
+  // optional per-launch timing of the convolution kernel
+  std::vector<cudaEvent_t> ev_start, ev_end;
+  mutable int64_t ev_recorded = 0;
+};
+
+namespace {
+
+constexpr int64_t kMaxI32 = 2147483647LL;
+
+i8c_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return I8C_OK;
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return I8C_ERR_NO_DEVICE;
+  return I8C_ERR_CUDA;
+}
+
+int64_t extent(int64_t in, int64_t pad, int64_t dil, int64_t k, int64_t stride) {
+  const int64_t num = in + 2 * pad - dil * (k - 1) - 1;
+  if (num < 0) return 0;
+  return num / stride + 1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+i8c_status check_shape(const i8c_conv_shape* s, int64_t* P, int64_t* Q) {
+  if (s == nullptr) return I8C_ERR_INVALID_ARG;
+  if (s->N < 1 || s->C < 1 || s->H < 1 || s->W < 1 || s->K < 1 || s->R < 1 || s->S < 1) return I8C_ERR_INVALID_ARG;
+  if (s->pad_h < 0 || s->pad_w < 0 || s->stride_h < 1 || s->stride_w < 1 || s->dil_h < 1 || s->dil_w < 1)
+    return I8C_ERR_INVALID_ARG;
+  *P = extent(s->H, s->pad_h, s->dil_h, s->R, s->stride_h);
+  *Q = extent(s->W, s->pad_w, s->dil_w, s->S, s->stride_w);
+  if (*P < 1 || *Q < 1) return I8C_ERR_UNSUPPORTED;
+  return I8C_OK;
+}
+
+i8c_status check_supported(const i8c_conv_shape* s, int64_t* P, int64_t* Q) {
+  i8c_status st = check_shape(s, P, Q);
+  if (st != I8C_OK) return st;
+  if (s->C % 32 != 0 || s->K % 32 != 0) return I8C_ERR_UNSUPPORTED;
+  // |acc| <= C*R*S*128*128 must fit int32
+  if (static_cast<int64_t>(s->C) * s->R * s->S * 16384 > kMaxI32) return I8C_ERR_OVERFLOW_RISK;
+  // 32-bit element offsets inside one image, 32-bit GEMM row count
+  const int64_t img = static_cast<int64_t>(s->C) * s->H * s->W;
+  const int64_t out_img = static_cast<int64_t>(s->K) * (*P) * (*Q);
+  const int64_t M = static_cast<int64_t>(s->N) * (*P) * (*Q);
+  if (img > kMaxI32 || out_img > kMaxI32 || M > kMaxI32 - 256) return I8C_ERR_OVERFLOW_RISK;
+  return I8C_OK;
+}
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled get_encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+int next_pow2(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+void free_plan_memory(i8c_plan* p) {
+  for (cudaEvent_t e : p->ev_start) cudaEventDestroy(e);
+  for (cudaEvent_t e : p->ev_end) cudaEventDestroy(e);
+  p->ev_start.clear();
+  p->ev_end.clear();
+  if (p->f16) cudaFree(p->f16);
+  if (p->status) cudaFree(p->status);
+  if (p->stage_x) cudaFree(p->stage_x);
+  if (p->stage_f) cudaFree(p->stage_f);
+  if (p->stage_y) cudaFree(p->stage_y);
+}
+
+ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
+  const i8c_conv_shape& s = pl->shape;
+  ConvParams p{};
+  p.x = x;
+  p.status = pl->status;
+  p.alpha = alpha;
+  p.H = s.H;
+  p.W = s.W;
+  p.K = s.K;
+  p.pad_h = s.pad_h;
+  p.pad_w = s.pad_w;
+  p.stride_h = s.stride_h;
+  p.stride_w = s.stride_w;
+  p.dil_h = s.dil_h;
+  p.dil_w = s.dil_w;
+  p.R = s.R;
+  p.S = s.S;
+  p.P = pl->P;
+  p.Q = pl->Q;
+  p.PQ = pl->P * pl->Q;
+  p.M = static_cast<int>(pl->M);
+  p.CB = s.C / 32;
+  p.KB = s.K / 32;
+  p.num_slices = pl->num_slices;
+  p.chunk_slices = pl->chunk_slices;
+  p.num_chunks = pl->num_chunks;
+  p.num_n_tiles = pl->num_n_tiles;
+  p.num_tiles = pl->num_tiles;
+  p.acc_buffers = pl->acc_buffers;
+  p.tmem_cols = pl->tmem_cols;
+  p.img_stride = static_cast<int64_t>(s.C) * s.H * s.W;
+  p.timeout_ns = pl->timeout_ns;
+  p.debug_flags = pl->debug_flags;
+  return p;
+}
+
+i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t* y, int32_t* acc, float alpha,
+                    cudaStream_t stream) {
+  const i8c_conv_shape& s = pl->shape;
+  cudaError_t e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  ConvParams p = make_params(pl, x, alpha);
+  p.y = y;
+  p.acc = acc;
+  p.out_mode = acc != nullptr ? 1 : 0;
+  const size_t nev = pl->ev_start.size();
+  if (nev > 0) {
+    e = cudaEventRecord(pl->ev_start[pl->ev_recorded % nev], stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (nev > 0) {
+    e = cudaEventRecord(pl->ev_end[pl->ev_recorded % nev], stream);
+    ++pl->ev_recorded;
+  }
+  return from_cuda(e);
+}
+
+// Plans behind the one-shot entry points, one per (device, stream, shape).
+std::mutex g_cache_mu;
+std::map<std::array<int64_t, 15>, i8c_plan*> g_cache;
+
+i8c_status cached_plan(const i8c_conv_shape* s, cudaStream_t stream, i8c_plan** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  std::array<int64_t, 15> key{dev, static_cast<int64_t>(reinterpret_cast<uintptr_t>(stream)),
+                              s->N, s->C, s->H, s->W, s->K, s->R, s->S, s->pad_h, s->pad_w,
+                              s->stride_h, s->stride_w, s->dil_h * 65536LL + s->dil_w, 0};
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  auto it = g_cache.find(key);
+  if (it != g_cache.end()) {
+    *out = it->second;
+    return I8C_OK;
+  }
+  i8c_plan* p = nullptr;
+  i8c_status st = i8c_plan_create(s, nullptr, &p);
+  if (st != I8C_OK) return st;
+  g_cache[key] = p;
+  *out = p;
+  return I8C_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* i8c_status_string(i8c_status status) {
+  switch (status) {
+    case I8C_OK: return "ok";
+    case I8C_ERR_INVALID_ARG: return "invalid argument";
+    case I8C_ERR_UNSUPPORTED: return "unsupported shape";
+    case I8C_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case I8C_ERR_OVERFLOW_RISK: return "int32 accumulator or index overflow possible";
+    case I8C_ERR_CUDA: return "CUDA error";
+    case I8C_ERR_TIMEOUT: return "device-side wait timed out";
+    case I8C_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+  }
+  return "unknown status";
+}
+
+int64_t i8c_launch_count(void) { return i8c::g_launches.load(std::memory_order_relaxed); }
+
+i8c_status i8c_output_size(const i8c_conv_shape* shape, int32_t* P, int32_t* Q) {
+  if (P == nullptr || Q == nullptr) return I8C_ERR_INVALID_ARG;
+  int64_t p = 0, q = 0;
+  i8c_status st = check_shape(shape, &p, &q);
+  if (st != I8C_OK) return st;
+  if (p > kMaxI32 || q > kMaxI32) return I8C_ERR_OVERFLOW_RISK;
+  *P = static_cast<int32_t>(p);
+  *Q = static_cast<int32_t>(q);
+  return I8C_OK;
+}
+
+i8c_status i8c_supported(const i8c_conv_shape* shape) {
+  int64_t p = 0, q = 0;
+  return check_supported(shape, &p, &q);
+}
+
+i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts, i8c_plan** out) {
+  if (out == nullptr) return I8C_ERR_INVALID_ARG;
+  *out = nullptr;
+  int64_t P = 0, Q = 0;
+  i8c_status st = check_supported(shape, &P, &Q);
+  if (st != I8C_OK) return st;
+  i8c_options o{};
+  if (opts) o = *opts;
+  if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
+    return I8C_ERR_INVALID_ARG;
+  if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
+      o.timing_events < 0 || o.timing_events > 65536)
+    return I8C_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (prop.major != 10 || prop.minor != 3) return I8C_ERR_NO_DEVICE;
+  EncodeTiled encode = get_encode_tiled();
+  if (encode == nullptr) return I8C_ERR_CUDA;
+
+  i8c_plan* p = new (std::nothrow) i8c_plan();
+  if (p == nullptr) return I8C_ERR_CUDA;
+  const i8c_conv_shape& s = *shape;
+  p->shape = s;
+  p->P = static_cast<int>(P);
+  p->Q = static_cast<int>(Q);
+  p->M = static_cast<int64_t>(s.N) * P * Q;
+  p->device = dev;
+  int bn = o.block_n;
+  if (bn == 0) bn = s.K <= 32 ? 32 : (s.K <= 64 ? 64 : (s.K <= 128 ? 128 : 256));
+  p->block_n = bn;
+  p->num_n_tiles = (s.K + bn - 1) / bn;
+  p->num_m_tiles = static_cast<int>((p->M + 127) / 128);
+  const int64_t tiles = static_cast<int64_t>(p->num_m_tiles) * p->num_n_tiles;
+  if (tiles > kMaxI32) {
+    delete p;
+    return I8C_ERR_OVERFLOW_RISK;
+  }
+  p->num_tiles = static_cast<int>(tiles);
+  const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
+  p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+  p->num_slices = (s.C / 32) * s.R * s.S;
+  const int max_chunk = o.max_chunk_slices > 0 ? o.max_chunk_slices : 32;
+  p->num_chunks = (p->num_slices + max_chunk - 1) / max_chunk;
+  p->chunk_slices = (p->num_slices + p->num_chunks - 1) / p->num_chunks;
+  const int run_cols = p->num_chunks > 1 ? bn : 0;
+  p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
+  p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
+  p->smem_bytes = i8c::conv_smem_bytes(bn);
+  p->timeout_ns = static_cast<uint64_t>(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
+  p->debug_flags = o.debug_flags;
+  p->x_bytes = static_cast<size_t>(s.N) * s.C * s.H * s.W;
+  p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
+  p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
+
+  e = i8c::conv_prepare(bn);
+  if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
+  if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
+  p->workspace_bytes = static_cast<int64_t>(p->f_bytes * 2 + sizeof(int));
+  if (e == cudaSuccess && o.host_staging) {
+    e = cudaMalloc(&p->stage_x, p->x_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->stage_f, p->f_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->stage_y, p->y_bytes);
+    p->workspace_bytes += static_cast<int64_t>(p->x_bytes + p->f_bytes + p->y_bytes);
+  }
+  for (int i = 0; e == cudaSuccess && i < o.timing_events; ++i) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    e = cudaEventCreate(&a);
+    if (e == cudaSuccess) e = cudaEventCreate(&b);
+    if (a) p->ev_start.push_back(a);
+    if (b) p->ev_end.push_back(b);
+  }
+  if (e != cudaSuccess) {
+    free_plan_memory(p);
+    delete p;
+    return from_cuda(e);
+  }
+
+  // fp16 filter as a 3-D tensor {32 channels, K, C/32*R*S}; one box is the
+  // 32-channel rows of BN output channels for one K-slice, 64-byte swizzled.
+  cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(s.K), static_cast<cuuint64_t>(p->num_slices)};
+  cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(s.K) * 64};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p->f16, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) {
+    free_plan_memory(p);
+    delete p;
+    return I8C_ERR_CUDA;
+  }
+  *out = p;
+  return I8C_OK;
+}
+
+i8c_status i8c_plan_destroy(i8c_plan* plan) {
+  if (plan == nullptr) return I8C_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  free_plan_memory(plan);
+  delete plan;
+  return from_cuda(e);
+}
+
+i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
+  if (pl == nullptr || info == nullptr) return I8C_ERR_INVALID_ARG;
+  const i8c_conv_shape& s = pl->shape;
+  info->P = pl->P;
+  info->Q = pl->Q;
+  info->M = pl->M;
+  info->gemm_n = s.K;
+  info->gemm_k = s.C * s.R * s.S;
+  info->block_m = 128;
+  info->block_n = pl->block_n;
+  info->num_tiles = pl->num_tiles;
+  info->num_ctas = pl->num_ctas;
+  info->num_chunks = pl->num_chunks;
+  info->chunk_slices = pl->chunk_slices;
+  info->acc_buffers = pl->acc_buffers;
+  info->smem_bytes = pl->smem_bytes;
+  info->kernels_per_run = 2;
+  info->ops = 2 * pl->M * s.K * static_cast<int64_t>(s.C) * s.R * s.S;
+  info->workspace_bytes = pl->workspace_bytes;
+  return I8C_OK;
+}
+
+i8c_status i8c_plan_kernel_time(const i8c_plan* pl, double* total_ms, int64_t* launches) {
+  if (pl == nullptr || total_ms == nullptr || launches == nullptr) return I8C_ERR_INVALID_ARG;
+  const int64_t nev = static_cast<int64_t>(pl->ev_start.size());
+  *total_ms = 0.0;
+  *launches = 0;
+  if (nev == 0 || pl->ev_recorded == 0) return I8C_OK;
+  const int64_t count = pl->ev_recorded < nev ? pl->ev_recorded : nev;
+  cudaError_t e = cudaEventSynchronize(pl->ev_end[(pl->ev_recorded - 1) % nev]);
+  if (e != cudaSuccess) return from_cuda(e);
+  double sum = 0.0;
+  for (int64_t i = pl->ev_recorded - count; i < pl->ev_recorded; ++i) {
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, pl->ev_start[i % nev], pl->ev_end[i % nev]);
+    if (e != cudaSuccess) return from_cuda(e);
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = count;
+  pl->ev_recorded = 0;
+  return I8C_OK;
+}
+
+i8c_status i8c_plan_run(const i8c_plan* plan, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
+                        cudaStream_t stream) {
+  if (plan == nullptr || x == nullptr || f == nullptr || y == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  return run_plan(plan, x, f, y, nullptr, alpha, stream);
+}
+
+i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t* f, int32_t* acc,
+                            cudaStream_t stream) {
+  if (plan == nullptr || x == nullptr || f == nullptr || acc == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(acc)) return I8C_ERR_MISALIGNED;
+  return run_plan(plan, x, f, nullptr, acc, 1.0f, stream);
+}
+
+i8c_status i8c_plan_run_host(const i8c_plan* pl, const int8_t* x_host, const int8_t* f_host, int8_t* y_host,
+                             float alpha, cudaStream_t stream) {
+  if (pl == nullptr || x_host == nullptr || f_host == nullptr || y_host == nullptr) return I8C_ERR_INVALID_ARG;
+  if (pl->stage_x == nullptr) return I8C_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemcpyAsync(pl->stage_x, x_host, pl->x_bytes, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(pl->stage_f, f_host, pl->f_bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  i8c_status st = run_plan(pl, pl->stage_x, pl->stage_f, pl->stage_y, nullptr, alpha, stream);
+  if (st != I8C_OK) return st;
+  return from_cuda(cudaMemcpyAsync(y_host, pl->stage_y, pl->y_bytes, cudaMemcpyDeviceToHost, stream));
+}
+
+i8c_status i8c_plan_status(const i8c_plan* pl, cudaStream_t stream) {
+  if (pl == nullptr) return I8C_ERR_INVALID_ARG;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  int h = 0;
+  e = cudaMemcpy(&h, pl->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (h != 0) {
+    e = cudaMemset(pl->status, 0, sizeof(int));
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return h == 0 ? I8C_OK : static_cast<i8c_status>(h);
+}
+
+i8c_status i8c_conv2d_fprop(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape, float alpha,
+                            cudaStream_t stream) {
+  if (x == nullptr || f == nullptr || y == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  i8c_plan* p = nullptr;
+  i8c_status st = cached_plan(shape, stream, &p);
+  if (st != I8C_OK) return st;
+  return run_plan(p, x, f, y, nullptr, alpha, stream);
+}
+
+i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, const i8c_conv_shape* shape,
+                                cudaStream_t stream) {
+  if (x == nullptr || f == nullptr || acc == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(acc)) return I8C_ERR_MISALIGNED;
+  i8c_plan* p = nullptr;
+  i8c_status st = cached_plan(shape, stream, &p);
+  if (st != I8C_OK) return st;
+  return run_plan(p, x, f, nullptr, acc, 1.0f, stream);
+}
+
+i8c_status i8c_pack_nchw_to_ncxhwx32(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,
+                                     cudaStream_t stream) {
+  if (src == nullptr || dst == nullptr || N < 1 || C < 1 || H < 1 || W < 1) return I8C_ERR_INVALID_ARG;
+  if (C % 32 != 0) return I8C_ERR_UNSUPPORTED;
+  return from_cuda(i8c::launch_pack_act(src, dst, N, C, H, W, true, stream));
+}
+
+i8c_status i8c_unpack_ncxhwx32_to_nchw(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,
+                                       cudaStream_t stream) {
+  if (src == nullptr || dst == nullptr || N < 1 || C < 1 || H < 1 || W < 1) return I8C_ERR_INVALID_ARG;
+  if (C % 32 != 0) return I8C_ERR_UNSUPPORTED;
+  return from_cuda(i8c::launch_pack_act(src, dst, N, C, H, W, false, stream));
+}
+
+i8c_status i8c_pack_kcrs_to_cxrskx32(const int8_t* src, int8_t* dst, int32_t K, int32_t C, int32_t R, int32_t S,
+                                     cudaStream_t stream) {
+  if (src == nullptr || dst == nullptr || K < 1 || C < 1 || R < 1 || S < 1) return I8C_ERR_INVALID_ARG;
+  if (C % 32 != 0) return I8C_ERR_UNSUPPORTED;
+  return from_cuda(i8c::launch_pack_filter(src, dst, K, C, R, S, true, stream));
+}
+
+i8c_status i8c_unpack_cxrskx32_to_kcrs(const int8_t* src, int8_t* dst, int32_t K, int32_t C, int32_t R, int32_t S,
+                                       cudaStream_t stream) {
+  if (src == nullptr || dst == nullptr || K < 1 || C < 1 || R < 1 || S < 1) return I8C_ERR_INVALID_ARG;
+  if (C % 32 != 0) return I8C_ERR_UNSUPPORTED;
+  return from_cuda(i8c::launch_pack_filter(src, dst, K, C, R, S, false, stream));
+}
+
+}  // extern "C"

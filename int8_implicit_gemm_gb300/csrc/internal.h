@@ -1,0 +1,29 @@
+// Internal interfaces between the library's translation units (not exported).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "conv_fprop_tc.cuh"
+
+namespace i8c {
+
+extern std::atomic<int64_t> g_launches;
+
+// conv_kernels.cu
+int conv_smem_bytes(int block_n);
+cudaError_t conv_prepare(int block_n);  // raise the dynamic shared memory limit
+cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& p, int num_ctas,
+                        cudaStream_t stream);
+
+// layout_kernels.cu
+cudaError_t launch_filter_to_f16(const int8_t* f, uint16_t* f16, int64_t count, cudaStream_t stream);
+cudaError_t launch_pack_act(const int8_t* src, int8_t* dst, int N, int C, int H, int W, bool to_interleaved,
+                            cudaStream_t stream);
+cudaError_t launch_pack_filter(const int8_t* src, int8_t* dst, int K, int C, int R, int S, bool to_interleaved,
+                               cudaStream_t stream);
+
+}  // namespace i8c

@@ -1,0 +1,78 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every entry
+point its header declares, and its host-side argument checks behave as
+documented.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ext():
+    from int8_implicit_gemm_gb300 import build_lib
+    build_lib.build()
+    import int8_implicit_gemm_gb300 as ext
+    return ext
+
+
+def _declared(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(i8c_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(ext):
+    headers = [h for h in os.listdir(os.path.join(ROOT, "include")) if h.endswith(".h")]
+    assert headers
+    lib = ctypes.CDLL(ext.LIB_PATH)
+    for h in headers:
+        names = _declared(h)
+        assert names, h
+        for name in names:
+            assert hasattr(lib, name), f"{name} declared in {h} but not exported"
+
+
+def test_status_strings(ext):
+    assert ext.status_string(0) == "ok"
+    assert "aligned" in ext.status_string(ext.I8C_ERR_MISALIGNED)
+    assert ext.status_string(99) == "unknown status"
+
+
+def test_output_size_page4(ext):
+    # the 5x9 dilated layer of the kernel-benchmark trace: 508 x 496
+    assert ext.i8c_output_size((8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3)) == (508, 496)
+    assert ext.i8c_output_size((32, 128, 112, 112, 256, 3, 3, 1, 1, 2, 2, 1, 1)) == (56, 56)
+
+
+@pytest.mark.parametrize("shape,status", [
+    ((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), 0),
+    ((1, 48, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), 2),       # C not a multiple of 32
+    ((1, 32, 16, 16, 40, 3, 3, 1, 1, 1, 1, 1, 1), 2),       # K not a multiple of 32
+    ((1, 32, 2, 2, 32, 5, 5, 0, 0, 1, 1, 1, 1), 2),         # filter larger than the padded input
+    ((0, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), 1),       # empty batch
+    ((1, 32, 16, 16, 32, 3, 3, -1, 1, 1, 1, 1, 1), 1),      # negative padding
+    ((1, 32, 16, 16, 32, 3, 3, 1, 1, 0, 1, 1, 1), 1),       # zero stride
+    ((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 0), 1),       # zero dilation
+    ((1, 4096, 64, 64, 32, 7, 7, 3, 3, 1, 1, 1, 1), 4),     # C*R*S*2^14 >= 2^31
+])
+def test_supported(ext, shape, status):
+    assert ext.i8c_supported(shape) == status
+
+
+def test_no_cpu_fallback(ext):
+    """Without a usable device the library refuses to run instead of computing on the host."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(ext.I8ConvError) as ei:
+        ext.Plan((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1))
+    assert ei.value.status in (ext.I8C_ERR_NO_DEVICE, ext.I8C_ERR_CUDA)
+
+
+def test_null_pointers_rejected(ext):
+    st = ext.lib.i8c_conv2d_fprop(None, None, None, ctypes.byref(ext.ConvShape.of(
+        (1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1))), ctypes.c_float(1.0), None)
+    assert st == ext.I8C_ERR_INVALID_ARG

@@ -1,0 +1,116 @@
+"""GPU tests of the boundary itself: layout kernels, the one-shot entry
+points, host-buffer runs, alignment errors and the bounded-wait failure path."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available()
+    return torch
+
+
+def test_pack_unpack_activations(torch_cuda):
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    N, C, H, W = 3, 96, 7, 5
+    a = synth.uniform_int8(3, N * C * H * W, -128, 127).reshape(N, C, H, W)
+    src = torch.from_numpy(a).cuda()
+    dst = torch.empty_like(src)
+    ext.i8c_pack_nchw_to_ncxhwx32(src, dst, N, C, H, W)
+    assert np.array_equal(dst.cpu().numpy().reshape(-1), oracle.nchw_to_ncxhwx32(a).reshape(-1))
+    back = torch.empty_like(src)
+    ext.i8c_unpack_ncxhwx32_to_nchw(dst, back, N, C, H, W)
+    assert np.array_equal(back.cpu().numpy(), a)
+
+
+def test_pack_unpack_filters(torch_cuda):
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    K, C, R, S = 64, 64, 5, 3
+    f = synth.uniform_int8(4, K * C * R * S, -128, 127).reshape(K, C, R, S)
+    src = torch.from_numpy(f).cuda()
+    dst = torch.empty_like(src)
+    ext.i8c_pack_kcrs_to_cxrskx32(src, dst, K, C, R, S)
+    assert np.array_equal(dst.cpu().numpy().reshape(-1), oracle.kcrs_to_cxrskx32(f).reshape(-1))
+    back = torch.empty_like(src)
+    ext.i8c_unpack_cxrskx32_to_kcrs(dst, back, K, C, R, S)
+    assert np.array_equal(back.cpu().numpy(), f)
+
+
+def test_one_shot_entry_points(torch_cuda):
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 20, 20, 128, 3, 3, 1, 1, 1, 1, 1, 1)
+    x = synth.uniform_int8(10, 2 * 64 * 400, -128, 127).reshape(2, 64, 20, 20)
+    f = synth.uniform_int8(11, 128 * 64 * 9, -128, 127).reshape(128, 64, 3, 3)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -11)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    y = ext.conv2d_fprop(xd, fd, shape, 2.0 ** -11)
+    acc = torch.empty(y.shape, dtype=torch.int32, device="cuda")
+    ext.i8c_conv2d_fprop_acc(xd, fd, acc, shape)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), y_ref)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref.astype(np.int32))
+
+
+def test_host_buffer_run(torch_cuda):
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 32, 24, 24, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x = synth.uniform_int8(12, 2 * 32 * 576, -128, 127).reshape(2, 32, 24, 24)
+    f = synth.uniform_int8(13, 64 * 32 * 9, -128, 127).reshape(64, 32, 3, 3)
+    y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -9)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xh = torch.from_numpy(xp).pin_memory()
+    fh = torch.from_numpy(fp).pin_memory()
+    yh = torch.empty(y_ref.size, dtype=torch.int8).pin_memory()
+    plan = ext.Plan(shape, host_staging=True)
+    stream = torch.cuda.current_stream()
+    plan.run_host(xh, fh, yh, 2.0 ** -9, stream)
+    stream.synchronize()
+    assert plan.status() == 0
+    assert np.array_equal(yh.numpy(), y_ref.reshape(-1))
+
+
+def test_misaligned_pointer_rejected(torch_cuda):
+    import ctypes
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (1, 32, 8, 8, 32, 3, 3, 1, 1, 1, 1, 1, 1)
+    x = torch.zeros(32 * 64 + 16, dtype=torch.int8, device="cuda")
+    f = torch.zeros(32 * 32 * 9, dtype=torch.int8, device="cuda")
+    y = torch.zeros(32 * 64, dtype=torch.int8, device="cuda")
+    plan = ext.Plan(shape)
+    st = ext.lib.i8c_plan_run(plan.handle, x.data_ptr() + 1, f.data_ptr(), y.data_ptr(), ctypes.c_float(1.0),
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == ext.I8C_ERR_MISALIGNED
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
+    """A producer skips one arrival on purpose: the MMA warp's wait runs out
+    after 20 ms, every role stops, the kernel returns and the plan reports
+    I8C_ERR_TIMEOUT.  The same context then runs a correct convolution."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x = synth.uniform_int8(14, 2 * 64 * 256, -128, 127).reshape(2, 64, 16, 16)
+    f = synth.uniform_int8(15, 64 * 64 * 9, -128, 127).reshape(64, 64, 3, 3)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
+    bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE)
+    bad.run(xd, fd, y, 1.0)
+    assert bad.status() == ext.I8C_ERR_TIMEOUT
+    assert bad.status() == ext.I8C_OK          # the status word was cleared
+    y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    y2, _ = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, want_acc=False)
+    assert np.array_equal(y2, y_ref)

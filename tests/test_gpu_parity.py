@@ -1,0 +1,121 @@
+"""GPU parity: the tcgen05 implicit-GEMM path against the CPU oracle, bit for
+bit, on seeded inputs -- int32 accumulators and int8 outputs.  Small shapes
+span several tiles and ragged tails and are compared element by element;
+the five full-size workloads are compared on sampled outputs plus, at every
+output element, the property y == epilogue(acc)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw
+    (1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1),     # the 16x16 single-image layer, two tiles
+    (2, 64, 13, 11, 64, 3, 3, 1, 1, 1, 1, 1, 1),     # ragged last tile (286 rows)
+    (3, 32, 30, 30, 96, 5, 9, 2, 4, 1, 1, 2, 3),     # dilated 5x9, K=96 inside a 128-wide tile
+    (2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1),   # stride 2, two exact-fp32 chunks
+    (1, 64, 12, 12, 512, 3, 3, 1, 1, 1, 1, 1, 1),    # two N-tiles of 256
+    (1, 512, 6, 6, 64, 3, 3, 1, 1, 1, 1, 1, 1),      # 4608-long reduction, five chunks
+    (4, 64, 10, 10, 32, 1, 1, 0, 0, 1, 1, 1, 1),     # 1x1 filter
+    (2, 32, 17, 19, 64, 3, 2, 2, 1, 3, 2, 2, 3),     # mixed stride / dilation / padding per axis
+    (2, 32, 3, 3, 32, 3, 3, 0, 0, 1, 1, 1, 1),       # 1x1 output
+    (1, 32, 1, 1, 32, 3, 3, 1, 1, 1, 1, 1, 1),       # 1x1 input, all but the centre tap padded
+    (5, 96, 9, 7, 160, 2, 3, 0, 1, 1, 2, 2, 1),      # K=160 -> 256-wide tile, C=96
+]
+
+
+def _data(shape, seed, lo=-128, hi=127):
+    N, C, H, W, K, R, S = shape[:7]
+    x = synth.uniform_int8(seed, N * C * H * W, lo, hi).reshape(N, C, H, W)
+    f = synth.uniform_int8(seed + 1, K * C * R * S, lo, hi).reshape(K, C, R, S)
+    return x, f
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("alpha", [2.0 ** -9, 1.0 / 3.0])
+def test_small_shapes_exact(shape, alpha):
+    x, f = _data(shape, 1000 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, alpha)
+    y, acc = gpu_util.gpu_run(shape, x, f, alpha)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+@pytest.mark.parametrize("opts", [
+    dict(num_ctas=1), dict(num_ctas=3), dict(max_chunk_slices=1), dict(max_chunk_slices=5),
+    dict(block_n=32), dict(block_n=64), dict(block_n=128), dict(block_n=256, num_ctas=2),
+], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
+def test_plan_options_exact(opts):
+    shape = (2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1)
+    x, f = _data(shape, 77)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **opts)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+def test_extreme_magnitudes_exact():
+    """Every product near 2^14 and odd sums just below 2^24 per chunk: the
+    fp32 tensor-core accumulation must stay exact chunk by chunk."""
+    shape = (1, 1024, 6, 6, 64, 3, 3, 1, 1, 1, 1, 1, 1)   # 288 slices -> 9 chunks of 32
+    N, C, H, W, K, R, S = shape[:7]
+    x = np.full((N, C, H, W), -128, np.int8)
+    f = np.full((K, C, R, S), -128, np.int8)
+    rng = np.random.default_rng(9)
+    x.reshape(-1)[rng.choice(x.size, 97, replace=False)] = -127
+    f.reshape(-1)[rng.choice(f.size, 501, replace=False)] = -127
+    f[3] = 127                                             # one channel of large negative sums
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -20)
+    assert np.abs(acc_ref).max() > 2 ** 27
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -20)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+def test_saturation_and_ties():
+    shape = (1, 32, 8, 8, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x, f = _data(shape, 5)
+    for alpha in (1.0, 2.0 ** -9, 2.0 ** -14, 1e30, -1.0, 0.0):
+        y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, alpha)
+        y, _ = gpu_util.gpu_run(shape, x, f, alpha, want_acc=False)
+        assert np.array_equal(y, y_ref), alpha
+
+
+def test_deterministic_repeat():
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = (4, 256, 14, 14, 256, 3, 3, 1, 1, 1, 1, 1, 1)
+    x, f = _data(shape, 21)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    plan = ext.Plan(shape)
+    outs = []
+    for _ in range(3):
+        y = torch.empty(4 * 256 * 14 * 14, dtype=torch.int8, device="cuda")
+        plan.run(xd, fd, y, 2.0 ** -12)
+        outs.append(y.cpu().numpy())
+    assert plan.status() == 0
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
+@pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
+def test_full_size_workloads(wl):
+    """The five workloads at full size, in the launch configuration the
+    benchmark times: sampled outputs against the oracle point by point, and
+    y == epilogue(acc) at every output element."""
+    shape = wl.shape_tuple()
+    x = wl.activations_nchw()
+    f = wl.filters_kcrs()
+    y, acc = gpu_util.gpu_run(shape, x, f, wl.alpha)
+    orc = oracle.Oracle()
+    P, Q = orc.out_size(shape)
+    pts = gpu_util.sample_points(shape, P, Q, 3000, seed=wl.x_seed)
+    ref = orc.conv_acc_points(x, f, shape, pts)
+    idx = gpu_util.packed_index(shape, P, Q, pts)
+    assert np.array_equal(acc.reshape(-1)[idx].astype(np.int64), ref)
+    assert np.array_equal(y.reshape(-1)[idx], orc.requantize(ref, wl.alpha))
+    assert np.array_equal(y.reshape(-1), orc.requantize(acc.reshape(-1).astype(np.int64), wl.alpha))
