@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def ext():
-    from int8_implicit_gemm_gb300 import build_lib
-    build_lib.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import int8_implicit_gemm_gb300 as ext
     return ext
 
