@@ -129,6 +129,30 @@ i8c_status i8c_conv2d_fprop(const int8_t* x, const int8_t* f, int8_t* y, const i
 i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, const i8c_conv_shape* shape,
                                 cudaStream_t stream);
 
+/* Same convolution and arguments as i8c_conv2d_fprop, for callers that must
+ * not allocate device memory.  The pages have no counterpart to this entry
+ * point; it exists for code whose device memory is owned by someone else
+ * (a framework's caching allocator or a fixed memory-pool budget), for
+ * latency-critical paths where cudaMalloc's implicit synchronisation is not
+ * acceptable, and for plug-ins that may use only the buffers they are given.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  Its scratch
+ * (the fp16 copy of the filter and a status word) lives in one 8 MiB static
+ * device array inside the library, which every GPU that loads the library
+ * keeps until the process exits.  Limit: K*C*R*S <= 4,194,176 filter
+ * elements; larger filters return I8C_ERR_UNSUPPORTED and nothing is
+ * enqueued.  Other argument errors are as for i8c_conv2d_fprop.
+ *
+ * The first call on a device looks up the array's device address and sets up
+ * the kernels for that device (host-side queries, no allocation); make that
+ * first call before any stream capture.  All calls share the one array and
+ * each call overwrites it, so calls that may overlap on the GPU (different
+ * streams, or different host threads) race and must be serialised by the
+ * caller.  A device-side wait that runs out is recorded only in the shared
+ * status word and is not reported back; the output is then undefined. */
+i8c_status i8c_conv2d_fprop_noalloc(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape,
+                                    float alpha, cudaStream_t stream);
+
 /* Compile-once / run-many (host-latency tutorial, "Compiling once"): a plan
  * holds the validated shape, the tile schedule, the filter staging buffer
  * and a device status word, allocated on the current device.  `opts` may be

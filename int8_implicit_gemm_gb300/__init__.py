@@ -84,6 +84,7 @@ def _load() -> ctypes.CDLL:
         "i8c_supported": [S],
         "i8c_conv2d_fprop": [P, P, P, S, F, P],
         "i8c_conv2d_fprop_acc": [P, P, P, S, P],
+        "i8c_conv2d_fprop_noalloc": [P, P, P, S, F, P],
         "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
         "i8c_plan_run": [P, P, P, P, F, P],
         "i8c_plan_run_acc": [P, P, P, P, P],
@@ -160,6 +161,13 @@ def i8c_conv2d_fprop(x, f, y, shape, alpha: float, stream=None) -> None:
 def i8c_conv2d_fprop_acc(x, f, acc, shape, stream=None) -> None:
     _check(lib.i8c_conv2d_fprop_acc(_ptr(x), _ptr(f), _ptr(acc), ctypes.byref(ConvShape.of(shape)),
                                     _stream(stream)), "i8c_conv2d_fprop_acc")
+
+
+def i8c_conv2d_fprop_noalloc(x, f, y, shape, alpha: float, stream=None) -> None:
+    """The convolution without any device allocation: scratch lives in the
+    library's fixed static device array (see include/i8conv.h)."""
+    _check(lib.i8c_conv2d_fprop_noalloc(_ptr(x), _ptr(f), _ptr(y), ctypes.byref(ConvShape.of(shape)),
+                                        ctypes.c_float(alpha), _stream(stream)), "i8c_conv2d_fprop_noalloc")
 
 
 def i8c_pack_nchw_to_ncxhwx32(src, dst, N, C, H, W, stream=None) -> None:
