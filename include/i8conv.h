@@ -76,12 +76,17 @@ typedef struct {
   int32_t timing_events;     /* > 0: bracket each convolution kernel with CUDA events (keeps
                                 the last timing_events launches) for i8c_plan_kernel_time;
                                 for benchmarks, not for use under graph capture               */
+  int32_t kernel_variant;    /* 0 = auto, 1 = per-tap gather kernel, 2 = halo kernel (16x8
+                                output patches; I8C_ERR_UNSUPPORTED if its halo does not fit) */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so
  * the MMA warp's bounded wait runs out and the kernel reports
  * I8C_ERR_TIMEOUT without faulting or hanging.  Used by the failure tests. */
 #define I8C_DEBUG_SKIP_FIRST_ARRIVE 1
+/* debug_flags: record clock64 timestamps of the pipeline waits of CTA 0 in a
+ * plan-owned buffer, read back with i8c_plan_trace (pipeline analysis). */
+#define I8C_DEBUG_TRACE 2
 
 typedef struct i8c_plan i8c_plan;
 
@@ -100,6 +105,7 @@ typedef struct {
   int32_t kernels_per_run;   /* kernel launches enqueued by one i8c_plan_run   */
   int64_t ops;               /* 2*N*K*P*Q*C*R*S                                 */
   int64_t workspace_bytes;   /* device memory owned by the plan                */
+  int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel     */
 } i8c_plan_info;
 
 /* Output height P and width Q for a shape (formula above).  Returns
@@ -192,6 +198,12 @@ i8c_status i8c_plan_get_info(const i8c_plan* plan, i8c_plan_info* info);
  * since the previous call and their count, and starts a new window.  Only
  * the last timing_events launches are kept. */
 i8c_status i8c_plan_kernel_time(const i8c_plan* plan, double* total_ms, int64_t* launches);
+
+/* With I8C_DEBUG_TRACE: copies up to `count` entries of the last run's trace
+ * (synchronous): entry (role*4 + event)*512 + i is the SM clock at event
+ * `event` of step i of role 0 MMA issuer, 1 filter TMA, 2 activation
+ * producer, 3 epilogue; 0 where not reached. */
+i8c_status i8c_plan_trace(const i8c_plan* plan, long long* out, int64_t count);
 
 /* Frees the plan's device memory.  Synchronises the device first. */
 i8c_status i8c_plan_destroy(i8c_plan* plan);

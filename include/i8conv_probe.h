@@ -1,0 +1,41 @@
+/*
+ * i8conv engine probes -- microbenchmarks of the tensor-core engine the
+ * convolution kernels are built on, for choosing tile shapes and for the
+ * roofline denominator.  Not part of the convolution path.  The pages have no
+ * counterpart; they name only the Ampere 16x8x32 integer MMA of the CUTLASS
+ * configuration in the "int8 fprop2d kernel with NCxHWx interleaved layout"
+ * issue, which sm_103a's tcgen05 tensor cores do not offer.
+ */
+#ifndef I8CONV_PROBE_H_
+#define I8CONV_PROBE_H_
+
+#include "i8conv.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One CTA per SM (num_ctas CTAs); in each, one thread issues `iters`
+ * tcgen05.mma.cta_group::1.kind::f16 instructions (M = 128, N = n in
+ * {32, 64, 128, 256}, K = 16, fp32 accumulate) back to back on zero operands
+ * resident in shared memory.  a_swizzled selects A's layout: 1 = 64-byte
+ * swizzle; 0 = no swizzle with contiguous 8-row core matrices; 2 = no swizzle
+ * with 8-row groups 160 bytes apart (a 10-position halo row); 3 = as 2 but
+ * starting 16 bytes into the buffer (a filter tap shifted by one column).
+ * B is always 64-byte swizzled.  loop_mode 0 issues bare MMAs; 1-3 issue them
+ * in the convolution's per-K-slice pattern (pairs of MMAs with the A start
+ * from a shared-memory table; 2 adds a completed-barrier check every 4
+ * slices, 3 also a commit every 4 slices).
+ *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles to issue,
+ *           SM cycles until all MMAs completed, 1 if the completion wait
+ *           succeeded (bounded at 2 s)
+ *   elapsed_ms: host float, kernel duration from CUDA events on `stream`.
+ * Synchronises `stream`. */
+i8c_status i8c_probe_mma_f16(int32_t n, int32_t a_swizzled, int32_t loop_mode, int32_t num_ctas, int32_t iters,
+                             long long* cycles, float* elapsed_ms, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I8CONV_PROBE_H_ */

@@ -26,6 +26,7 @@ I8C_ERR_CUDA = 5
 I8C_ERR_TIMEOUT = 6
 I8C_ERR_NO_DEVICE = 7
 I8C_DEBUG_SKIP_FIRST_ARRIVE = 1
+I8C_DEBUG_TRACE = 2
 
 
 class I8ConvError(RuntimeError):
@@ -55,7 +56,7 @@ class Options(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("max_chunk_slices", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
                 ("host_staging", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
-                ("timing_events", ctypes.c_int32)]
+                ("timing_events", ctypes.c_int32), ("kernel_variant", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -66,7 +67,7 @@ class PlanInfo(ctypes.Structure):
                 ("num_chunks", ctypes.c_int32), ("chunk_slices", ctypes.c_int32),
                 ("acc_buffers", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("kernels_per_run", ctypes.c_int32), ("ops", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("kernel_variant", ctypes.c_int32)]
 
     def asdict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -92,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "i8c_plan_status": [P, P],
         "i8c_plan_get_info": [P, ctypes.POINTER(PlanInfo)],
         "i8c_plan_kernel_time": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
+        "i8c_plan_trace": [P, P, I64],
         "i8c_plan_destroy": [P],
         "i8c_pack_nchw_to_ncxhwx32": [P, P, I32, I32, I32, I32, P],
         "i8c_unpack_ncxhwx32_to_nchw": [P, P, I32, I32, I32, I32, P],
@@ -102,6 +104,8 @@ def _load() -> ctypes.CDLL:
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    lib.i8c_probe_mma_f16.argtypes = [I32, I32, I32, I32, I32, P, ctypes.POINTER(F), P]
+    lib.i8c_probe_mma_f16.restype = ctypes.c_int
     lib.i8c_status_string.argtypes = [ctypes.c_int]
     lib.i8c_status_string.restype = ctypes.c_char_p
     lib.i8c_launch_count.argtypes = []
@@ -186,14 +190,25 @@ def i8c_unpack_cxrskx32_to_kcrs(src, dst, K, C, R, S, stream=None) -> None:
     _check(lib.i8c_unpack_cxrskx32_to_kcrs(_ptr(src), _ptr(dst), K, C, R, S, _stream(stream)), "unpack")
 
 
+def i8c_probe_mma_f16(n: int, a_swizzled: int, num_ctas: int, iters: int, loop_mode: int = 0, stream=None):
+    """Tensor-core probe (include/i8conv_probe.h): returns (per-CTA cycles array
+    [num_ctas, 3] = issue cycles, completion cycles, ok flag; elapsed ms)."""
+    import torch
+    buf = torch.zeros(3 * num_ctas, dtype=torch.int64, device="cuda")
+    ms = ctypes.c_float()
+    _check(lib.i8c_probe_mma_f16(n, int(a_swizzled), loop_mode, num_ctas, iters, buf.data_ptr(), ctypes.byref(ms),
+                                 _stream(stream)), "i8c_probe_mma_f16")
+    return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
+
+
 class Plan:
     """A validated convolution plan on the current CUDA device (i8c_plan_*)."""
 
     def __init__(self, shape, block_n=0, num_ctas=0, max_chunk_slices=0, wait_timeout_us=0,
-                 host_staging=False, debug_flags=0, timing_events=0):
+                 host_staging=False, debug_flags=0, timing_events=0, kernel_variant=0):
         self.shape = ConvShape.of(shape)
         opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(bool(host_staging)), debug_flags,
-                       timing_events)
+                       timing_events, kernel_variant)
         h = ctypes.c_void_p()
         _check(lib.i8c_plan_create(ctypes.byref(self.shape), ctypes.byref(opts), ctypes.byref(h)),
                "i8c_plan_create")
@@ -218,6 +233,13 @@ class Plan:
         ms, n = ctypes.c_double(), ctypes.c_int64()
         _check(lib.i8c_plan_kernel_time(self.handle, ctypes.byref(ms), ctypes.byref(n)), "i8c_plan_kernel_time")
         return ms.value, n.value
+
+    def trace(self):
+        """The clock64 trace of CTA 0 (plan created with I8C_DEBUG_TRACE), shape (4 roles, 4 events, 512)."""
+        import numpy as np
+        out = np.zeros(16 * 512, dtype=np.int64)
+        _check(lib.i8c_plan_trace(self.handle, out.ctypes.data, out.size), "i8c_plan_trace")
+        return out.reshape(4, 4, 512)
 
     def status(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status word."""

@@ -1,0 +1,416 @@
+// INT8 NCxHWx<32> Conv2d fprop on the sm_103a tensor cores, halo variant.
+//
+// Same GEMM view and exact fp16/fp32-chunk arithmetic as conv_fprop_tc.cuh,
+// but the 128 GEMM rows of a tile are a 16 x 8 patch of output pixels of one
+// image (16 output rows, 8 consecutive output columns).  For one 32-channel
+// block cb the producers load the input region every tap of the patch needs
+// -- the halo, (15*sh + (R-1)*dh + 1) rows x (7*sw + (S-1)*dw + 1) columns --
+// once, convert it to fp16 once, and store it as four 8-channel planes in the
+// canonical no-swizzle K-major layout with one 16-byte entry per pixel.  The
+// A operand of filter tap (r, s) is then a shifted view of that halo: eight
+// consecutive output columns are eight consecutive 16-byte entries (a core
+// matrix), consecutive output rows are sh halo rows apart (the descriptor's
+// stride), and the tap offset moves the start address by r*dh rows and
+// s*dw columns.  Each input vector is converted once per patch instead of
+// once per tap.  Column strides > 1 are handled by storing the halo columns
+// phase by phase (all columns c with c % sw == 0 first, then 1, ...), so the
+// eight columns of a core matrix stay adjacent.
+//
+// Warp roles (384 threads) as in the gather kernel: warp 0 MMA issuer and
+// TMEM owner, warp 1 filter TMA, warps 4-7 halo producers, warps 8-11
+// epilogue.  All waits are bounded.
+#pragma once
+
+#include "conv_fprop_tc.cuh"
+
+namespace i8c {
+
+struct HaloParams {
+  ConvParams c;
+  int TPH, TQW;             // patches per image along P (16 rows each) and Q (8 columns each)
+  int HR, CW;               // halo rows, halo positions per row
+  uint32_t plane_bytes;     // one 8-channel plane: HR*CW*16 (rounded up to 128)
+  uint32_t halo_bytes;      // one halo stage: 4 planes
+  uint32_t stg_bytes;       // one int8 staging slot: HR*CW*32 (rounded up to 128)
+  int nstg;                 // int8 staging slots: 2 or 3
+  int nbs;                  // filter pipeline stages (<= kMaxBStages)
+  int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
+  uint32_t off_stg, off_b, off_bar;
+  int phase_off[9];         // first position of column phase f (f < sw); phase_off[sw] = CW
+};
+
+
+constexpr int kMaxBStages = 16;
+constexpr int kHaloBarBytes = 512;
+
+struct PatchTile {
+  int n, p0, q0, nt;
+};
+
+__device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp) {
+  const int nt = tile % hp.c.num_n_tiles;
+  int rest = tile / hp.c.num_n_tiles;
+  const int qt = rest % hp.TQW;
+  rest /= hp.TQW;
+  const int pt = rest % hp.TPH;
+  return {rest / hp.TPH, pt * 16, qt * 8, nt};
+}
+
+template <int BN>
+__global__ void __launch_bounds__(384, 1)
+    conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+  const ConvParams& p = hp.c;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + hp.off_bar);
+  uint64_t* b_full = bars;
+  uint64_t* b_empty = bars + kMaxBStages;
+  uint64_t* h_full = bars + 2 * kMaxBStages;
+  uint64_t* h_empty = h_full + 2;
+  uint64_t* acc_full = h_full + 4;
+  uint64_t* acc_empty = h_full + 6;
+  uint64_t* drain = h_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 9);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 9) + 1;
+
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
+  const int lane = threadIdx.x & 31;
+  const int nbs = hp.nbs;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nbs; ++i) {
+      ptx::mbar_init(&b_full[i], 1);
+      ptx::mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&h_full[i], 128);
+      ptx::mbar_init(&h_empty[i], 1);
+      ptx::mbar_init(&acc_full[i], 1);
+      ptx::mbar_init(&acc_empty[i], 128);
+    }
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1 && lane == 0) ptx::prefetch_tensormap(&tmap_f);
+  if (warp == 0) {
+    ptx::tmem_alloc(tmem_slot, p.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t nb = static_cast<uint32_t>(p.acc_buffers);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs the loop in uniform control flow so that every
+    // descriptor is computed from loop counters and kernel parameters in
+    // uniform registers; one elected lane issues each MMA and commit.
+    constexpr uint32_t idesc = ptx::idesc_f16_f32(128, BN);
+    const uint32_t sbo = static_cast<uint32_t>(p.stride_h * hp.CW * 16);
+    const uint32_t lbo = hp.plane_bytes;
+    const uint64_t a_desc0 = ptx::smem_desc_noswizzle_kmajor(0, lbo, sbo);
+    const uint64_t b_desc0 = ptx::smem_desc_sw64_kmajor(0);
+    // start-address fields (16-byte units)
+    const uint32_t h_lo = ptx::smem_addr(smem) >> 4;
+    const uint32_t b_lo = ptx::smem_addr(smem + hp.off_b) >> 4;
+    const uint32_t halo_lo = hp.halo_bytes >> 4;
+    const uint32_t chunk2_lo = (2 * lbo) >> 4;
+    const int G = hp.bgroup;
+    const uint32_t slice_lo = static_cast<uint32_t>(BN * 64) >> 4;
+    const uint32_t stage_lo = static_cast<uint32_t>(G) * slice_lo;
+    // tap (r, s) -> halo position r*dh*CW + phase_off(f) + idx with
+    // s*dw = idx*sw + f; phase_off(f) = f*(CW/sw) + min(f, CW%sw)
+    const int row_step = p.dil_h * hp.CW;
+    const int dw_div = p.dil_w / p.stride_w, dw_mod = p.dil_w % p.stride_w;
+    const int cw_q = hp.CW / p.stride_w, cw_r = hp.CW % p.stride_w;
+    // Loop nest: channel block (one halo) -> filter row -> run of G taps of
+    // that row (one filter stage; G divides S).  Waits, releases and
+    // accumulator switches happen only at run boundaries (chunk lengths are
+    // multiples of G); inside a run each K-slice is two MMAs and affine
+    // address updates, with no data-dependent branches.
+    uint32_t u = 0, hseq = 0, st = 0, bph = 0, g = 0;
+    bool ok = true;
+    if (lane == 0) trace_mark(p, 0, 0, 0);
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      int kk = 0, next_chunk = 0;
+      uint32_t buf = 0, d_tmem = tmem_base;
+      uint32_t acc_flag = 0;  // 0 for the first MMA of a chunk, then 1
+      for (int cb = 0; ok && cb < p.CB; ++cb) {
+        if (!__all_sync(0xffffffffu,
+                        ptx::mbar_wait(&h_full[hseq & 1u], (hseq >> 1) & 1u, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const uint32_t h_stage = h_lo + (hseq & 1u) * halo_lo;
+        int rowpos = 0;
+        for (int r = 0; ok && r < p.R; ++r, rowpos += row_step) {
+          int fph = 0, idx = 0;  // column phase and index of tap s = 0 of this row
+          for (int sb = 0; sb < p.S; sb += G) {
+            if (kk == next_chunk) {
+              // a new exact-fp32 chunk: hand the previous accumulator to the
+              // epilogue and take the next buffer
+              if (kk != 0) {
+                if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
+                __syncwarp();
+                ++u;
+              }
+              buf = nb == 1 ? 0u : (u & 1u);
+              const uint32_t aph = nb == 1 ? (u & 1u) : ((u >> 1) & 1u);
+              if (!__all_sync(0xffffffffu,
+                              ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, p.timeout_ns, abort_flag))) {
+                ok = false;
+                break;
+              }
+              d_tmem = tmem_base + buf * BN;
+              next_chunk = kk + p.chunk_slices;
+              acc_flag = 0;
+            }
+            if (lane == 0) trace_mark(p, 0, 1, g / G + 1);
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_full[st], bph, p.timeout_ns, abort_flag))) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            if (lane == 0) trace_mark(p, 0, 2, g / G);
+            uint32_t b_cur = b_lo + st * stage_lo;
+            for (int t = 0; t < G; ++t) {
+              const uint32_t a_cur = h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx);
+              const uint64_t ad0 = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
+              const uint64_t ad1 = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
+              const uint64_t bd = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
+              if (ptx::elect_one()) {
+                ptx::mma_f16_ss(d_tmem, ad0, bd, idesc, acc_flag);
+                ptx::mma_f16_ss(d_tmem, ad1, bd + 2, idesc, 1u);
+              }
+              __syncwarp();
+              acc_flag = 1;
+              b_cur += slice_lo;
+              fph += dw_mod;
+              const int carry = fph >= p.stride_w ? 1 : 0;
+              fph -= carry * p.stride_w;
+              idx += dw_div + carry;
+            }
+            if (ptx::elect_one()) ptx::mma_commit(&b_empty[st]);
+            __syncwarp();
+            if (lane == 0) trace_mark(p, 0, 3, g / G);
+            if (++st == static_cast<uint32_t>(nbs)) {
+              st = 0;
+              bph ^= 1u;
+            }
+            kk += G;
+            g += G;
+          }
+        }
+        if (!ok) break;
+        if (ptx::elect_one()) ptx::mma_commit(&h_empty[hseq & 1u]);
+        __syncwarp();
+        ++hseq;
+      }
+      if (!ok) break;
+      if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
+      __syncwarp();
+      ++u;
+    }
+    if (lane == 0) {
+      trace_mark(p, 0, 0, 1);
+      if (p.trace != nullptr && blockIdx.x == 0) p.trace[4 * kTraceSlots] = g;
+    }
+    if (!ok && lane == 0) raise_timeout(p, abort_flag);
+    // every MMA issued by this warp has completed before TMEM is freed
+    if (ptx::elect_one()) ptx::mma_commit(drain);
+    __syncwarp();
+    if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ filter TMA producer
+    const int G = hp.bgroup;
+    const uint32_t stage_bytes = static_cast<uint32_t>(G * BN * 64);
+    uint32_t g = 0, st = 0, bph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const int n0 = (tile % p.num_n_tiles) * BN;
+      for (int kk = 0; kk < p.num_slices; kk += G, ++g) {
+        if (lane == 0) trace_mark(p, 1, 0, g);
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_empty[st], bph ^ 1u, p.timeout_ns, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) trace_mark(p, 1, 1, g);
+        // G consecutive K-slices; slices past the end of the filter read as zeros
+        if (ptx::elect_one()) {
+          ptx::mbar_arrive_expect_tx(&b_full[st], stage_bytes);
+          ptx::tma_load_3d(smem + hp.off_b + st * stage_bytes, &tmap_f, &b_full[st], 0, n0, kk);
+        }
+        __syncwarp();
+        if (++st == static_cast<uint32_t>(nbs)) {
+          st = 0;
+          bph ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_timeout(p, abort_flag);
+    // wait for the loads still in flight (at most one per stage)
+    const uint32_t first = g > static_cast<uint32_t>(nbs) ? g - nbs : 0u;
+    for (uint32_t i = first; i < g; ++i) {
+      if (!ptx::mbar_wait(&b_full[i % nbs], (i / nbs) & 1u, p.timeout_ns, nullptr)) {
+        if (lane == 0) raise_timeout(p, abort_flag);
+        break;
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ halo producers
+    const int pt = threadIdx.x - 128;
+    const int items = 2 * hp.HR * hp.CW;  // (position, 16-byte half) pairs
+    const int HW32 = p.H * p.W * 32;
+    const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
+    int l_tile = blockIdx.x, l_cb = 0;
+
+    auto issue_load = [&](uint32_t slot) {
+      if (l_tile < p.num_tiles) {
+        const PatchTile t = decode_patch(l_tile, hp);
+        const int hb0 = t.p0 * p.stride_h - p.pad_h;
+        const int wb0 = t.q0 * p.stride_w - p.pad_w;
+        const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + l_cb * HW32;
+        const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
+        for (int it = pt; it < items; it += 128) {
+          const int e = it >> 1, h = it & 1;
+          const int b = e / hp.CW;
+          const int pos = e - b * hp.CW;
+          int f = p.stride_w - 1;
+          while (pos < hp.phase_off[f]) --f;
+          const int c = (pos - hp.phase_off[f]) * p.stride_w + f;
+          const int hh = hb0 + b, ww = wb0 + c;
+          const bool in = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
+          const int8_t* src = in ? img + (hh * p.W + ww) * 32 + h * 16 : p.x;
+          ptx::cp_async_16_ca(dst0 + e * 32 + h * 16, src, in ? 16u : 0u);
+        }
+        if (++l_cb == p.CB) {
+          l_cb = 0;
+          l_tile += gridDim.x;
+        }
+      }
+      ptx::cp_async_commit();
+    };
+
+    const uint32_t total = static_cast<uint32_t>((p.num_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) /
+                                                 gridDim.x) *
+                           static_cast<uint32_t>(p.CB);
+    const int nstg = hp.nstg;
+    for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
+    bool ok = true;
+    for (uint32_t s = 0; s < total; ++s) {
+      if (pt == 0) trace_mark(p, 2, 0, s);
+      issue_load((s + nstg - 1) % nstg);
+      if (nstg == 3) ptx::cp_async_wait<2>();
+      else ptx::cp_async_wait<1>();
+      if (pt == 0) trace_mark(p, 2, 1, s);
+      const uint32_t hs = s & 1u;
+      if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (pt == 0) trace_mark(p, 2, 2, s);
+      const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
+      uint8_t* halo = smem + hs * hp.halo_bytes;
+      for (int it = pt; it < items; it += 128) {
+        const int e = it >> 1, h = it & 1;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16);
+        uint4 c0, c1;
+        i8x4_to_f16x4(v.x, c0.x, c0.y);
+        i8x4_to_f16x4(v.y, c0.z, c0.w);
+        i8x4_to_f16x4(v.z, c1.x, c1.y);
+        i8x4_to_f16x4(v.w, c1.z, c1.w);
+        *reinterpret_cast<uint4*>(halo + (2 * h) * hp.plane_bytes + e * 16) = c0;
+        *reinterpret_cast<uint4*>(halo + (2 * h + 1) * hp.plane_bytes + e * 16) = c1;
+      }
+      ptx::fence_proxy_async_smem();
+      if (pt == 0) trace_mark(p, 2, 3, s);
+      if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
+    }
+    if (!ok) raise_timeout(p, abort_flag);
+    ptx::cp_async_wait_all();
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3;
+    const int row = 32 * qd + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
+    uint32_t u = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const PatchTile t = decode_patch(tile, hp);
+      const int pp = t.p0 + (row >> 3);
+      const int qq = t.q0 + (row & 7);
+      const bool valid = pp < p.P && qq < p.Q;
+      for (int c = 0; c < p.num_chunks; ++c, ++u) {
+        const uint32_t buf = u % nb;
+        if (row == 0) trace_mark(p, 3, 0, u);
+        const bool got = ptx::mbar_wait(&acc_full[buf], (u / nb) & 1u, p.timeout_ns, abort_flag);
+        if (row == 0) trace_mark(p, 3, 1, u);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t t_acc = tmem_base + lane_addr + buf * BN;
+        const uint32_t t_run = tmem_base + lane_addr + nb * BN;
+        const bool first = c == 0, last = c + 1 == p.num_chunks;
+#pragma unroll 1
+        for (int g32 = 0; g32 < BN / 32; ++g32) {
+          const int k0 = t.nt * BN + g32 * 32;
+          if (k0 >= p.K) break;
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(t_acc + g32 * 32, v);
+          ptx::tmem_wait_ld();
+          int a[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = __float2int_rn(__uint_as_float(v[i]));
+          if (!first) {
+            uint32_t rsum[32];
+            ptx::tmem_ld_32x32b_x32(t_run + g32 * 32, rsum);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] += static_cast<int>(rsum[i]);
+          }
+          if (!last) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = static_cast<uint32_t>(a[i]);
+            ptx::tmem_st_32x32b_x32(t_run + g32 * 32, w);
+          } else if (valid) {
+            const int64_t off = ((static_cast<int64_t>(t.n) * p.KB + (k0 >> 5)) * p.P + pp) * p.Q + qq;
+            if (p.out_mode == 0) {
+              uint32_t o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                o[i] = pack4_s8(requant(a[4 * i], p.alpha), requant(a[4 * i + 1], p.alpha),
+                                requant(a[4 * i + 2], p.alpha), requant(a[4 * i + 3], p.alpha));
+              uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
+              dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+              dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+              int4* dst = reinterpret_cast<int4*>(p.acc + off * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = make_int4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
+            }
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&acc_empty[buf]);
+        if (row == 0) trace_mark(p, 3, 2, u);
+      }
+    }
+    if (!ok) raise_timeout(p, abort_flag);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace i8c

@@ -60,7 +60,17 @@ struct ConvParams {
   uint64_t timeout_ns;
   int out_mode;
   int debug_flags;
+  long long* trace;  // optional clock64 trace of CTA 0 (null = off), kTraceSlots per role
 };
+
+// Trace layout (CTA 0 only): role r, event e, index i ->
+// trace[(r * 4 + e) * kTraceSlots + i].  Roles: 0 MMA, 1 filter TMA,
+// 2 activation producer thread 0, 3 epilogue thread 0.
+constexpr int kTraceSlots = 512;
+__device__ __forceinline__ void trace_mark(const ConvParams& p, int role, int ev, uint32_t i) {
+  if (p.trace != nullptr && blockIdx.x == 0 && i < static_cast<uint32_t>(kTraceSlots))
+    p.trace[(role * 4 + ev) * kTraceSlots + i] = clock64();
+}
 
 constexpr int kStatusTimeout = 6;  // I8C_ERR_TIMEOUT
 

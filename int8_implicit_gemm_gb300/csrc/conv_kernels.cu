@@ -49,4 +49,39 @@ cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& 
   }
 }
 
+template <int BN>
+static cudaError_t halo_prepare_one() {
+  return cudaFuncSetAttribute(conv_fprop_halo_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kMaxDynamicSmem);
+}
+
+cudaError_t conv_halo_prepare(int block_n) {
+  switch (block_n) {
+    case 32: return halo_prepare_one<32>();
+    case 64: return halo_prepare_one<64>();
+    case 128: return halo_prepare_one<128>();
+    case 256: return halo_prepare_one<256>();
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int BN>
+static cudaError_t halo_launch_one(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
+                                   cudaStream_t stream) {
+  conv_fprop_halo_kernel<BN><<<num_ctas, 384, smem, stream>>>(tmap, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_halo(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+                             cudaStream_t stream) {
+  switch (block_n) {
+    case 32: return halo_launch_one<32>(tmap, p, smem_bytes, num_ctas, stream);
+    case 64: return halo_launch_one<64>(tmap, p, smem_bytes, num_ctas, stream);
+    case 128: return halo_launch_one<128>(tmap, p, smem_bytes, num_ctas, stream);
+    case 256: return halo_launch_one<256>(tmap, p, smem_bytes, num_ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace i8c

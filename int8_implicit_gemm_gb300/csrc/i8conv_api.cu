@@ -19,7 +19,9 @@ struct i8c_plan {
   int P, Q;
   int64_t M;
   int device;
+  int kernel_variant;  // 1 = per-tap gather kernel, 2 = halo kernel
   int block_n, num_n_tiles, num_m_tiles, num_tiles, num_ctas;
+  i8c::HaloParams halo;  // geometry and shared-memory layout of the halo kernel
   int num_slices, chunk_slices, num_chunks, acc_buffers;
   uint32_t tmem_cols;
   int smem_bytes;
@@ -27,6 +29,7 @@ struct i8c_plan {
   int debug_flags;
   uint16_t* f16;   // fp16 copy of the filter, [C/32][R][S][K][32]
   int* status;     // device status word
+  long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), 16 * kTraceSlots entries
   CUtensorMap tmap;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
   size_t x_bytes, f_bytes, y_bytes;
@@ -101,6 +104,60 @@ int next_pow2(int v) {
   return p;
 }
 
+double wave_efficiency(int64_t tiles, int ctas) {
+  const int64_t waves = (tiles + ctas - 1) / ctas;
+  return static_cast<double>(tiles) / static_cast<double>(waves * ctas);
+}
+
+// Halo geometry and shared-memory layout for a tile width; returns false when
+// the halo does not fit with at least three filter stages.
+bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, i8c::HaloParams* h, int* smem_bytes) {
+  if (s.stride_w > 8) return false;
+  *h = i8c::HaloParams{};
+  h->TPH = (P + 15) / 16;
+  h->TQW = (Q + 7) / 8;
+  const int64_t HR = 15LL * s.stride_h + static_cast<int64_t>(s.R - 1) * s.dil_h + 1;
+  const int64_t CW = 7LL * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
+  if (HR * CW > 65536) return false;
+  h->HR = static_cast<int>(HR);
+  h->CW = static_cast<int>(CW);
+  const uint32_t pos = static_cast<uint32_t>(HR * CW);
+  h->plane_bytes = (pos * 16 + 127) / 128 * 128;
+  h->halo_bytes = 4 * h->plane_bytes;
+  h->stg_bytes = (pos * 32 + 127) / 128 * 128;
+  int off = 0;
+  for (int f = 0; f < s.stride_w; ++f) {
+    h->phase_off[f] = off;
+    off += static_cast<int>((CW - f + s.stride_w - 1) / s.stride_w);
+  }
+  h->phase_off[s.stride_w] = off;
+  // Filter stages of G K-slices each, G a divisor of S so that a stage is a
+  // run of taps of one filter row: the largest such G with G*BN <= 1024 and at
+  // least three stages in shared memory.
+  const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
+  for (int G = s.S; G >= 1; --G) {
+    if (s.S % G != 0 || G * bn > 1024 || G > 32) continue;
+    for (int nstg = 3; nstg >= 2; --nstg) {
+      const int64_t off_stg = 2LL * h->halo_bytes;
+      const int64_t off_b = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
+      const int64_t room = budget - off_b;
+      const int64_t stage = static_cast<int64_t>(G) * bn * 64;
+      if (room < 3 * stage) continue;
+      int64_t nbs = room / stage;
+      if (nbs > i8c::kMaxBStages) nbs = i8c::kMaxBStages;
+      h->bgroup = G;
+      h->nstg = nstg;
+      h->nbs = static_cast<int>(nbs);
+      h->off_stg = static_cast<uint32_t>(off_stg);
+      h->off_b = static_cast<uint32_t>(off_b);
+      h->off_bar = static_cast<uint32_t>(off_b + nbs * stage);
+      *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
+      return true;
+    }
+  }
+  return false;
+}
+
 void free_plan_memory(i8c_plan* p) {
   for (cudaEvent_t e : p->ev_start) cudaEventDestroy(e);
   for (cudaEvent_t e : p->ev_end) cudaEventDestroy(e);
@@ -108,6 +165,7 @@ void free_plan_memory(i8c_plan* p) {
   p->ev_end.clear();
   if (p->f16) cudaFree(p->f16);
   if (p->status) cudaFree(p->status);
+  if (p->trace) cudaFree(p->trace);
   if (p->stage_x) cudaFree(p->stage_x);
   if (p->stage_f) cudaFree(p->stage_f);
   if (p->stage_y) cudaFree(p->stage_y);
@@ -146,6 +204,7 @@ ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
   p.img_stride = static_cast<int64_t>(s.C) * s.H * s.W;
   p.timeout_ns = pl->timeout_ns;
   p.debug_flags = pl->debug_flags;
+  p.trace = pl->trace;
   return p;
 }
 
@@ -163,7 +222,13 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
     e = cudaEventRecord(pl->ev_start[pl->ev_recorded % nev], stream);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
+  if (pl->kernel_variant == 2) {
+    i8c::HaloParams hp = pl->halo;
+    hp.c = p;
+    e = i8c::launch_conv_halo(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream);
+  } else {
+    e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
+  }
   if (e != cudaSuccess) return from_cuda(e);
   if (nev > 0) {
     e = cudaEventRecord(pl->ev_end[pl->ev_recorded % nev], stream);
@@ -244,7 +309,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536)
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 2)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -265,38 +330,91 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->Q = static_cast<int>(Q);
   p->M = static_cast<int64_t>(s.N) * P * Q;
   p->device = dev;
-  int bn = o.block_n;
-  if (bn == 0) bn = s.K <= 32 ? 32 : (s.K <= 64 ? 64 : (s.K <= 128 ? 128 : 256));
+  const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
+  // Kernel and tile width.  The halo kernel (16x8 output patches) is preferred
+  // whenever its halo fits in shared memory; its tile width is the one with
+  // the best wave efficiency (ties go to the wider tile).
+  int bn = 0, halo_smem = 0;
+  p->kernel_variant = 1;
+  if (o.kernel_variant != 1) {
+    int best_bn = 0;
+    double best = -1.0;
+    for (int cand : {256, 128, 64, 32}) {
+      if (o.block_n != 0 && cand != o.block_n) continue;
+      if (o.block_n == 0 && cand > 32 && cand / 2 >= s.K) continue;
+      i8c::HaloParams h;
+      int sm = 0;
+      if (!halo_layout(s, p->P, p->Q, cand, &h, &sm)) continue;
+      const int nt = (s.K + cand - 1) / cand;
+      const int64_t t = static_cast<int64_t>(s.N) * h.TPH * h.TQW * nt;
+      // narrower tiles give the single MMA-issuing thread less tensor work per K-slice
+      const double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.97 : cand == 64 ? 0.9 : 0.75;
+      const double score =
+          wave_efficiency(t, ctas) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
+      if (score > best * 1.02) {
+        best = score;
+        best_bn = cand;
+      }
+    }
+    if (best_bn != 0) {
+      bn = best_bn;
+      p->kernel_variant = 2;
+      halo_layout(s, p->P, p->Q, bn, &p->halo, &halo_smem);
+    } else if (o.kernel_variant == 2) {
+      delete p;
+      return I8C_ERR_UNSUPPORTED;
+    }
+  }
+  if (bn == 0) {
+    bn = o.block_n;
+    if (bn == 0) bn = s.K <= 32 ? 32 : (s.K <= 64 ? 64 : (s.K <= 128 ? 128 : 256));
+  }
   p->block_n = bn;
   p->num_n_tiles = (s.K + bn - 1) / bn;
-  p->num_m_tiles = static_cast<int>((p->M + 127) / 128);
-  const int64_t tiles = static_cast<int64_t>(p->num_m_tiles) * p->num_n_tiles;
+  const int64_t m_tiles = p->kernel_variant == 2 ? static_cast<int64_t>(s.N) * p->halo.TPH * p->halo.TQW
+                                                 : (p->M + 127) / 128;
+  const int64_t tiles = m_tiles * p->num_n_tiles;
   if (tiles > kMaxI32) {
     delete p;
     return I8C_ERR_OVERFLOW_RISK;
   }
+  p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
-  const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
   p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
   p->num_slices = (s.C / 32) * s.R * s.S;
-  const int max_chunk = o.max_chunk_slices > 0 ? o.max_chunk_slices : 32;
+  int max_chunk = o.max_chunk_slices > 0 ? o.max_chunk_slices : 32;
+  if (p->kernel_variant == 2) {
+    // the halo kernel switches accumulators only between filter stages
+    const int G = p->halo.bgroup;
+    max_chunk = max_chunk / G * G;
+    if (max_chunk < G) max_chunk = G;
+  }
   p->num_chunks = (p->num_slices + max_chunk - 1) / max_chunk;
   p->chunk_slices = (p->num_slices + p->num_chunks - 1) / p->num_chunks;
+  if (p->kernel_variant == 2) {
+    p->chunk_slices = (p->chunk_slices + p->halo.bgroup - 1) / p->halo.bgroup * p->halo.bgroup;
+    p->num_chunks = (p->num_slices + p->chunk_slices - 1) / p->chunk_slices;
+  }
   const int run_cols = p->num_chunks > 1 ? bn : 0;
   p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
   p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
-  p->smem_bytes = i8c::conv_smem_bytes(bn);
+  p->smem_bytes = p->kernel_variant == 2 ? halo_smem : i8c::conv_smem_bytes(bn);
   p->timeout_ns = static_cast<uint64_t>(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
   p->debug_flags = o.debug_flags;
   p->x_bytes = static_cast<size_t>(s.N) * s.C * s.H * s.W;
   p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
   p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
 
-  e = i8c::conv_prepare(bn);
+  e = p->kernel_variant == 2 ? i8c::conv_halo_prepare(bn) : i8c::conv_prepare(bn);
   if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
   p->workspace_bytes = static_cast<int64_t>(p->f_bytes * 2 + sizeof(int));
+  if (e == cudaSuccess && (o.debug_flags & I8C_DEBUG_TRACE)) {
+    const size_t tb = sizeof(long long) * 16 * i8c::kTraceSlots;
+    e = cudaMalloc(&p->trace, tb);
+    if (e == cudaSuccess) e = cudaMemset(p->trace, 0, tb);
+  }
   if (e == cudaSuccess && o.host_staging) {
     e = cudaMalloc(&p->stage_x, p->x_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&p->stage_f, p->f_bytes);
@@ -320,7 +438,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   // 32-channel rows of BN output channels for one K-slice, 64-byte swizzled.
   cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(s.K), static_cast<cuuint64_t>(p->num_slices)};
   cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(s.K) * 64};
-  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn), 1};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn),
+                       static_cast<cuuint32_t>(p->kernel_variant == 2 ? p->halo.bgroup : 1)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p->f16, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -359,9 +478,17 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->acc_buffers = pl->acc_buffers;
   info->smem_bytes = pl->smem_bytes;
   info->kernels_per_run = 2;
+  info->kernel_variant = pl->kernel_variant;
   info->ops = 2 * pl->M * s.K * static_cast<int64_t>(s.C) * s.R * s.S;
   info->workspace_bytes = pl->workspace_bytes;
   return I8C_OK;
+}
+
+i8c_status i8c_plan_trace(const i8c_plan* pl, long long* out, int64_t count) {
+  if (pl == nullptr || out == nullptr || count < 0) return I8C_ERR_INVALID_ARG;
+  if (pl->trace == nullptr) return I8C_ERR_INVALID_ARG;
+  const int64_t n = count < 16 * i8c::kTraceSlots ? count : 16 * i8c::kTraceSlots;
+  return from_cuda(cudaMemcpy(out, pl->trace, sizeof(long long) * n, cudaMemcpyDeviceToHost));
 }
 
 i8c_status i8c_plan_kernel_time(const i8c_plan* pl, double* total_ms, int64_t* launches) {

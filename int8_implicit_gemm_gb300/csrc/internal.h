@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "conv_fprop_halo.cuh"
 #include "conv_fprop_tc.cuh"
 
 namespace i8c {
@@ -18,6 +19,11 @@ int conv_smem_bytes(int block_n);
 cudaError_t conv_prepare(int block_n);  // raise the dynamic shared memory limit
 cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& p, int num_ctas,
                         cudaStream_t stream);
+
+cudaError_t conv_halo_prepare(int block_n);  // allow the full dynamic shared memory
+cudaError_t launch_conv_halo(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+                             cudaStream_t stream);
+constexpr int kMaxDynamicSmem = 232448;
 
 // layout_kernels.cu
 cudaError_t launch_filter_to_f16(const int8_t* f, uint16_t* f16, int64_t count, cudaStream_t stream);

@@ -53,18 +53,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or `hint_ns` elapses, so waiting warps do not take issue slots
+// from the warps sharing their SM sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // `timeout_ns` elapses first or, if `abort_flag` is not null, when it becomes
-// non-zero (another role of the CTA already gave up).
+// non-zero (another role of the CTA already gave up).  Between checks the
+// thread sleeps in the barrier (at most 20 us at a time).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
                                           const volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
+}
+
+// One elected lane of the (converged) warp returns true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 d;\n\telect.sync d|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // ---------------------------------------------------------------- fences
@@ -184,6 +207,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw64_kmajor(uint32_t saddr) {
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(4) << 61;
   return d;
+}
+
+// Shared-memory matrix descriptor for a K-major operand in the canonical
+// layout without swizzle: a core matrix is 8 rows x 16 bytes stored as 128
+// contiguous bytes (row i at +16*i); `lbo` is the byte distance between the
+// two 16-byte K-chunks of one K=16 step, `sbo` the byte distance between
+// consecutive 8-row groups.  Both must be multiples of 16 and below 2^18.
+__device__ __forceinline__ uint64_t smem_desc_noswizzle_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;
+  d |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;  // swizzle mode 0 (none)
 }
 
 // Instruction descriptor for kind::f16: fp16 A and B, fp32 D, both K-major.

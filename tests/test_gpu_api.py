@@ -107,10 +107,12 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     xp, fp = gpu_util.packed_inputs(x, f)
     xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
     y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
-    bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE)
-    bad.run(xd, fd, y, 1.0)
-    assert bad.status() == ext.I8C_ERR_TIMEOUT
-    assert bad.status() == ext.I8C_OK          # the status word was cleared
+    for kernel in (1, 2):
+        bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE,
+                       kernel_variant=kernel)
+        bad.run(xd, fd, y, 1.0)
+        assert bad.status() == ext.I8C_ERR_TIMEOUT, kernel
+        assert bad.status() == ext.I8C_OK          # the status word was cleared
     y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
     y2, _ = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, want_acc=False)
     assert np.array_equal(y2, y_ref)

@@ -37,10 +37,11 @@ def _data(shape, seed, lo=-128, hi=127):
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("alpha", [2.0 ** -9, 1.0 / 3.0])
-def test_small_shapes_exact(shape, alpha):
+@pytest.mark.parametrize("kernel", [1, 2], ids=["gather", "halo"])
+def test_small_shapes_exact(shape, alpha, kernel):
     x, f = _data(shape, 1000 + sum(shape))
     y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, alpha)
-    y, acc = gpu_util.gpu_run(shape, x, f, alpha)
+    y, acc = gpu_util.gpu_run(shape, x, f, alpha, kernel_variant=kernel)
     assert np.array_equal(acc, acc_ref.astype(np.int32))
     assert np.array_equal(y, y_ref)
 
@@ -48,6 +49,9 @@ def test_small_shapes_exact(shape, alpha):
 @pytest.mark.parametrize("opts", [
     dict(num_ctas=1), dict(num_ctas=3), dict(max_chunk_slices=1), dict(max_chunk_slices=5),
     dict(block_n=32), dict(block_n=64), dict(block_n=128), dict(block_n=256, num_ctas=2),
+    dict(kernel_variant=1, num_ctas=1), dict(kernel_variant=1, max_chunk_slices=5),
+    dict(kernel_variant=1, block_n=64), dict(kernel_variant=2, block_n=256, max_chunk_slices=7),
+    dict(kernel_variant=2, block_n=32, num_ctas=5),
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_plan_options_exact(opts):
     shape = (2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1)
@@ -71,9 +75,10 @@ def test_extreme_magnitudes_exact():
     f[3] = 127                                             # one channel of large negative sums
     y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -20)
     assert np.abs(acc_ref).max() > 2 ** 27
-    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -20)
-    assert np.array_equal(acc, acc_ref.astype(np.int32))
-    assert np.array_equal(y, y_ref)
+    for kernel in (1, 2):
+        y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -20, kernel_variant=kernel)
+        assert np.array_equal(acc, acc_ref.astype(np.int32)), kernel
+        assert np.array_equal(y, y_ref), kernel
 
 
 def test_saturation_and_ties():
