@@ -51,7 +51,10 @@ cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& 
 
 template <int BN>
 static cudaError_t halo_prepare_one() {
-  return cudaFuncSetAttribute(conv_fprop_halo_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(conv_fprop_halo_kernel<BN, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kMaxDynamicSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(conv_fprop_halo_kernel<BN, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kMaxDynamicSmem);
 }
 
@@ -68,7 +71,8 @@ cudaError_t conv_halo_prepare(int block_n) {
 template <int BN>
 static cudaError_t halo_launch_one(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
                                    cudaStream_t stream) {
-  conv_fprop_halo_kernel<BN><<<num_ctas, 384, smem, stream>>>(tmap, p);
+  if (p.bgroup == 3) conv_fprop_halo_kernel<BN, 3><<<num_ctas, 384, smem, stream>>>(tmap, p);
+  else conv_fprop_halo_kernel<BN, 0><<<num_ctas, 384, smem, stream>>>(tmap, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -348,7 +348,9 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       const int nt = (s.K + cand - 1) / cand;
       const int64_t t = static_cast<int64_t>(s.N) * h.TPH * h.TQW * nt;
       // narrower tiles give the single MMA-issuing thread less tensor work per K-slice
-      const double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.97 : cand == 64 ? 0.9 : 0.75;
+      double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.97 : cand == 64 ? 0.9 : 0.75;
+      // runs of one K-slice (no room for longer filter stages) issue poorly
+      if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
       const double score =
           wave_efficiency(t, ctas) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
       if (score > best * 1.02) {

@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
         ptx::mbar_arrive(&full3);
       }
       __syncwarp();
-      const int G = 3, S = 3, sw = 2, dw_mod = 1, dw_div = 0, cw_q = 5, cw_r = 0;
+      // geometry from the (runtime) iteration count so the compiler cannot fold it
+      const int rt = iters >> 30;  // 0 for any real iteration count
+      const int G = 3, S = 3 + rt, sw = 2 + rt, dw_mod = 1 + rt, dw_div = rt, cw_q = 5 + rt, cw_r = rt;
       const uint64_t a_desc0 = ad & ~static_cast<uint64_t>(0x3FFF);
       const uint64_t b_desc0 = bd & ~static_cast<uint64_t>(0x3FFF);
       const uint32_t h_stage = static_cast<uint32_t>(ad & 0x3FFF), b_lo0 = static_cast<uint32_t>(bd & 0x3FFF);
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
         ptx::tc_fence_after();
         uint32_t b_cur = b_lo0 + static_cast<uint32_t>(run & 1) * slice_lo;
         int fph = 0, idx = 0;
-        const int rowpos = (run % 3) * 10;
+        const int rowpos = (run % S) * (10 + rt);
         for (int t = 0; t < G; ++t) {
           const uint32_t a_cur = loop_mode == 8
                                      ? h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx)
