@@ -67,7 +67,7 @@ def kernel_source_digest() -> str:
 def dram_traffic(workload: str):
     """Per-launch DRAM bytes of the convolution kernel from the committed ncu
     summary, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "conv_fprop_tc_dram_traffic.json")
+    path = os.path.join(ROOT, "profiles", "conv_fprop_dram_traffic.json")
     try:
         with open(path) as fh:
             d = json.load(fh)
@@ -250,6 +250,7 @@ def run_ours(args, wl, rank, world):
     plan_h.destroy()
 
     peak, peak_note = tensor_peak()
+    kernel_name = "conv_fprop_halo_kernel" if plan.info["kernel_variant"] == 2 else "conv_fprop_tc_kernel"
     kern_avg_ms = kern_ms / max(1, kern_n)
     achieved = ops / (kern_avg_ms * 1e-3) / 1e12
     traffic = dram_traffic(wl.name)
@@ -270,12 +271,12 @@ def run_ours(args, wl, rank, world):
             ["N", "C", "H", "W", "K", "R", "S", "pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w"], shape)),
             "P": P, "Q": Q, "alpha": wl.alpha,
             "l2": f"{nsets} rotating input/output sets, {nsets * set_bytes / 2**20:.0f} MiB total > 129 MiB L2",
-            "plan": {k: plan.info[k] for k in ("block_m", "block_n", "num_tiles", "num_ctas", "num_chunks",
-                                              "chunk_slices", "acc_buffers", "smem_bytes")},
+            "plan": {k: plan.info[k] for k in ("kernel_variant", "block_m", "block_n", "num_tiles", "num_ctas",
+                                              "num_chunks", "chunk_slices", "acc_buffers", "smem_bytes")},
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "conv_fprop_tc_kernel", "kernel_ms": round(kern_avg_ms, 6),
+                     "kernel": kernel_name, "kernel_ms": round(kern_avg_ms, 6),
                      "note": f"int8 ops (2*N*K*P*Q*C*R*S) per launch / CUDA-event duration; peak {peak_note}"},
         "e2e": {"value": round(ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS", "ms_per_step": round(e2e_ms, 6),
                 "h2d_bytes_per_step": x_bytes + f_bytes, "d2h_bytes_per_step": y_bytes,
