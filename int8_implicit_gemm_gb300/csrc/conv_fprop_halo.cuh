@@ -16,8 +16,9 @@
 // phase by phase (all columns c with c % sw == 0 first, then 1, ...), so the
 // eight columns of a core matrix stay adjacent.
 //
-// Warp roles (384 threads): warp 0 MMA issuer and TMEM owner, warp 1 filter
-// TMA, warps 2-7 halo producers, warps 8-11 epilogue.  All waits are bounded.
+// Warp roles (512 threads): warp 0 MMA issuer and TMEM owner, warp 1 filter
+// TMA, warps 2-7 halo producers, warps 8-15 epilogue (two per TMEM lane
+// quarter, each draining half of the tile's columns).  All waits are bounded.
 #pragma once
 
 #include "conv_fprop_tc.cuh"
@@ -40,7 +41,15 @@ struct HaloParams {
 
 
 constexpr int kMaxBStages = 16;
-constexpr int kProducers = 192;  // halo producer threads: warps 2-7
+constexpr int kProducers = 192;   // halo producer threads: warps 2-7
+constexpr int kEpilogue = 256;    // epilogue threads: warps 8-15, two per TMEM lane quarter
+constexpr int kHaloThreads = 512;
+// Register budgets per warpgroup after setmaxnreg: the two epilogue warpgroups
+// hold the running sums; 128 * (2 * kWorkerRegs + 2 * kEpilogueRegs) must not
+// exceed the 512 * 128 registers the block is launched with.
+constexpr uint32_t kWorkerRegs = 56;
+constexpr uint32_t kEpilogueRegs = 200;
+static_assert(128 * (2 * kWorkerRegs + 2 * kEpilogueRegs) <= 512 * 128, "register split");
 constexpr int kHaloBarBytes = 512;
 
 struct PatchTile {
@@ -59,7 +68,7 @@ __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp
 // GT > 0 fixes the run length (K-slices per filter stage) at compile time so
 // that the per-run tap loop is unrolled; GT == 0 reads it from the parameters.
 template <int BN, int GT>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kHaloThreads, 1)
     conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
   const ConvParams& p = hp.c;
   extern __shared__ uint8_t smem_raw[];
@@ -88,7 +97,7 @@ __global__ void __launch_bounds__(384, 1)
       ptx::mbar_init(&h_full[i], kProducers);
       ptx::mbar_init(&h_empty[i], 1);
       ptx::mbar_init(&acc_full[i], 1);
-      ptx::mbar_init(&acc_empty[i], 128);
+      ptx::mbar_init(&acc_empty[i], kEpilogue);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -103,10 +112,10 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t nb = static_cast<uint32_t>(p.acc_buffers);
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
+    ptx::setmaxnreg_dec<kWorkerRegs>();
     // The whole warp runs the loop in uniform control flow so that every
     // descriptor is computed from loop counters and kernel parameters in
     // uniform registers; one elected lane issues each MMA and commit.
@@ -168,10 +177,13 @@ __global__ void __launch_bounds__(384, 1)
           if (kk != 0) {
             if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
             __syncwarp();
+#if defined(I8C_PIPELINE_TRACE)
+            trace_mark(p, 0, 2, u);
+#endif
             ++u;
           }
-          buf = nb == 1 ? 0u : (u & 1u);
-          const uint32_t aph = nb == 1 ? (u & 1u) : ((u >> 1) & 1u);
+          buf = u & 1u;
+          const uint32_t aph = (u >> 1) & 1u;
 #if defined(I8C_PIPELINE_TRACE)
           const long long ta = tracing ? clock64() : 0;
 #endif
@@ -181,6 +193,7 @@ __global__ void __launch_bounds__(384, 1)
           }
 #if defined(I8C_PIPELINE_TRACE)
           if (tracing) stall_acc += clock64() - ta;
+          trace_mark(p, 0, 3, u);
 #endif
           d_tmem = tmem_base + buf * BN;
           next_chunk = kk + p.chunk_slices;
@@ -260,6 +273,7 @@ __global__ void __launch_bounds__(384, 1)
     if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
   } else if (warp == 1) {
     // ------------------------------------------------------------ filter TMA producer
+    ptx::setmaxnreg_dec<kWorkerRegs>();
     const int G = GT > 0 ? GT : hp.bgroup;
     const uint32_t stage_bytes = static_cast<uint32_t>(G * BN * 64);
     uint32_t g = 0, st = 0, bph = 0;
@@ -294,6 +308,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 2 && warp < 8) {
     // ------------------------------------------------------------ halo producers
+    ptx::setmaxnreg_dec<kWorkerRegs>();
     // Thread pt owns the 16-byte half (pt & 1) of halo positions
     // e = pt/2 + k*(kProducers/2), k = 0, 1, ...; both loops below walk the
     // same positions, so each thread converts exactly the bytes it copied.
@@ -373,9 +388,20 @@ __global__ void __launch_bounds__(384, 1)
     ptx::cp_async_wait_all();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
+    // The int32 running sums of a tile live in these warps' registers (the two
+    // epilogue warpgroups raise their register budget), so tensor memory only
+    // holds two fp32 chunk accumulators and a drain is one read of the
+    // accumulator that overlaps the MMAs of the next chunk.
+    ptx::setmaxnreg_inc<kEpilogueRegs>();
     const int qd = warp & 3;
     const int row = 32 * qd + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
+    // columns of this warp: half `eh` of the tile (all of it when BN == 32, for warps 8-11)
+    const int eh = (warp - 8) >> 2;
+    constexpr int kColsPerWarp = BN >= 64 ? BN / 2 : BN;
+    const int col0 = BN >= 64 ? eh * kColsPerWarp : 0;
+    const bool col_owner = BN >= 64 || eh == 0;
+    uint32_t run[kColsPerWarp];  // running int32 sums of this thread's pixel over its columns
     uint32_t u = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
@@ -384,77 +410,67 @@ __global__ void __launch_bounds__(384, 1)
       const int qq = t.q0 + (row & 7);
       const bool valid = pp < p.P && qq < p.Q;
       for (int c = 0; c < p.num_chunks; ++c, ++u) {
-        const uint32_t buf = u % nb;
-        const bool got = ptx::mbar_wait(&acc_full[buf], (u / nb) & 1u, p.timeout_ns, abort_flag);
+        const uint32_t buf = u & 1u;
+#if defined(I8C_PIPELINE_TRACE)
+        if (warp == 8 && lane == 0) trace_mark(p, 3, 0, u);
+#endif
+        const bool got = ptx::mbar_wait(&acc_full[buf], (u >> 1) & 1u, p.timeout_ns, abort_flag);
+#if defined(I8C_PIPELINE_TRACE)
+        if (warp == 8 && lane == 0) trace_mark(p, 3, 1, u);
+#endif
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t t_acc = tmem_base + lane_addr + buf * BN;
-        const uint32_t t_run = tmem_base + lane_addr + nb * BN;
-        const bool first = c == 0, last = c + 1 == p.num_chunks;
-        // 32 channels of this pixel -> the NCxHWx<32> output (or int32 accumulators)
-        auto store32 = [&](const uint32_t* a, int k0) {
-          const int64_t off = ((static_cast<int64_t>(t.n) * p.KB + (k0 >> 5)) * p.P + pp) * p.Q + qq;
-          if (p.out_mode == 0) {
-            uint32_t o[8];
+        const uint32_t t_acc = tmem_base + lane_addr + buf * BN + col0;
+        const bool first = c == 0;
+        if (col_owner) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = pack4_s8(requant(static_cast<int>(a[4 * i]), p.alpha),
-                              requant(static_cast<int>(a[4 * i + 1]), p.alpha),
-                              requant(static_cast<int>(a[4 * i + 2]), p.alpha),
-                              requant(static_cast<int>(a[4 * i + 3]), p.alpha));
-            uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(p.acc + off * 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3]);
-          }
-        };
-        if constexpr (BN >= 64) {
-          // 64 columns per step: one wait covers the accumulator and running-sum loads
-#pragma unroll 1
-          for (int g = 0; g < BN / 64; ++g) {
-            const int k0 = t.nt * BN + g * 64;
-            if (k0 >= p.K) break;
-            uint32_t v[64], r[64];
-            ptx::tmem_ld_32x32b_x64(t_acc + g * 64, v);
-            if (!first) ptx::tmem_ld_32x32b_x64(t_run + g * 64, r);
+          for (int g = 0; g < kColsPerWarp / 32; ++g) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(t_acc + g * 32, v);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 64; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
-            if (!first) {
-#pragma unroll
-              for (int i = 0; i < 64; ++i) v[i] += r[i];
-            }
-            if (!last) {
-              ptx::tmem_st_32x32b_x64(t_run + g * 64, v);
-            } else if (valid) {
-              store32(v, k0);
-              if (k0 + 32 < p.K) store32(v + 32, k0 + 32);
+            for (int i = 0; i < 32; ++i) {
+              const uint32_t a = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+              run[g * 32 + i] = first ? a : run[g * 32 + i] + a;
             }
           }
-        } else {
-          const int k0 = t.nt * BN;
-          uint32_t v[32], r[32];
-          ptx::tmem_ld_32x32b_x32(t_acc, v);
-          if (!first) ptx::tmem_ld_32x32b_x32(t_run, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
-          if (!first) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += r[i];
-          }
-          if (!last) ptx::tmem_st_32x32b_x32(t_run, v);
-          else if (valid) store32(v, k0);
         }
-        ptx::tmem_wait_st();
+        // the accumulator buffer is free once read
         ptx::tc_fence_before();
         ptx::mbar_arrive(&acc_empty[buf]);
+#if defined(I8C_PIPELINE_TRACE)
+        if (warp == 8 && lane == 0) trace_mark(p, 3, 2, u);
+#endif
+        if (c + 1 == p.num_chunks && col_owner && valid) {
+#pragma unroll
+          for (int g = 0; g < kColsPerWarp / 32; ++g) {
+            const int k0 = t.nt * BN + col0 + g * 32;
+            if (k0 < p.K) {
+              const int64_t off = ((static_cast<int64_t>(t.n) * p.KB + (k0 >> 5)) * p.P + pp) * p.Q + qq;
+              if (p.out_mode == 0) {
+                uint32_t o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  o[i] = pack4_s8(requant(static_cast<int>(run[g * 32 + 4 * i]), p.alpha),
+                                  requant(static_cast<int>(run[g * 32 + 4 * i + 1]), p.alpha),
+                                  requant(static_cast<int>(run[g * 32 + 4 * i + 2]), p.alpha),
+                                  requant(static_cast<int>(run[g * 32 + 4 * i + 3]), p.alpha));
+                uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(p.acc + off * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  dst[i] = make_uint4(run[g * 32 + 4 * i], run[g * 32 + 4 * i + 1], run[g * 32 + 4 * i + 2],
+                                      run[g * 32 + 4 * i + 3]);
+              }
+            }
+          }
+        }
       }
     }
     if (!ok) raise_timeout(p, abort_flag);

@@ -71,8 +71,8 @@ cudaError_t conv_halo_prepare(int block_n) {
 template <int BN>
 static cudaError_t halo_launch_one(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
                                    cudaStream_t stream) {
-  if (p.bgroup == 3) conv_fprop_halo_kernel<BN, 3><<<num_ctas, 384, smem, stream>>>(tmap, p);
-  else conv_fprop_halo_kernel<BN, 0><<<num_ctas, 384, smem, stream>>>(tmap, p);
+  if (p.bgroup == 3) conv_fprop_halo_kernel<BN, 3><<<num_ctas, kHaloThreads, smem, stream>>>(tmap, p);
+  else conv_fprop_halo_kernel<BN, 0><<<num_ctas, kHaloThreads, smem, stream>>>(tmap, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();
 }

@@ -347,8 +347,9 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (!halo_layout(s, p->P, p->Q, cand, &h, &sm)) continue;
       const int nt = (s.K + cand - 1) / cand;
       const int64_t t = static_cast<int64_t>(s.N) * h.TPH * h.TQW * nt;
-      // narrower tiles give the single MMA-issuing thread less tensor work per K-slice
-      double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.97 : cand == 64 ? 0.9 : 0.75;
+      // narrower MMAs leave the issuing warp's per-slice overhead exposed (the
+      // tensor core queues only about two MMAs); measured relative rates
+      double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
       // runs of one K-slice (no room for longer filter stages) issue poorly
       if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
       const double score =
@@ -397,9 +398,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     p->chunk_slices = (p->chunk_slices + p->halo.bgroup - 1) / p->halo.bgroup * p->halo.bgroup;
     p->num_chunks = (p->num_slices + p->chunk_slices - 1) / p->chunk_slices;
   }
-  const int run_cols = p->num_chunks > 1 ? bn : 0;
-  p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
-  p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
+  if (p->kernel_variant == 2) {
+    // halo kernel: two fp32 chunk accumulators; running sums live in registers
+    p->acc_buffers = 2;
+    p->tmem_cols = static_cast<uint32_t>(next_pow2(2 * bn));
+  } else {
+    const int run_cols = p->num_chunks > 1 ? bn : 0;
+    p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
+    p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
+  }
   p->smem_bytes = p->kernel_variant == 2 ? halo_smem : i8c::conv_smem_bytes(bn);
   p->timeout_ns = static_cast<uint64_t>(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
   p->debug_flags = o.debug_flags;
