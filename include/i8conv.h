@@ -78,6 +78,11 @@ typedef struct {
                                 for benchmarks, not for use under graph capture               */
   int32_t kernel_variant;    /* 0 = auto, 1 = per-tap gather kernel, 2 = halo kernel (16x8
                                 output patches; I8C_ERR_UNSUPPORTED if its halo does not fit) */
+  int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
+                                (currently the same as 2), 1 = int8 staging ring filled by
+                                cp.async ahead of use, 2 = straight into registers (no
+                                staging memory); I8C_ERR_UNSUPPORTED if the forced form
+                                does not fit                                               */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so
@@ -106,6 +111,11 @@ typedef struct {
   int64_t ops;               /* 2*N*K*P*Q*C*R*S                                 */
   int64_t workspace_bytes;   /* device memory owned by the plan                */
   int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel     */
+  int32_t halo_staging;      /* halo kernel: int8 staging slots (0 = loads
+                                straight into registers); 0 for the gather kernel */
+  int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of
+                                one filter row); 1 for the gather kernel       */
+  int32_t filter_stages;     /* filter pipeline stages in shared memory        */
 } i8c_plan_info;
 
 /* Output height P and width Q for a shape (formula above).  Returns

@@ -32,7 +32,7 @@ struct HaloParams {
   uint32_t plane_bytes;     // one 8-channel plane: HR*CW*16 (rounded up to 128)
   uint32_t halo_bytes;      // one halo stage: 4 planes
   uint32_t stg_bytes;       // one int8 staging slot: HR*CW*32 (rounded up to 128)
-  int nstg;                 // int8 staging slots: 2 or 3
+  int nstg;                 // int8 staging slots: 2 or 3, or 0 (producers load into registers)
   int nbs;                  // filter pipeline stages (<= kMaxBStages)
   int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
   uint32_t off_stg, off_b, off_bar;
@@ -63,6 +63,169 @@ __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp
   rest /= hp.TQW;
   const int pt = rest % hp.TPH;
   return {rest / hp.TPH, pt * 16, qt * 8, nt};
+}
+
+// First halo position of thread pt and the walk between its positions.
+struct HaloWalk {
+  int e_first, b_first, pos_first, b_step, pos_step;
+};
+constexpr int kHaloStep = kProducers / 2;
+
+__device__ __forceinline__ HaloWalk halo_walk(const HaloParams& hp, int pt) {
+  HaloWalk w;
+  w.e_first = pt >> 1;
+  w.b_first = w.e_first / hp.CW;
+  w.pos_first = w.e_first - w.b_first * hp.CW;
+  w.b_step = kHaloStep / hp.CW;
+  w.pos_step = kHaloStep - w.b_step * hp.CW;
+  return w;
+}
+
+// Input column (relative to the halo's first column) of halo position pos in
+// its row: positions are ordered by column phase (column mod stride_w).
+__device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
+  int f = hp.c.stride_w - 1;
+  while (pos < hp.phase_off[f]) --f;
+  return (pos - hp.phase_off[f]) * hp.c.stride_w + f;
+}
+
+__device__ __forceinline__ uint32_t halo_stage_count(const HaloParams& hp) {
+  const ConvParams& p = hp.c;
+  return static_cast<uint32_t>((p.num_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x) *
+         static_cast<uint32_t>(p.CB);
+}
+
+__device__ __forceinline__ void halo_store_f16(const HaloParams& hp, uint8_t* halo, int e, int h, const uint4& v) {
+  uint4 c0, c1;
+  i8x4_to_f16x4(v.x, c0.x, c0.y);
+  i8x4_to_f16x4(v.y, c0.z, c0.w);
+  i8x4_to_f16x4(v.z, c1.x, c1.y);
+  i8x4_to_f16x4(v.w, c1.z, c1.w);
+  *reinterpret_cast<uint4*>(halo + (2 * h) * hp.plane_bytes + e * 16) = c0;
+  *reinterpret_cast<uint4*>(halo + (2 * h + 1) * hp.plane_bytes + e * 16) = c1;
+}
+
+// Producer through the int8 staging ring (hp.nstg slots of 32 bytes per
+// position).  Returns false when a wait timed out.
+__device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_t* smem, uint64_t* h_full,
+                                                   uint64_t* h_empty, volatile int* abort_flag, int pt) {
+  const ConvParams& p = hp.c;
+  const int h = pt & 1;
+  const int positions = hp.HR * hp.CW;
+  const HaloWalk w = halo_walk(hp, pt);
+  const int HW32 = p.H * p.W * 32;
+  const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
+  int l_tile = blockIdx.x, l_cb = 0;
+
+  auto issue_load = [&](uint32_t slot) {
+    if (l_tile < p.num_tiles) {
+      const PatchTile t = decode_patch(l_tile, hp);
+      const int hb0 = t.p0 * p.stride_h - p.pad_h;
+      const int wb0 = t.q0 * p.stride_w - p.pad_w;
+      const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + l_cb * HW32;
+      const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
+      int b = w.b_first, pos = w.pos_first;
+      for (int e = w.e_first; e < positions; e += kHaloStep) {
+        const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+        const bool in = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
+        const int8_t* src = in ? img + (hh * p.W + ww) * 32 + h * 16 : p.x;
+        ptx::cp_async_16_ca(dst0 + e * 32 + h * 16, src, in ? 16u : 0u);
+        b += w.b_step;
+        pos += w.pos_step;
+        if (pos >= hp.CW) {
+          pos -= hp.CW;
+          ++b;
+        }
+      }
+      if (++l_cb == p.CB) {
+        l_cb = 0;
+        l_tile += gridDim.x;
+      }
+    }
+    ptx::cp_async_commit();
+  };
+
+  const uint32_t total = halo_stage_count(hp);
+  const int nstg = hp.nstg;
+  for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
+  bool ok = true;
+  for (uint32_t s = 0; s < total; ++s) {
+    issue_load((s + nstg - 1) % nstg);
+    if (nstg == 3) ptx::cp_async_wait<2>();
+    else ptx::cp_async_wait<1>();
+    const uint32_t hs = s & 1u;
+    if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
+    uint8_t* halo = smem + hs * hp.halo_bytes;
+    for (int e = w.e_first; e < positions; e += kHaloStep)
+      halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+    ptx::fence_proxy_async_smem();
+    if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
+  }
+  ptx::cp_async_wait_all();
+  return ok;
+}
+
+// Producer that loads straight into registers, kBatch positions at a time
+// (zeros outside the image).  Returns false when a wait timed out.
+__device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_t* smem, uint64_t* h_full,
+                                                   uint64_t* h_empty, volatile int* abort_flag, int pt) {
+  const ConvParams& p = hp.c;
+  constexpr int kBatch = 4;
+  const int h = pt & 1;
+  const int positions = hp.HR * hp.CW;
+  const HaloWalk w = halo_walk(hp, pt);
+  const int HW32 = p.H * p.W * 32;
+  const uint32_t total = halo_stage_count(hp);
+  int tile = blockIdx.x, cb = 0;
+  for (uint32_t s = 0; s < total; ++s) {
+    const PatchTile t = decode_patch(tile, hp);
+    const int hb0 = t.p0 * p.stride_h - p.pad_h;
+    const int wb0 = t.q0 * p.stride_w - p.pad_w;
+    const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + cb * HW32;
+    const uint32_t hs = s & 1u;
+    uint8_t* halo = smem + hs * hp.halo_bytes;
+    int e = w.e_first, b = w.b_first, pos = w.pos_first;
+    bool stage_free = false;
+    do {
+      uint4 v[kBatch];
+      int eb[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        eb[k] = e;
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (e < positions) {
+          const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+          if (hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
+            v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
+          e += kHaloStep;
+          b += w.b_step;
+          pos += w.pos_step;
+          if (pos >= hp.CW) {
+            pos -= hp.CW;
+            ++b;
+          }
+        }
+      }
+      if (!stage_free) {
+        if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) return false;
+        stage_free = true;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (eb[k] < positions) halo_store_f16(hp, halo, eb[k], h, v[k]);
+    } while (e < positions);
+    ptx::fence_proxy_async_smem();
+    if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
+    if (++cb == p.CB) {
+      cb = 0;
+      tile += gridDim.x;
+    }
+  }
+  return true;
 }
 
 // GT > 0 fixes the run length (K-slices per filter stage) at compile time so
@@ -308,84 +471,19 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     }
   } else if (warp >= 2 && warp < 8) {
     // ------------------------------------------------------------ halo producers
-    ptx::setmaxnreg_dec<kWorkerRegs>();
     // Thread pt owns the 16-byte half (pt & 1) of halo positions
-    // e = pt/2 + k*(kProducers/2), k = 0, 1, ...; both loops below walk the
-    // same positions, so each thread converts exactly the bytes it copied.
+    // e = pt/2 + k*(kProducers/2), k = 0, 1, ...  Two ways to bring a channel
+    // block in, chosen by the plan: through an int8 staging ring that
+    // cp.async fills nstg-1 channel blocks ahead (deep prefetch, costs
+    // shared memory), or straight into registers in batches whose first one
+    // is in flight while the thread waits for the halo stage (no staging
+    // memory, which leaves room for longer filter stages).  Either way the
+    // bytes are converted to fp16 and stored into the free halo stage.
+    ptx::setmaxnreg_dec<kWorkerRegs>();
     const int pt = threadIdx.x - 64;
-    const int h = pt & 1;
-    const int positions = hp.HR * hp.CW;
-    const int e_first = pt >> 1;
-    constexpr int e_step = kProducers / 2;
-    const int b_first = e_first / hp.CW, pos_first = e_first - b_first * hp.CW;
-    const int b_step = e_step / hp.CW, pos_step = e_step - b_step * hp.CW;
-    const int HW32 = p.H * p.W * 32;
-    const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
-    int l_tile = blockIdx.x, l_cb = 0;
-
-    auto issue_load = [&](uint32_t slot) {
-      if (l_tile < p.num_tiles) {
-        const PatchTile t = decode_patch(l_tile, hp);
-        const int hb0 = t.p0 * p.stride_h - p.pad_h;
-        const int wb0 = t.q0 * p.stride_w - p.pad_w;
-        const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + l_cb * HW32;
-        const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
-        int b = b_first, pos = pos_first;
-        for (int e = e_first; e < positions; e += e_step) {
-          int f = p.stride_w - 1;
-          while (pos < hp.phase_off[f]) --f;
-          const int c = (pos - hp.phase_off[f]) * p.stride_w + f;
-          const int hh = hb0 + b, ww = wb0 + c;
-          const bool in = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
-          const int8_t* src = in ? img + (hh * p.W + ww) * 32 + h * 16 : p.x;
-          ptx::cp_async_16_ca(dst0 + e * 32 + h * 16, src, in ? 16u : 0u);
-          b += b_step;
-          pos += pos_step;
-          if (pos >= hp.CW) {
-            pos -= hp.CW;
-            ++b;
-          }
-        }
-        if (++l_cb == p.CB) {
-          l_cb = 0;
-          l_tile += gridDim.x;
-        }
-      }
-      ptx::cp_async_commit();
-    };
-
-    const uint32_t total = static_cast<uint32_t>((p.num_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) /
-                                                 gridDim.x) *
-                           static_cast<uint32_t>(p.CB);
-    const int nstg = hp.nstg;
-    for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
-    bool ok = true;
-    for (uint32_t s = 0; s < total; ++s) {
-      issue_load((s + nstg - 1) % nstg);
-      if (nstg == 3) ptx::cp_async_wait<2>();
-      else ptx::cp_async_wait<1>();
-      const uint32_t hs = s & 1u;
-      if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
-      uint8_t* halo = smem + hs * hp.halo_bytes;
-      for (int e = e_first; e < positions; e += e_step) {
-        const uint4 v = *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16);
-        uint4 c0, c1;
-        i8x4_to_f16x4(v.x, c0.x, c0.y);
-        i8x4_to_f16x4(v.y, c0.z, c0.w);
-        i8x4_to_f16x4(v.z, c1.x, c1.y);
-        i8x4_to_f16x4(v.w, c1.z, c1.w);
-        *reinterpret_cast<uint4*>(halo + (2 * h) * hp.plane_bytes + e * 16) = c0;
-        *reinterpret_cast<uint4*>(halo + (2 * h + 1) * hp.plane_bytes + e * 16) = c1;
-      }
-      ptx::fence_proxy_async_smem();
-      if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
-    }
+    const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, smem, h_full, h_empty, abort_flag, pt)
+                                : halo_produce_direct(hp, smem, h_full, h_empty, abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
-    ptx::cp_async_wait_all();
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
     // The int32 running sums of a tile live in these warps' registers (the two

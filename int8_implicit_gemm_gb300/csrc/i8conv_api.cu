@@ -111,7 +111,10 @@ double wave_efficiency(int64_t tiles, int ctas) {
 
 // Halo geometry and shared-memory layout for a tile width; returns false when
 // the halo does not fit with at least three filter stages.
-bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, i8c::HaloParams* h, int* smem_bytes) {
+// Shared-memory layout of the halo kernel for tile width bn: two fp16 halo
+// stages, the int8 staging ring (if any), the filter stages, the barriers.
+// loads: 0 = auto, 1 = staging ring only, 2 = register loads only.
+bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int loads, i8c::HaloParams* h, int* smem_bytes) {
   if (s.stride_w > 8) return false;
   *h = i8c::HaloParams{};
   h->TPH = (P + 15) / 16;
@@ -133,11 +136,17 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, i8c::HaloParams*
   h->phase_off[s.stride_w] = off;
   // Filter stages of G K-slices each, G a divisor of S so that a stage is a
   // run of taps of one filter row: the largest such G with G*BN <= 1024 and at
-  // least three stages in shared memory.
+  // least three stages in shared memory.  The producers load into registers
+  // unless the staging ring (three slots, else two) is asked for: measured on
+  // the 3x3 layers, the ring's deeper prefetch gains nothing at width 256
+  // and costs filter stages.
   const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
+  static const int kSlots[3] = {3, 2, 0};
+  const int first = loads == 1 ? 0 : 2, last = loads == 1 ? 1 : 2;
   for (int G = s.S; G >= 1; --G) {
     if (s.S % G != 0 || G * bn > 1024 || G > 32) continue;
-    for (int nstg = 3; nstg >= 2; --nstg) {
+    for (int k = first; k <= last; ++k) {
+      const int nstg = kSlots[k];
       const int64_t off_stg = 2LL * h->halo_bytes;
       const int64_t off_b = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
       const int64_t room = budget - off_b;
@@ -309,7 +318,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 2)
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 2 || o.halo_loads < 0 || o.halo_loads > 2)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -344,7 +353,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (o.block_n == 0 && cand > 32 && cand / 2 >= s.K) continue;
       i8c::HaloParams h;
       int sm = 0;
-      if (!halo_layout(s, p->P, p->Q, cand, &h, &sm)) continue;
+      if (!halo_layout(s, p->P, p->Q, cand, o.halo_loads, &h, &sm)) continue;
       const int nt = (s.K + cand - 1) / cand;
       const int64_t t = static_cast<int64_t>(s.N) * h.TPH * h.TQW * nt;
       // narrower MMAs leave the issuing warp's per-slice overhead exposed (the
@@ -362,7 +371,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     if (best_bn != 0) {
       bn = best_bn;
       p->kernel_variant = 2;
-      halo_layout(s, p->P, p->Q, bn, &p->halo, &halo_smem);
+      halo_layout(s, p->P, p->Q, bn, o.halo_loads, &p->halo, &halo_smem);
     } else if (o.kernel_variant == 2) {
       delete p;
       return I8C_ERR_UNSUPPORTED;
@@ -488,6 +497,12 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->smem_bytes = pl->smem_bytes;
   info->kernels_per_run = 2;
   info->kernel_variant = pl->kernel_variant;
+  info->halo_staging = pl->kernel_variant == 2 ? pl->halo.nstg : 0;
+  info->filter_run = pl->kernel_variant == 2 ? pl->halo.bgroup : 1;
+  info->filter_stages = pl->kernel_variant == 2 ? pl->halo.nbs
+                        : pl->block_n >= 256 ? i8c::TileCfg<256>::kStages
+                        : pl->block_n >= 128 ? i8c::TileCfg<128>::kStages
+                                             : i8c::TileCfg<64>::kStages;
   info->ops = 2 * pl->M * s.K * static_cast<int64_t>(s.C) * s.R * s.S;
   info->workspace_bytes = pl->workspace_bytes;
   return I8C_OK;

@@ -76,3 +76,30 @@ def test_null_pointers_rejected(ext):
     st = ext.lib.i8c_conv2d_fprop(None, None, None, ctypes.byref(ext.ConvShape.of(
         (1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1))), ctypes.c_float(1.0), None)
     assert st == ext.I8C_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("ctype,cls_name", [("i8c_conv_shape", "ConvShape"), ("i8c_options", "Options"),
+                                            ("i8c_plan_info", "PlanInfo")])
+def test_binding_structs_match_header(ext, tmp_path, ctype, cls_name):
+    """The binding's ctypes structures have the header's size and field offsets
+    (compiled with the host C compiler against include/i8conv.h)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    cls = getattr(ext, cls_name)
+    fields = [n for n, _ in cls._fields_]
+    lines = [f'  printf("size %zu\\n", sizeof({ctype}));']
+    lines += [f'  printf("{n} %zu\\n", offsetof({ctype}, {n}));' for n in fields]
+    src = tmp_path / "abi.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "i8conv.h"\nint main(void) {\n'
+                   + "\n".join(lines) + "\n  return 0;\n}\n")
+    exe = tmp_path / "abi"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                         text=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(cls)
+    for n in fields:
+        assert int(out[n]) == getattr(cls, n).offset, n
