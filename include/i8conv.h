@@ -77,7 +77,9 @@ typedef struct {
                                 the last timing_events launches) for i8c_plan_kernel_time;
                                 for benchmarks, not for use under graph capture               */
   int32_t kernel_variant;    /* 0 = auto, 1 = per-tap gather kernel, 2 = halo kernel (16x8
-                                output patches; I8C_ERR_UNSUPPORTED if its halo does not fit) */
+                                output patches; I8C_ERR_UNSUPPORTED if its halo does not fit),
+                                3 = halo kernel on CTA pairs (clusters of two SMs sharing one
+                                M = 256 MMA per K-step; block_n 64, 128 or 256)              */
   int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
                                 (currently the same as 2), 1 = int8 staging ring filled by
                                 cp.async ahead of use, 2 = straight into registers (no
@@ -100,7 +102,7 @@ typedef struct {
   int32_t P, Q;              /* output height and width                        */
   int64_t M;                 /* GEMM rows: N*P*Q                               */
   int32_t gemm_n, gemm_k;    /* GEMM columns (K) and reduction length (C*R*S)  */
-  int32_t block_m, block_n;  /* tile shape                                     */
+  int32_t block_m, block_n;  /* tile shape (block_m 256 for a CTA pair's tile) */
   int32_t num_tiles;         /* M-tiles x N-tiles                              */
   int32_t num_ctas;          /* persistent grid size                           */
   int32_t num_chunks;        /* exact fp32 chunks per tile                     */
@@ -110,7 +112,8 @@ typedef struct {
   int32_t kernels_per_run;   /* kernel launches enqueued by one i8c_plan_run   */
   int64_t ops;               /* 2*N*K*P*Q*C*R*S                                 */
   int64_t workspace_bytes;   /* device memory owned by the plan                */
-  int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel     */
+  int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel,
+                                3 = halo kernel on CTA pairs                   */
   int32_t halo_staging;      /* halo kernel: int8 staging slots (0 = loads
                                 straight into registers); 0 for the gather kernel */
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of

@@ -25,7 +25,15 @@ extern "C" {
  * B is always 64-byte swizzled.  loop_mode 0 issues bare MMAs; 1-3 issue them
  * in the convolution's per-K-slice pattern (pairs of MMAs with the A start
  * from a shared-memory table; 2 adds a completed-barrier check every 4
- * slices, 3 also a commit every 4 slices).
+ * slices, 3 also a commit every 4 slices).  Modes 4-18 issue from a whole
+ * warp in uniform control flow with one elected lane: 4 (A start from loop
+ * counters), 5 (from a table), 6-7 (with epilogue warps waiting, sleeping or
+ * polling), 8-9 (the convolution's run loop: runs of three K-slices, a
+ * completed-barrier wait before and a commit after each run), 10 (four
+ * warps storing to shared memory alongside), 11-14 (six MMAs, then 0, 200,
+ * 400 or 800 idle cycles: queue depth), 15-18 (mode 8 without its commit,
+ * without its wait, with one elected block per run, with one elected block
+ * and neither wait nor commit).  iters must be a multiple of 6.
  *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles to issue,
  *           SM cycles until all MMAs completed, 1 if the completion wait
  *           succeeded (bounded at 2 s)

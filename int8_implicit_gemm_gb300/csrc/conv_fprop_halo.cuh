@@ -16,9 +16,10 @@
 // phase by phase (all columns c with c % sw == 0 first, then 1, ...), so the
 // eight columns of a core matrix stay adjacent.
 //
-// Warp roles (512 threads): warp 0 MMA issuer and TMEM owner, warp 1 filter
-// TMA, warps 2-7 halo producers, warps 8-15 epilogue (two per TMEM lane
-// quarter, each draining half of the tile's columns).  All waits are bounded.
+// Warp roles (512 threads): warp 0 MMA issuer and TMEM owner, warp 4 filter
+// TMA, warps 1-3 and 5-7 halo producers, warps 8-15 epilogue (two per TMEM
+// lane quarter, each draining half of the tile's columns).  All waits are
+// bounded.
 #pragma once
 
 #include "conv_fprop_tc.cuh"
@@ -28,6 +29,7 @@ namespace i8c {
 struct HaloParams {
   ConvParams c;
   int TPH, TQW;             // patches per image along P (16 rows each) and Q (8 columns each)
+  int num_patches;          // N * TPH * TQW
   int HR, CW;               // halo rows, halo positions per row
   uint32_t plane_bytes;     // one 8-channel plane: HR*CW*16 (rounded up to 128)
   uint32_t halo_bytes;      // one halo stage: 4 planes
@@ -41,6 +43,11 @@ struct HaloParams {
 
 
 constexpr int kMaxBStages = 16;
+// Warp roles: 0 MMA issuer, kTmaWarp filter TMA, the other warps below 8 halo
+// producers, 8-15 epilogue.  Warps w, w+4, w+8, w+12 share one scheduler;
+// the mostly sleeping TMA warp sits next to the MMA warp, whose issue latency
+// the tensor core's short queue exposes, instead of a busy producer warp.
+constexpr int kTmaWarp = 4;
 constexpr int kProducers = 192;   // halo producer threads: warps 2-7
 constexpr int kEpilogue = 256;    // epilogue threads: warps 8-15, two per TMEM lane quarter
 constexpr int kHaloThreads = 512;
@@ -54,15 +61,50 @@ constexpr int kHaloBarBytes = 512;
 
 struct PatchTile {
   int n, p0, q0, nt;
+  bool valid;  // false for the missing second patch of a CTA pair's last tile
 };
 
-__device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp) {
+// Tile schedule of one CTA: tiles first, first + step, ...; a tile is
+// (group of cg patches, N-tile) and this CTA computes patch `rank` of the
+// group (cg = 2 for CTA pairs, whose two CTAs walk the same tiles).
+struct TileSched {
+  int first, step, rank, cg;
+};
+
+// Derived from the block index alone, so the compiler can recompute it
+// instead of keeping it in registers: in a 1-D grid of clusters of two, CTA
+// 2c + r is rank r of cluster c.
+template <int CG>
+__device__ __forceinline__ TileSched tile_sched() {
+  if constexpr (CG == 2)
+    return {static_cast<int>(blockIdx.x) >> 1, static_cast<int>(gridDim.x) >> 1, static_cast<int>(blockIdx.x) & 1,
+            2};
+  return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), 0, 1};
+}
+
+__device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp, const TileSched& ts) {
   const int nt = tile % hp.c.num_n_tiles;
-  int rest = tile / hp.c.num_n_tiles;
-  const int qt = rest % hp.TQW;
-  rest /= hp.TQW;
+  const int patch = (tile / hp.c.num_n_tiles) * ts.cg + ts.rank;
+  const int qt = patch % hp.TQW;
+  const int rest = patch / hp.TQW;
   const int pt = rest % hp.TPH;
-  return {rest / hp.TPH, pt * 16, qt * 8, nt};
+  return {rest / hp.TPH, pt * 16, qt * 8, nt, patch < hp.num_patches};
+}
+
+// Arrive on a barrier of the MMA-issuing CTA, called by all 32 lanes of a
+// warp (`mine`: whether this lane's arrival counts): each lane arrives on
+// this CTA's own barrier, or for rank 1 of a pair one lane arrives for the
+// whole warp on the barrier at the same offset in rank 0, after a warp
+// barrier that orders the other lanes' writes before its cluster-scope
+// release (one remote transaction per warp instead of 32).
+__device__ __forceinline__ void arrive_on_leader(uint64_t* bar, const TileSched& ts, bool mine = true) {
+  if (ts.rank == 0) {
+    if (mine) ptx::mbar_arrive(bar);
+  } else {
+    __syncwarp();  // orders every lane's prior shared-memory writes before lane 0's release
+    const uint32_t n = __popc(__ballot_sync(0xffffffffu, mine));
+    if ((threadIdx.x & 31) == 0 && n != 0) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_addr(bar), 0), n);
+  }
 }
 
 // First halo position of thread pt and the walk between its positions.
@@ -89,10 +131,10 @@ __device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
   return (pos - hp.phase_off[f]) * hp.c.stride_w + f;
 }
 
-__device__ __forceinline__ uint32_t halo_stage_count(const HaloParams& hp) {
+__device__ __forceinline__ uint32_t halo_stage_count(const HaloParams& hp, const TileSched& ts) {
   const ConvParams& p = hp.c;
-  return static_cast<uint32_t>((p.num_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x) *
-         static_cast<uint32_t>(p.CB);
+  const int tiles = p.num_tiles > ts.first ? (p.num_tiles - ts.first + ts.step - 1) / ts.step : 0;
+  return static_cast<uint32_t>(tiles) * static_cast<uint32_t>(p.CB);
 }
 
 __device__ __forceinline__ void halo_store_f16(const HaloParams& hp, uint8_t* halo, int e, int h, const uint4& v) {
@@ -107,19 +149,20 @@ __device__ __forceinline__ void halo_store_f16(const HaloParams& hp, uint8_t* ha
 
 // Producer through the int8 staging ring (hp.nstg slots of 32 bytes per
 // position).  Returns false when a wait timed out.
-__device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_t* smem, uint64_t* h_full,
-                                                   uint64_t* h_empty, volatile int* abort_flag, int pt) {
+__device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                   uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
+                                                   int pt) {
   const ConvParams& p = hp.c;
   const int h = pt & 1;
   const int positions = hp.HR * hp.CW;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
   const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
-  int l_tile = blockIdx.x, l_cb = 0;
+  int l_tile = ts.first, l_cb = 0;
 
   auto issue_load = [&](uint32_t slot) {
     if (l_tile < p.num_tiles) {
-      const PatchTile t = decode_patch(l_tile, hp);
+      const PatchTile t = decode_patch(l_tile, hp, ts);
       const int hb0 = t.p0 * p.stride_h - p.pad_h;
       const int wb0 = t.q0 * p.stride_w - p.pad_w;
       const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + l_cb * HW32;
@@ -127,7 +170,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_
       int b = w.b_first, pos = w.pos_first;
       for (int e = w.e_first; e < positions; e += kHaloStep) {
         const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
-        const bool in = hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
+        const bool in = t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
         const int8_t* src = in ? img + (hh * p.W + ww) * 32 + h * 16 : p.x;
         ptx::cp_async_16_ca(dst0 + e * 32 + h * 16, src, in ? 16u : 0u);
         b += w.b_step;
@@ -139,13 +182,13 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_
       }
       if (++l_cb == p.CB) {
         l_cb = 0;
-        l_tile += gridDim.x;
+        l_tile += ts.step;
       }
     }
     ptx::cp_async_commit();
   };
 
-  const uint32_t total = halo_stage_count(hp);
+  const uint32_t total = halo_stage_count(hp, ts);
   const int nstg = hp.nstg;
   for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
   bool ok = true;
@@ -154,7 +197,8 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_
     if (nstg == 3) ptx::cp_async_wait<2>();
     else ptx::cp_async_wait<1>();
     const uint32_t hs = s & 1u;
-    if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+    // warp-uniform outcome: the arrive below is a warp-wide operation
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag))) {
       ok = false;
       break;
     }
@@ -163,7 +207,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_
     for (int e = w.e_first; e < positions; e += kHaloStep)
       halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
     ptx::fence_proxy_async_smem();
-    if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
+    arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
   }
   ptx::cp_async_wait_all();
   return ok;
@@ -171,18 +215,19 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, uint8_
 
 // Producer that loads straight into registers, kBatch positions at a time
 // (zeros outside the image).  Returns false when a wait timed out.
-__device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_t* smem, uint64_t* h_full,
-                                                   uint64_t* h_empty, volatile int* abort_flag, int pt) {
+__device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                   uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
+                                                   int pt) {
   const ConvParams& p = hp.c;
   constexpr int kBatch = 4;
   const int h = pt & 1;
   const int positions = hp.HR * hp.CW;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
-  const uint32_t total = halo_stage_count(hp);
-  int tile = blockIdx.x, cb = 0;
+  const uint32_t total = halo_stage_count(hp, ts);
+  int tile = ts.first, cb = 0;
   for (uint32_t s = 0; s < total; ++s) {
-    const PatchTile t = decode_patch(tile, hp);
+    const PatchTile t = decode_patch(tile, hp, ts);
     const int hb0 = t.p0 * p.stride_h - p.pad_h;
     const int wb0 = t.q0 * p.stride_w - p.pad_w;
     const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + cb * HW32;
@@ -199,7 +244,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_
         v[k] = make_uint4(0, 0, 0, 0);
         if (e < positions) {
           const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
-          if (hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
+          if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
             v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
           e += kHaloStep;
           b += w.b_step;
@@ -211,7 +256,10 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_
         }
       }
       if (!stage_free) {
-        if (!ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) return false;
+        // every lane runs the first batch, so the warp is converged here; the
+        // outcome is made warp-uniform because the arrive below is warp-wide
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)))
+          return false;
         stage_free = true;
       }
 #pragma unroll
@@ -219,10 +267,10 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_
         if (eb[k] < positions) halo_store_f16(hp, halo, eb[k], h, v[k]);
     } while (e < positions);
     ptx::fence_proxy_async_smem();
-    if (!((p.debug_flags & 1) && s == 0 && pt == 0)) ptx::mbar_arrive(&h_full[hs]);
+    arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
     if (++cb == p.CB) {
       cb = 0;
-      tile += gridDim.x;
+      tile += ts.step;
     }
   }
   return true;
@@ -230,9 +278,15 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, uint8_
 
 // GT > 0 fixes the run length (K-slices per filter stage) at compile time so
 // that the per-run tap loop is unrolled; GT == 0 reads it from the parameters.
-template <int BN, int GT>
+// CG == 2: CTA pairs (clusters of two) issue M = 256 MMAs whose A rows come
+// from the two CTAs' patches and whose B columns are split between them, so
+// each CTA stages half of every filter tile; rank 0 issues the MMAs, both
+// CTAs produce their own halo and drain their own 128 accumulator rows.
+template <int BN, int GT, int CG>
 __global__ void __launch_bounds__(kHaloThreads, 1)
     conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+  static_assert(CG == 1 || CG == 2, "CTA group");
+  static_assert(CG == 1 || BN >= 64, "a CTA pair splits B into halves of at least 32 rows");
   const ConvParams& p = hp.c;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -250,6 +304,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
   const int nbs = hp.nbs;
+  constexpr int BNH = BN / CG;  // filter rows (output channels) this CTA stages per K-slice
+#if defined(I8C_PIPELINE_TRACE)
+  // per-CTA span (global timer) and SM, for the pipeline analysis build only
+  if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < kTraceSlots) {
+    p.trace[8 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::globaltimer_ns());
+    p.trace[10 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::smid());
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nbs; ++i) {
@@ -257,203 +319,286 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&h_full[i], kProducers);
+      ptx::mbar_init(&h_full[i], kProducers * CG);  // a pair's rank 0 counts both CTAs' producers
       ptx::mbar_init(&h_empty[i], 1);
       ptx::mbar_init(&acc_full[i], 1);
-      ptx::mbar_init(&acc_empty[i], kEpilogue);
+      ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 1 && lane == 0) ptx::prefetch_tensormap(&tmap_f);
+  if (warp == kTmaWarp && lane == 0) ptx::prefetch_tensormap(&tmap_f);
   if (warp == 0) {
-    ptx::tmem_alloc(tmem_slot, p.tmem_cols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_cg<CG>(tmem_slot, p.tmem_cols);
+    ptx::tmem_relinquish_cg<CG>();
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     ptx::setmaxnreg_dec<kWorkerRegs>();
-    // The whole warp runs the loop in uniform control flow so that every
-    // descriptor is computed from loop counters and kernel parameters in
-    // uniform registers; one elected lane issues each MMA and commit.
-    constexpr uint32_t idesc = ptx::idesc_f16_f32(128, BN);
-    const uint32_t sbo = static_cast<uint32_t>(p.stride_h * hp.CW * 16);
-    const uint32_t lbo = hp.plane_bytes;
-    const uint64_t a_desc0 = ptx::smem_desc_noswizzle_kmajor(0, lbo, sbo);
-    const uint64_t b_desc0 = ptx::smem_desc_sw64_kmajor(0);
-    // start-address fields (16-byte units)
-    const uint32_t h_lo = ptx::smem_addr(smem) >> 4;
-    const uint32_t b_lo = ptx::smem_addr(smem + hp.off_b) >> 4;
-    const uint32_t halo_lo = hp.halo_bytes >> 4;
-    const uint32_t chunk2_lo = (2 * lbo) >> 4;
-    const int G = GT > 0 ? GT : hp.bgroup;
-    const uint32_t slice_lo = static_cast<uint32_t>(BN * 64) >> 4;
-    const uint32_t stage_lo = static_cast<uint32_t>(G) * slice_lo;
-    // tap (r, s) -> halo position r*dh*CW + phase_off(f) + idx with
-    // s*dw = idx*sw + f; phase_off(f) = f*(CW/sw) + min(f, CW%sw)
-    const int row_step = p.dil_h * hp.CW;
-    const int dw_div = p.dil_w / p.stride_w, dw_mod = p.dil_w % p.stride_w;
-    const int cw_q = hp.CW / p.stride_w, cw_r = hp.CW % p.stride_w;
-    // One flat loop over runs: a run is G taps of one filter row (one filter
-    // stage; G divides S).  Waits, releases and accumulator switches happen only
-    // at run boundaries (chunk lengths are multiples of G); the run's K-slices
-    // are unrolled into MMA pairs with affine addresses.  Counters advance with
-    // selects so that a run costs as few branches as possible -- the tensor
-    // core's instruction queue holds only about two MMAs.
-    const int runs_per_row = p.S / G;
-    const int runs_per_tile = p.CB * p.R * runs_per_row;
-    uint32_t u = 0, hseq = 0, st = 0, bph = 0, g = 0;
-    bool ok = true;
-#if defined(I8C_PIPELINE_TRACE)
-    const bool tracing = p.trace != nullptr && blockIdx.x == 0;
-    long long stall_acc = 0, stall_b = 0, stall_h = 0;
-#endif
-    trace_mark(p, 0, 0, 0);  // whole warp: no lane-dependent code around the issue loop
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      int kk = 0, next_chunk = 0;
-      uint32_t buf = 0, d_tmem = tmem_base;
-      uint32_t acc_flag = 0;  // 0 for the first MMA of a chunk, then 1
-      int rrun = 0, rrow = 0, rowpos = 0, fph = 0, idx = 0;
-      for (int run = 0; run < runs_per_tile; ++run) {
-        if (rrun == 0 && rrow == 0) {
-#if defined(I8C_PIPELINE_TRACE)
-          const long long th = tracing ? clock64() : 0;
-#endif
-          if (!__all_sync(0xffffffffu,
-                          ptx::mbar_wait(&h_full[hseq & 1u], (hseq >> 1) & 1u, p.timeout_ns, abort_flag))) {
-            ok = false;
-            break;
-          }
-#if defined(I8C_PIPELINE_TRACE)
-          if (tracing) stall_h += clock64() - th;
-#endif
-        }
-        if (kk == next_chunk) {
-          // a new exact-fp32 chunk: hand the previous accumulator to the
-          // epilogue and take the next buffer
-          if (kk != 0) {
-            if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
-            __syncwarp();
-#if defined(I8C_PIPELINE_TRACE)
-            trace_mark(p, 0, 2, u);
-#endif
-            ++u;
-          }
-          buf = u & 1u;
-          const uint32_t aph = (u >> 1) & 1u;
-#if defined(I8C_PIPELINE_TRACE)
-          const long long ta = tracing ? clock64() : 0;
-#endif
-          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&acc_empty[buf], aph ^ 1u, p.timeout_ns, abort_flag))) {
-            ok = false;
-            break;
-          }
-#if defined(I8C_PIPELINE_TRACE)
-          if (tracing) stall_acc += clock64() - ta;
-          trace_mark(p, 0, 3, u);
-#endif
-          d_tmem = tmem_base + buf * BN;
-          next_chunk = kk + p.chunk_slices;
-          acc_flag = 0;
-        }
-#if defined(I8C_PIPELINE_TRACE)
-        const long long tb = tracing ? clock64() : 0;
-#endif
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_full[st], bph, p.timeout_ns, abort_flag))) {
-          ok = false;
-          break;
-        }
-#if defined(I8C_PIPELINE_TRACE)
-        if (tracing) stall_b += clock64() - tb;
-#endif
-        ptx::tc_fence_after();
-        const uint32_t h_stage = h_lo + (hseq & 1u) * halo_lo;
-        uint32_t b_cur = b_lo + st * stage_lo;
+    const TileSched ts = tile_sched<CG>();  // per role: kept live only where used
+    if (CG == 1 || ts.rank == 0) {
+      // The whole warp runs the loop in uniform control flow so that every
+      // descriptor is computed from loop counters and kernel parameters in
+      // uniform registers; one elected lane issues each MMA and commit.
+      constexpr uint32_t idesc = ptx::idesc_f16_f32(128 * CG, BN);
+      constexpr bool kCW = CG == 2;  // barriers with arrivals from the peer CTA: cluster-scope acquire
+      constexpr uint16_t kPair = 3;  // commits of a pair signal the barrier in both CTAs
+      auto commit_all = [&](uint64_t* bar) {
+        if constexpr (CG == 2) ptx::mma_commit_pair(bar, kPair);
+        else ptx::mma_commit(bar);
+      };
+      const uint32_t sbo = static_cast<uint32_t>(p.stride_h * hp.CW * 16);
+      const uint32_t lbo = hp.plane_bytes;
+      const uint64_t a_desc0 = ptx::smem_desc_noswizzle_kmajor(0, lbo, sbo);
+      const uint64_t b_desc0 = ptx::smem_desc_sw64_kmajor(0);
+      // start-address fields (16-byte units)
+      const uint32_t h_lo = ptx::smem_addr(smem) >> 4;
+      const uint32_t b_lo = ptx::smem_addr(smem + hp.off_b) >> 4;
+      const uint32_t halo_lo = hp.halo_bytes >> 4;
+      const uint32_t chunk2_lo = (2 * lbo) >> 4;
+      const int G = GT > 0 ? GT : hp.bgroup;
+      const uint32_t slice_lo = static_cast<uint32_t>(BNH * 64) >> 4;
+      const uint32_t stage_lo = static_cast<uint32_t>(G) * slice_lo;
+      // tap (r, s) -> halo position r*dh*CW + phase_off(f) + idx with
+      // s*dw = idx*sw + f; phase_off(f) = f*(CW/sw) + min(f, CW%sw)
+      const int row_step = p.dil_h * hp.CW;
+      const int dw_div = p.dil_w / p.stride_w, dw_mod = p.dil_w % p.stride_w;
+      const int cw_q = hp.CW / p.stride_w, cw_r = hp.CW % p.stride_w;
+      // Runs: a run is one filter stage of G K-slices, G taps of one channel
+      // block -- part of a filter row (G divides S) or whole rows (S divides
+      // G, G divides R*S) -- so a run never spans two channel blocks.  Its
+      // slices are unrolled into MMA pairs whose tap addresses advance with
+      // selects.  Waits, releases and accumulator switches happen only at run
+      // boundaries (chunk lengths are multiples of G); a barrier wait costs a
+      // few hundred cycles even when its phase has completed, so fewer, longer
+      // runs keep the tensor core's short instruction queue fed.
+      const int runs_per_cb = (p.R * p.S) / G;
+      const int runs_per_tile = p.CB * runs_per_cb;
+      // GT > 0 (the host picks it only when S divides GT): a run is GT / S
+      // whole filter rows, and the halo offsets of its taps relative to its
+      // first row are the same for every run -- computed once, so a K-slice
+      // costs one add on its way to the descriptor.
+      int tapoff[GT > 0 ? GT : 1];
+      if constexpr (GT > 0) {
 #pragma unroll
-        for (int t = 0; t < G; ++t) {
-          const uint32_t a_cur = h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx);
-          const uint64_t ad0 = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
-          const uint64_t ad1 = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
-          const uint64_t bd = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
-          if (ptx::elect_one()) {
-            ptx::mma_f16_ss(d_tmem, ad0, bd, idesc, acc_flag);
-            ptx::mma_f16_ss(d_tmem, ad1, bd + 2, idesc, 1u);
-          }
-          __syncwarp();
-          acc_flag = 1;
-          b_cur += slice_lo;
-          fph += dw_mod;
-          const int carry = fph >= p.stride_w ? 1 : 0;
-          fph -= carry * p.stride_w;
-          idx += dw_div + carry;
-        }
-        if (ptx::elect_one()) ptx::mma_commit(&b_empty[st]);
-        __syncwarp();
-        st = st + 1 == static_cast<uint32_t>(nbs) ? 0u : st + 1;
-        bph ^= st == 0 ? 1u : 0u;
-        kk += G;
-        g += G;
-        // advance run -> row -> channel block with selects
-        rrun += 1;
-        const bool row_end = rrun == runs_per_row;
-        rrun = row_end ? 0 : rrun;
-        fph = row_end ? 0 : fph;
-        idx = row_end ? 0 : idx;
-        rowpos += row_end ? row_step : 0;
-        rrow += row_end ? 1 : 0;
-        if (rrow == p.R) {  // channel block done: release its halo
-          if (ptx::elect_one()) ptx::mma_commit(&h_empty[hseq & 1u]);
-          __syncwarp();
-          ++hseq;
-          rrow = 0;
-          rowpos = 0;
+        for (int t = 0; t < GT; ++t) {
+          const int r = t / p.S, sd = (t - r * p.S) * p.dil_w;
+          const int f = sd % p.stride_w;
+          tapoff[t] = r * row_step + f * cw_q + min(f, cw_r) + sd / p.stride_w;
         }
       }
-      if (!ok) break;
-      if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
-      __syncwarp();
-      ++u;
-    }
-    trace_mark(p, 0, 0, 1);
-    if (p.trace != nullptr && blockIdx.x == 0) {
-      p.trace[4 * kTraceSlots] = g;
+      const int run_rowstep = GT > 0 ? (G / p.S) * row_step : 0;
+      uint32_t u = 0, hseq = 0, st = 0, bph = 0, g = 0;
+      bool ok = true;
 #if defined(I8C_PIPELINE_TRACE)
-      p.trace[4 * kTraceSlots + 1] = stall_acc;
-      p.trace[4 * kTraceSlots + 2] = stall_b;
-      p.trace[4 * kTraceSlots + 3] = stall_h;
+      const bool tracing = p.trace != nullptr && blockIdx.x == 0;
+      long long stall_acc = 0, stall_b = 0, stall_h = 0;
+      long long nr_acc = 0, nr_b = 0, nr_h = 0;  // waits that found the phase still open
 #endif
+      auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, ptx::mbar_wait<kCW>(bar, parity, p.timeout_ns, abort_flag));
+      };
+      trace_mark(p, 0, 0, 0);  // whole warp: no lane-dependent code around the issue loop
+      for (int tile = ts.first; ok && tile < p.num_tiles; tile += ts.step) {
+        int kk = 0, next_chunk = 0;
+        uint32_t buf = 0, d_tmem = tmem_base;
+        uint32_t acc_flag = 0;  // 0 for the first MMA of a chunk, then 1
+        // tap state: column count tc within the filter row, row trow within
+        // the channel block, the halo offset of the row, column phase and index
+        // (GT > 0: only the run within the channel block and its first row)
+        int tc = 0, trow = 0, rowpos = 0, fph = 0, idx = 0, rcb = 0;
+        for (int run = 0; run < runs_per_tile; ++run) {
+          if (GT > 0 ? rcb == 0 : (tc == 0 && trow == 0)) {  // first run of a channel block: its halo
+#if defined(I8C_PIPELINE_TRACE)
+            const long long th = tracing ? clock64() : 0;
+            nr_h += ptx::mbar_test_wait<kCW>(&h_full[hseq & 1u], (hseq >> 1) & 1u) ? 0 : 1;
+#endif
+            if (!wwait(&h_full[hseq & 1u], (hseq >> 1) & 1u)) {
+              ok = false;
+              break;
+            }
+#if defined(I8C_PIPELINE_TRACE)
+            if (tracing) stall_h += clock64() - th;
+#endif
+          }
+          if (kk == next_chunk) {
+            // a new exact-fp32 chunk: hand the previous accumulator to the
+            // epilogue and take the next buffer
+            if (kk != 0) {
+              if (ptx::elect_one()) commit_all(&acc_full[buf]);
+              __syncwarp();
+#if defined(I8C_PIPELINE_TRACE)
+              trace_mark(p, 0, 2, u);
+#endif
+              ++u;
+            }
+            buf = u & 1u;
+            const uint32_t aph = (u >> 1) & 1u;
+#if defined(I8C_PIPELINE_TRACE)
+            const long long ta = tracing ? clock64() : 0;
+            nr_acc += ptx::mbar_test_wait<kCW>(&acc_empty[buf], aph ^ 1u) ? 0 : 1;
+#endif
+            if (!wwait(&acc_empty[buf], aph ^ 1u)) {
+              ok = false;
+              break;
+            }
+#if defined(I8C_PIPELINE_TRACE)
+            if (tracing) stall_acc += clock64() - ta;
+            trace_mark(p, 0, 3, u);
+#endif
+            d_tmem = tmem_base + buf * BN;
+            next_chunk = kk + p.chunk_slices;
+            acc_flag = 0;
+          }
+#if defined(I8C_PIPELINE_TRACE)
+          const long long tb = tracing ? clock64() : 0;
+          nr_b += ptx::mbar_test_wait<kCW>(&b_full[st], bph) ? 0 : 1;
+#endif
+          if (!wwait(&b_full[st], bph)) {
+            ok = false;
+            break;
+          }
+#if defined(I8C_PIPELINE_TRACE)
+          if (tracing) stall_b += clock64() - tb;
+          trace_mark(p, 0, 1, g / G);  // filter stage acquired
+#endif
+          ptx::tc_fence_after();
+          const uint32_t h_stage = h_lo + (hseq & 1u) * halo_lo;
+          uint32_t b_cur = b_lo + st * stage_lo;
+#pragma unroll
+          for (int t = 0; t < G; ++t) {
+            const uint32_t a_cur =
+                GT > 0 ? h_stage + static_cast<uint32_t>(rowpos + tapoff[GT > 0 ? t : 0])
+                       : h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx);
+            const uint64_t ad0 = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
+            const uint64_t ad1 = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
+            const uint64_t bd = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
+            if (ptx::elect_one()) {
+              if constexpr (CG == 2) {
+                ptx::mma_f16_ss_pair(d_tmem, ad0, bd, idesc, acc_flag);
+                ptx::mma_f16_ss_pair(d_tmem, ad1, bd + 2, idesc, 1u);
+              } else {
+                ptx::mma_f16_ss(d_tmem, ad0, bd, idesc, acc_flag);
+                ptx::mma_f16_ss(d_tmem, ad1, bd + 2, idesc, 1u);
+              }
+            }
+            __syncwarp();
+            acc_flag = 1;
+            b_cur += slice_lo;
+            if constexpr (GT > 0) continue;
+            // next tap: column s + 1 of the row (s*dw = idx*sw + fph), or the
+            // first column of the next row, or of the first row after the
+            // channel block's last tap
+            fph += dw_mod;
+            const int carry = fph >= p.stride_w ? 1 : 0;
+            fph -= carry * p.stride_w;
+            idx += dw_div + carry;
+            ++tc;
+            const bool row_end = tc == p.S;
+            tc = row_end ? 0 : tc;
+            fph = row_end ? 0 : fph;
+            idx = row_end ? 0 : idx;
+            rowpos += row_end ? row_step : 0;
+            trow += row_end ? 1 : 0;
+            const bool cb_end = trow == p.R;
+            trow = cb_end ? 0 : trow;
+            rowpos = cb_end ? 0 : rowpos;
+          }
+          if (ptx::elect_one()) commit_all(&b_empty[st]);
+          __syncwarp();
+#if defined(I8C_PIPELINE_TRACE)
+          trace_mark(p, 1, 2, g / G);  // filter stage released (commit issued)
+#endif
+          st = st + 1 == static_cast<uint32_t>(nbs) ? 0u : st + 1;
+          bph ^= st == 0 ? 1u : 0u;
+          kk += G;
+          g += G;
+          bool cb_done = tc == 0 && trow == 0;
+          if constexpr (GT > 0) {
+            rowpos += run_rowstep;
+            cb_done = ++rcb == runs_per_cb;
+            rcb = cb_done ? 0 : rcb;
+            rowpos = cb_done ? 0 : rowpos;
+          }
+          if (cb_done) {  // channel block done: release its halo
+            if (ptx::elect_one()) commit_all(&h_empty[hseq & 1u]);
+            __syncwarp();
+            ++hseq;
+          }
+        }
+        if (!ok) break;
+        if (ptx::elect_one()) commit_all(&acc_full[buf]);
+        __syncwarp();
+        ++u;
+      }
+      trace_mark(p, 0, 0, 1);
+      if (p.trace != nullptr && blockIdx.x == 0) {
+        p.trace[4 * kTraceSlots] = g;
+#if defined(I8C_PIPELINE_TRACE)
+        p.trace[4 * kTraceSlots + 1] = stall_acc;
+        p.trace[4 * kTraceSlots + 2] = stall_b;
+        p.trace[4 * kTraceSlots + 3] = stall_h;
+        p.trace[4 * kTraceSlots + 4] = nr_acc;
+        p.trace[4 * kTraceSlots + 5] = nr_b;
+        p.trace[4 * kTraceSlots + 6] = nr_h;
+#endif
+      }
+      if (!ok && lane == 0) raise_timeout(p, abort_flag);
+      // every MMA issued by this warp has completed before TMEM is freed
+      // (a pair's rank 1 learns it through the final cluster barrier)
+      if (ptx::elect_one()) {
+        if constexpr (CG == 2) ptx::mma_commit_pair(drain, 1);
+        else ptx::mma_commit(drain);
+      }
+      __syncwarp();
+      if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
     }
-    if (!ok && lane == 0) raise_timeout(p, abort_flag);
-    // every MMA issued by this warp has completed before TMEM is freed
-    if (ptx::elect_one()) ptx::mma_commit(drain);
-    __syncwarp();
-    if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
-  } else if (warp == 1) {
+  } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
     ptx::setmaxnreg_dec<kWorkerRegs>();
+    // the fp16 filter is written by the conversion kernel launched just
+    // before this one, which this kernel may overlap (dependent launch)
+    ptx::griddep_wait();
+    const TileSched ts = tile_sched<CG>();
     const int G = GT > 0 ? GT : hp.bgroup;
-    const uint32_t stage_bytes = static_cast<uint32_t>(G * BN * 64);
+    const uint32_t stage_bytes = static_cast<uint32_t>(G * BNH * 64);
     uint32_t g = 0, st = 0, bph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const int n0 = (tile % p.num_n_tiles) * BN;
+    for (int tile = ts.first; ok && tile < p.num_tiles; tile += ts.step) {
+      const int n0 = (tile % p.num_n_tiles) * BN + ts.rank * BNH;
       for (int kk = 0; kk < p.num_slices; kk += G, ++g) {
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_empty[st], bph ^ 1u, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
-        // G consecutive K-slices; slices past the end of the filter read as zeros
+#if defined(I8C_PIPELINE_TRACE)
+        trace_mark(p, 1, 3, g);  // slot free
+#endif
+        // G consecutive K-slices; slices past the end of the filter read as
+        // zeros.  A pair's two halves both complete on rank 0's barrier.
         if (ptx::elect_one()) {
-          ptx::mbar_arrive_expect_tx(&b_full[st], stage_bytes);
-          ptx::tma_load_3d(smem + hp.off_b + st * stage_bytes, &tmap_f, &b_full[st], 0, n0, kk);
+          uint8_t* dst = smem + hp.off_b + st * stage_bytes;
+          if constexpr (CG == 1) {
+            ptx::mbar_arrive_expect_tx(&b_full[st], stage_bytes);
+            ptx::tma_load_3d(dst, &tmap_f, &b_full[st], 0, n0, kk);
+          } else if (ts.rank == 0) {
+            ptx::mbar_arrive_expect_tx(&b_full[st], 2 * stage_bytes);
+            ptx::tma_load_3d_pair(dst, &tmap_f, ptx::smem_addr(&b_full[st]), 0, n0, kk);
+          } else {
+            ptx::tma_load_3d_pair(dst, &tmap_f, ptx::mapa(ptx::smem_addr(&b_full[st]), 0), 0, n0, kk);
+          }
         }
         __syncwarp();
+#if defined(I8C_PIPELINE_TRACE)
+        trace_mark(p, 1, 1, g);  // load issued
+#endif
         if (++st == static_cast<uint32_t>(nbs)) {
           st = 0;
           bph ^= 1u;
@@ -461,15 +606,16 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       }
     }
     if (!ok && lane == 0) raise_timeout(p, abort_flag);
-    // wait for the loads still in flight (at most one per stage)
+    // wait for the loads still in flight (at most one per stage); rank 0 of a
+    // pair waits for both CTAs' halves, which rank 1 cannot observe
     const uint32_t first = g > static_cast<uint32_t>(nbs) ? g - nbs : 0u;
-    for (uint32_t i = first; i < g; ++i) {
-      if (!ptx::mbar_wait(&b_full[i % nbs], (i / nbs) & 1u, p.timeout_ns, nullptr)) {
+    for (uint32_t i = (CG == 2 && ts.rank != 0) ? g : first; i < g; ++i) {
+      if (!ptx::mbar_wait<CG == 2>(&b_full[i % nbs], (i / nbs) & 1u, p.timeout_ns, nullptr)) {
         if (lane == 0) raise_timeout(p, abort_flag);
         break;
       }
     }
-  } else if (warp >= 2 && warp < 8) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ halo producers
     // Thread pt owns the 16-byte half (pt & 1) of halo positions
     // e = pt/2 + k*(kProducers/2), k = 0, 1, ...  Two ways to bring a channel
@@ -480,9 +626,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // memory, which leaves room for longer filter stages).  Either way the
     // bytes are converted to fp16 and stored into the free halo stage.
     ptx::setmaxnreg_dec<kWorkerRegs>();
-    const int pt = threadIdx.x - 64;
-    const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_direct(hp, smem, h_full, h_empty, abort_flag, pt);
+    const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
+    const TileSched ts = tile_sched<CG>();
+    const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
+                                : halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
@@ -502,11 +649,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     uint32_t run[kColsPerWarp];  // running int32 sums of this thread's pixel over its columns
     uint32_t u = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const PatchTile t = decode_patch(tile, hp);
-      const int pp = t.p0 + (row >> 3);
-      const int qq = t.q0 + (row & 7);
-      const bool valid = pp < p.P && qq < p.Q;
+    for (int tile = tile_sched<CG>().first; ok && tile < p.num_tiles; tile += tile_sched<CG>().step) {
       for (int c = 0; c < p.num_chunks; ++c, ++u) {
         const uint32_t buf = u & 1u;
 #if defined(I8C_PIPELINE_TRACE)
@@ -536,13 +679,17 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             }
           }
         }
-        // the accumulator buffer is free once read
+        // the accumulator buffer is free once read (a pair's rank 0 waits for both CTAs)
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&acc_empty[buf]);
+        arrive_on_leader(&acc_empty[buf], tile_sched<CG>());
 #if defined(I8C_PIPELINE_TRACE)
         if (warp == 8 && lane == 0) trace_mark(p, 3, 2, u);
 #endif
-        if (c + 1 == p.num_chunks && col_owner && valid) {
+        if (c + 1 < p.num_chunks || !col_owner) continue;
+        const PatchTile t = decode_patch(tile, hp, tile_sched<CG>());
+        const int pp = t.p0 + (row >> 3);
+        const int qq = t.q0 + (row & 7);
+        if (t.valid && pp < p.P && qq < p.Q) {
 #pragma unroll
           for (int g = 0; g < kColsPerWarp / 32; ++g) {
             const int k0 = t.nt * BN + col0 + g * 32;
@@ -576,9 +723,17 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair's CTAs leave together: no remote arrive, multicast commit or MMA
+  // operand read targets a CTA that has exited, and both free their tensor
+  // memory together.
+  if (CG == 2) ptx::cluster_sync();
+#if defined(I8C_PIPELINE_TRACE)
+  if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < kTraceSlots)
+    p.trace[9 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::globaltimer_ns());
+#endif
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+    ptx::tmem_dealloc_cg<CG>(tmem_base, p.tmem_cols);
   }
 }
 

@@ -1,4 +1,4 @@
-// Instantiations and launch of the tcgen05 implicit-GEMM kernel per tile width.
+// Instantiations and launch of the per-tap gather kernel per tile width.
 #include "internal.h"
 
 namespace i8c {
@@ -45,45 +45,6 @@ cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& 
     case 64: return launch_one<64>(tmap, p, num_ctas, stream);
     case 128: return launch_one<128>(tmap, p, num_ctas, stream);
     case 256: return launch_one<256>(tmap, p, num_ctas, stream);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int BN>
-static cudaError_t halo_prepare_one() {
-  cudaError_t e = cudaFuncSetAttribute(conv_fprop_halo_kernel<BN, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxDynamicSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(conv_fprop_halo_kernel<BN, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMaxDynamicSmem);
-}
-
-cudaError_t conv_halo_prepare(int block_n) {
-  switch (block_n) {
-    case 32: return halo_prepare_one<32>();
-    case 64: return halo_prepare_one<64>();
-    case 128: return halo_prepare_one<128>();
-    case 256: return halo_prepare_one<256>();
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int BN>
-static cudaError_t halo_launch_one(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
-                                   cudaStream_t stream) {
-  if (p.bgroup == 3) conv_fprop_halo_kernel<BN, 3><<<num_ctas, kHaloThreads, smem, stream>>>(tmap, p);
-  else conv_fprop_halo_kernel<BN, 0><<<num_ctas, kHaloThreads, smem, stream>>>(tmap, p);
-  g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_conv_halo(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
-                             cudaStream_t stream) {
-  switch (block_n) {
-    case 32: return halo_launch_one<32>(tmap, p, smem_bytes, num_ctas, stream);
-    case 64: return halo_launch_one<64>(tmap, p, smem_bytes, num_ctas, stream);
-    case 128: return halo_launch_one<128>(tmap, p, smem_bytes, num_ctas, stream);
-    case 256: return halo_launch_one<256>(tmap, p, smem_bytes, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

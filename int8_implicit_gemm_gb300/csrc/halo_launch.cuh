@@ -1,0 +1,80 @@
+// Instantiation, shared-memory set-up and launch of the halo kernel for one
+// CTA-group size (included by one translation unit per size, so that the two
+// sets of instantiations compile in parallel).
+#pragma once
+
+#include "internal.h"
+
+namespace i8c {
+
+using HaloKernel = void (*)(const CUtensorMap, const HaloParams);
+
+// Run lengths with an unrolled tap loop and precomputed tap offsets, for runs
+// of whole filter rows (S divides the run length): 3 (a row of a 3x3
+// filter) and 9 (a whole 3x3 channel block, or a row of a 9-wide filter);
+// every other run takes the generic instantiation (GT = 0).
+template <int BN, int CG>
+HaloKernel halo_kernel_for(int bgroup, int S) {
+  if (bgroup == 3 && 3 % S == 0) return conv_fprop_halo_kernel<BN, 3, CG>;
+  if (bgroup == 9 && 9 % S == 0) return conv_fprop_halo_kernel<BN, 9, CG>;
+  return conv_fprop_halo_kernel<BN, 0, CG>;
+}
+
+template <int BN, int CG>
+cudaError_t halo_prepare_bn() {
+  for (int g : {3, 9, 0}) {
+    const cudaError_t e = cudaFuncSetAttribute(halo_kernel_for<BN, CG>(g, 1),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// CTA pairs are launched as clusters of two.  Single CTAs are launched as
+// programmatic dependents of the filter conversion kernel: their prologue
+// (barriers, tensor memory, halo loads) overlaps that kernel's tail and only
+// the filter loads wait for it.
+template <int CG>
+cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
+  cfg.blockDim = dim3(kHaloThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int BN, int CG>
+cudaError_t halo_launch_bn(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
+                           cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, p);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Clusters of two that can be resident at once (0 if the query fails).
+template <int BN>
+int halo_max_clusters_bn(int bgroup, int S, int smem) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = halo_launch_config<2>(smem, 2, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(halo_kernel_for<BN, 2>(bgroup, S)), &cfg) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace i8c

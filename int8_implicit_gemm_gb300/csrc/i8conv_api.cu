@@ -19,7 +19,8 @@ struct i8c_plan {
   int P, Q;
   int64_t M;
   int device;
-  int kernel_variant;  // 1 = per-tap gather kernel, 2 = halo kernel
+  int kernel_variant;  // 1 = per-tap gather kernel, 2 = halo kernel, 3 = halo kernel on CTA pairs
+  int cta_group;       // CTAs per MMA tile: 2 for variant 3, else 1
   int block_n, num_n_tiles, num_m_tiles, num_tiles, num_ctas;
   i8c::HaloParams halo;  // geometry and shared-memory layout of the halo kernel
   int num_slices, chunk_slices, num_chunks, acc_buffers;
@@ -109,16 +110,20 @@ double wave_efficiency(int64_t tiles, int ctas) {
   return static_cast<double>(tiles) / static_cast<double>(waves * ctas);
 }
 
-// Halo geometry and shared-memory layout for a tile width; returns false when
-// the halo does not fit with at least three filter stages.
-// Shared-memory layout of the halo kernel for tile width bn: two fp16 halo
+// Halo geometry and shared-memory layout of the halo kernel for tile width bn
+// on cg CTAs (each CTA of a pair stages bn/2 filter rows): two fp16 halo
 // stages, the int8 staging ring (if any), the filter stages, the barriers.
-// loads: 0 = auto, 1 = staging ring only, 2 = register loads only.
-bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int loads, i8c::HaloParams* h, int* smem_bytes) {
+// loads: 0 = auto, 1 = staging ring only, 2 = register loads only.  Returns
+// false when the halo does not fit with at least three filter stages.
+bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int loads, i8c::HaloParams* h,
+                 int* smem_bytes) {
   if (s.stride_w > 8) return false;
   *h = i8c::HaloParams{};
   h->TPH = (P + 15) / 16;
   h->TQW = (Q + 7) / 8;
+  const int64_t patches = static_cast<int64_t>(s.N) * h->TPH * h->TQW;
+  if (patches > kMaxI32) return false;
+  h->num_patches = static_cast<int>(patches);
   const int64_t HR = 15LL * s.stride_h + static_cast<int64_t>(s.R - 1) * s.dil_h + 1;
   const int64_t CW = 7LL * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
   if (HR * CW > 65536) return false;
@@ -134,24 +139,30 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int loads, i8c::
     off += static_cast<int>((CW - f + s.stride_w - 1) / s.stride_w);
   }
   h->phase_off[s.stride_w] = off;
-  // Filter stages of G K-slices each, G a divisor of S so that a stage is a
-  // run of taps of one filter row: the largest such G with G*BN <= 1024 and at
-  // least three stages in shared memory.  The producers load into registers
-  // unless the staging ring (three slots, else two) is asked for: measured on
-  // the 3x3 layers, the ring's deeper prefetch gains nothing at width 256
-  // and costs filter stages.
+  // Filter stages of G K-slices each: a run of taps of one channel block,
+  // either part of a filter row (G divides S) or whole rows (S divides G, G
+  // divides R*S).  Longer stages need fewer barrier waits per MMA, so the
+  // largest G is taken that leaves at least three stages (two for whole-row
+  // stages, which are long enough to double-buffer) beside the halo.  The
+  // producers load into registers unless the staging ring (three slots, else
+  // two) is asked for: measured on the 3x3 layers, the ring's deeper prefetch
+  // gains nothing and costs filter stages.
   const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
   static const int kSlots[3] = {3, 2, 0};
   const int first = loads == 1 ? 0 : 2, last = loads == 1 ? 1 : 2;
-  for (int G = s.S; G >= 1; --G) {
-    if (s.S % G != 0 || G * bn > 1024 || G > 32) continue;
+  const int RS = s.R * s.S;
+  for (int G = RS; G >= 1; --G) {
+    const bool part_row = s.S % G == 0;
+    const bool whole_rows = G % s.S == 0 && RS % G == 0;
+    if (!(part_row || whole_rows) || G > 32) continue;
+    const int min_stages = part_row ? 3 : 2;
     for (int k = first; k <= last; ++k) {
       const int nstg = kSlots[k];
       const int64_t off_stg = 2LL * h->halo_bytes;
       const int64_t off_b = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
       const int64_t room = budget - off_b;
-      const int64_t stage = static_cast<int64_t>(G) * bn * 64;
-      if (room < 3 * stage) continue;
+      const int64_t stage = static_cast<int64_t>(G) * (bn / cg) * 64;
+      if (room < min_stages * stage) continue;
       int64_t nbs = room / stage;
       if (nbs > i8c::kMaxBStages) nbs = i8c::kMaxBStages;
       h->bgroup = G;
@@ -231,10 +242,12 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
     e = cudaEventRecord(pl->ev_start[pl->ev_recorded % nev], stream);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  if (pl->kernel_variant == 2) {
+  if (pl->kernel_variant >= 2) {
     i8c::HaloParams hp = pl->halo;
     hp.c = p;
-    e = i8c::launch_conv_halo(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream);
+    e = pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+                                : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
+                                                          stream);
   } else {
     e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
   }
@@ -318,7 +331,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 2 || o.halo_loads < 0 || o.halo_loads > 2)
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -342,37 +355,54 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
   // Kernel and tile width.  The halo kernel (16x8 output patches) is preferred
   // whenever its halo fits in shared memory; its tile width is the one with
-  // the best wave efficiency (ties go to the wider tile).
-  int bn = 0, halo_smem = 0;
+  // the best wave efficiency (ties go to the wider tile).  Variant 3 runs it
+  // on CTA pairs (clusters of two): one M = 256 MMA per K-step for two
+  // patches, each CTA staging half of the filter tile.
+  int bn = 0, halo_smem = 0, groups = 0;
   p->kernel_variant = 1;
+  p->cta_group = 1;
   if (o.kernel_variant != 1) {
-    int best_bn = 0;
+    const int cg = o.kernel_variant == 3 ? 2 : 1;
+    int best_bn = 0, best_groups = 0;
     double best = -1.0;
     for (int cand : {256, 128, 64, 32}) {
       if (o.block_n != 0 && cand != o.block_n) continue;
-      if (o.block_n == 0 && cand > 32 && cand / 2 >= s.K) continue;
+      if (cg == 2 && cand < 64) continue;
+      if (o.block_n == 0 && cand > 32 * cg && cand / 2 >= s.K) continue;  // half the tile would be empty
       i8c::HaloParams h;
       int sm = 0;
-      if (!halo_layout(s, p->P, p->Q, cand, o.halo_loads, &h, &sm)) continue;
+      if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, &h, &sm)) continue;
+      int g = ctas / cg;
+      if (cg == 2) {
+        // pairs that fit on the GPU at once (clusters need both SMs free)
+        if (i8c::halo_prepare_pair(cand) != cudaSuccess) continue;
+        const int fit = i8c::halo_pair_max_clusters(cand, h.bgroup, s.S, sm);
+        if (fit < 1) continue;
+        if (g > fit) g = fit;
+        if (g < 1) g = 1;
+      }
       const int nt = (s.K + cand - 1) / cand;
-      const int64_t t = static_cast<int64_t>(s.N) * h.TPH * h.TQW * nt;
+      const int64_t t = (static_cast<int64_t>(h.num_patches) + cg - 1) / cg * nt;
       // narrower MMAs leave the issuing warp's per-slice overhead exposed (the
       // tensor core queues only about two MMAs); measured relative rates
       double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
       // runs of one K-slice (no room for longer filter stages) issue poorly
       if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
       const double score =
-          wave_efficiency(t, ctas) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
+          wave_efficiency(t, g) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
       if (score > best * 1.02) {
         best = score;
         best_bn = cand;
+        best_groups = g;
       }
     }
     if (best_bn != 0) {
       bn = best_bn;
-      p->kernel_variant = 2;
-      halo_layout(s, p->P, p->Q, bn, o.halo_loads, &p->halo, &halo_smem);
-    } else if (o.kernel_variant == 2) {
+      groups = best_groups;
+      p->kernel_variant = cg == 2 ? 3 : 2;
+      p->cta_group = cg;
+      halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, &p->halo, &halo_smem);
+    } else if (o.kernel_variant >= 2) {
       delete p;
       return I8C_ERR_UNSUPPORTED;
     }
@@ -383,8 +413,9 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   }
   p->block_n = bn;
   p->num_n_tiles = (s.K + bn - 1) / bn;
-  const int64_t m_tiles = p->kernel_variant == 2 ? static_cast<int64_t>(s.N) * p->halo.TPH * p->halo.TQW
-                                                 : (p->M + 127) / 128;
+  const int64_t m_tiles = p->kernel_variant >= 2
+                              ? (static_cast<int64_t>(p->halo.num_patches) + p->cta_group - 1) / p->cta_group
+                              : (p->M + 127) / 128;
   const int64_t tiles = m_tiles * p->num_n_tiles;
   if (tiles > kMaxI32) {
     delete p;
@@ -392,10 +423,11 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   }
   p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
-  p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+  if (p->cta_group == 2) p->num_ctas = 2 * (groups < p->num_tiles ? groups : p->num_tiles);
+  else p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
   p->num_slices = (s.C / 32) * s.R * s.S;
   int max_chunk = o.max_chunk_slices > 0 ? o.max_chunk_slices : 32;
-  if (p->kernel_variant == 2) {
+  if (p->kernel_variant >= 2) {
     // the halo kernel switches accumulators only between filter stages
     const int G = p->halo.bgroup;
     max_chunk = max_chunk / G * G;
@@ -403,11 +435,11 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   }
   p->num_chunks = (p->num_slices + max_chunk - 1) / max_chunk;
   p->chunk_slices = (p->num_slices + p->num_chunks - 1) / p->num_chunks;
-  if (p->kernel_variant == 2) {
+  if (p->kernel_variant >= 2) {
     p->chunk_slices = (p->chunk_slices + p->halo.bgroup - 1) / p->halo.bgroup * p->halo.bgroup;
     p->num_chunks = (p->num_slices + p->chunk_slices - 1) / p->chunk_slices;
   }
-  if (p->kernel_variant == 2) {
+  if (p->kernel_variant >= 2) {
     // halo kernel: two fp32 chunk accumulators; running sums live in registers
     p->acc_buffers = 2;
     p->tmem_cols = static_cast<uint32_t>(next_pow2(2 * bn));
@@ -416,14 +448,16 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
     p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
   }
-  p->smem_bytes = p->kernel_variant == 2 ? halo_smem : i8c::conv_smem_bytes(bn);
+  p->smem_bytes = p->kernel_variant >= 2 ? halo_smem : i8c::conv_smem_bytes(bn);
   p->timeout_ns = static_cast<uint64_t>(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
   p->debug_flags = o.debug_flags;
   p->x_bytes = static_cast<size_t>(s.N) * s.C * s.H * s.W;
   p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
   p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
 
-  e = p->kernel_variant == 2 ? i8c::conv_halo_prepare(bn) : i8c::conv_prepare(bn);
+  e = p->kernel_variant == 3   ? i8c::halo_prepare_pair(bn)
+      : p->kernel_variant == 2 ? i8c::halo_prepare_single(bn)
+                               : i8c::conv_prepare(bn);
   if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
@@ -453,11 +487,12 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   }
 
   // fp16 filter as a 3-D tensor {32 channels, K, C/32*R*S}; one box is the
-  // 32-channel rows of BN output channels for one K-slice, 64-byte swizzled.
+  // 32-channel rows of the output channels one CTA stages (BN, or BN/2 per
+  // CTA of a pair) for a run of K-slices, 64-byte swizzled.
   cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(s.K), static_cast<cuuint64_t>(p->num_slices)};
   cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(s.K) * 64};
-  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn),
-                       static_cast<cuuint32_t>(p->kernel_variant == 2 ? p->halo.bgroup : 1)};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn / p->cta_group),
+                       static_cast<cuuint32_t>(p->kernel_variant >= 2 ? p->halo.bgroup : 1)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p->f16, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -487,7 +522,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->M = pl->M;
   info->gemm_n = s.K;
   info->gemm_k = s.C * s.R * s.S;
-  info->block_m = 128;
+  info->block_m = 128 * pl->cta_group;
   info->block_n = pl->block_n;
   info->num_tiles = pl->num_tiles;
   info->num_ctas = pl->num_ctas;
@@ -497,9 +532,9 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->smem_bytes = pl->smem_bytes;
   info->kernels_per_run = 2;
   info->kernel_variant = pl->kernel_variant;
-  info->halo_staging = pl->kernel_variant == 2 ? pl->halo.nstg : 0;
-  info->filter_run = pl->kernel_variant == 2 ? pl->halo.bgroup : 1;
-  info->filter_stages = pl->kernel_variant == 2 ? pl->halo.nbs
+  info->halo_staging = pl->kernel_variant >= 2 ? pl->halo.nstg : 0;
+  info->filter_run = pl->kernel_variant >= 2 ? pl->halo.bgroup : 1;
+  info->filter_stages = pl->kernel_variant >= 2 ? pl->halo.nbs
                         : pl->block_n >= 256 ? i8c::TileCfg<256>::kStages
                         : pl->block_n >= 128 ? i8c::TileCfg<128>::kStages
                                              : i8c::TileCfg<64>::kStages;

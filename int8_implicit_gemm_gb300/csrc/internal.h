@@ -20,9 +20,16 @@ cudaError_t conv_prepare(int block_n);  // raise the dynamic shared memory limit
 cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& p, int num_ctas,
                         cudaStream_t stream);
 
-cudaError_t conv_halo_prepare(int block_n);  // allow the full dynamic shared memory
-cudaError_t launch_conv_halo(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
-                             cudaStream_t stream);
+// halo_kernels_single.cu / halo_kernels_pair.cu: the halo kernel on single
+// CTAs and on CTA pairs (clusters of two); prepare allows the full dynamic
+// shared memory, max_clusters is the number of pairs that fit at once.
+cudaError_t halo_prepare_single(int block_n);
+cudaError_t halo_launch_single(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes,
+                               int num_ctas, cudaStream_t stream);
+cudaError_t halo_prepare_pair(int block_n);
+cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes,
+                             int num_ctas, cudaStream_t stream);
+int halo_pair_max_clusters(int block_n, int bgroup, int S, int smem_bytes);
 constexpr int kMaxDynamicSmem = 232448;
 
 // layout_kernels.cu

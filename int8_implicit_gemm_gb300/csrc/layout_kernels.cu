@@ -9,6 +9,9 @@ namespace i8c {
 // CxRSKx<32> int8 -> the same layout in fp16 (the tensor-core operand type).
 // 16 int8 in, 16 fp16 out per thread step; count is a multiple of 32.
 __global__ void filter_to_f16_kernel(const int8_t* __restrict__ f, uint16_t* __restrict__ out, int64_t vecs) {
+  // the convolution kernel that follows waits for this grid's completion
+  // before it reads the converted filter; it may launch right away
+  ptx::griddep_launch_dependents();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < vecs;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int4 v = reinterpret_cast<const int4*>(f)[i];
@@ -32,6 +35,9 @@ cudaError_t launch_filter_to_f16(const int8_t* f, uint16_t* f16, int64_t count, 
   int64_t blocks = (vecs + threads - 1) / threads;
   if (blocks > 4096) blocks = 4096;
   if (blocks < 1) blocks = 1;
+  static const cudaError_t carveout = cudaFuncSetAttribute(
+      filter_to_f16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  (void)carveout;  // a preference only: the kernel runs either way
   filter_to_f16_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(f, f16, vecs);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return cudaGetLastError();

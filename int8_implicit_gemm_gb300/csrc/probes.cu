@@ -114,11 +114,16 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
         out[3 * blockIdx.x + 1] = t2 - t0;
         out[3 * blockIdx.x + 2] = done ? 1 : 0;
       }
-    } else if (loop_mode == 8 || loop_mode == 9) {
+    } else if (loop_mode == 8 || loop_mode == 9 || (loop_mode >= 15 && loop_mode <= 18)) {
       // mode 8: the convolution kernel's run loop verbatim (runs of 3 K-slices,
       // a completed-barrier wait + fence before each run, column-phase
       // arithmetic, a commit after each run); mode 9: the same with the tap
-      // address advanced by a constant
+      // address advanced by a constant.  Modes 15-18 take parts away: 15 no
+      // commit, 16 no barrier wait, 17 one elected block per run (all six
+      // MMAs and the commit), 18 as 17 without wait and commit.
+      const bool do_commit = loop_mode != 15 && loop_mode != 18;
+      const bool do_wait = loop_mode != 16 && loop_mode != 18;
+      const bool per_run = loop_mode == 17 || loop_mode == 18;
       __shared__ uint64_t full3;
       if (threadIdx.x == 0) {
         ptx::mbar_init(&full3, 1);
@@ -136,11 +141,39 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
       uint32_t acc_flag = 0;
       const long long t0 = clock64();
       for (int run = 0; run < iters / (2 * G); ++run) {
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full3, 0, 1000000000ull, nullptr))) break;
-        ptx::tc_fence_after();
+        if (do_wait) {
+          if (!__all_sync(0xffffffffu, ptx::mbar_wait(&full3, 0, 1000000000ull, nullptr))) break;
+          ptx::tc_fence_after();
+        }
         uint32_t b_cur = b_lo0 + static_cast<uint32_t>(run & 1) * slice_lo;
         int fph = 0, idx = 0;
         const int rowpos = (run % S) * (10 + rt);
+        if (per_run) {
+          uint64_t a0[3], a1[3], bq[3];
+#pragma unroll
+          for (int t = 0; t < 3; ++t) {
+            const uint32_t a_cur = h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx);
+            a0[t] = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
+            a1[t] = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
+            bq[t] = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
+            b_cur += slice_lo;
+            fph += dw_mod;
+            const int carry = fph >= sw ? 1 : 0;
+            fph -= carry * sw;
+            idx += dw_div + carry;
+          }
+          if (ptx::elect_one()) {
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+              ptx::mma_f16_ss(tmem, a0[t], bq[t], idesc, acc_flag | static_cast<uint32_t>(t));
+              ptx::mma_f16_ss(tmem, a1[t], bq[t] + 2, idesc, 1u);
+            }
+            if (do_commit) ptx::mma_commit(&sink2);
+          }
+          __syncwarp();
+          acc_flag = 1;
+          continue;
+        }
         for (int t = 0; t < G; ++t) {
           const uint32_t a_cur = loop_mode == 8
                                      ? h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx)
@@ -160,8 +193,10 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
           fph -= carry * sw;
           idx += dw_div + carry;
         }
-        if (ptx::elect_one()) ptx::mma_commit(&sink2);
-        __syncwarp();
+        if (do_commit) {
+          if (ptx::elect_one()) ptx::mma_commit(&sink2);
+          __syncwarp();
+        }
         (void)S;
       }
       const long long t1 = clock64();

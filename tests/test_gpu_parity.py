@@ -38,8 +38,10 @@ def _data(shape, seed, lo=-128, hi=127):
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("alpha", [2.0 ** -9, 1.0 / 3.0])
 @pytest.mark.parametrize("kernel", [dict(kernel_variant=1), dict(kernel_variant=2),
-                                    dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2)],
-                         ids=["gather", "halo", "halo-staged", "halo-direct"])
+                                    dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
+                                    dict(kernel_variant=3), dict(kernel_variant=3, block_n=64),
+                                    dict(kernel_variant=3, block_n=256, halo_loads=1)],
+                         ids=["gather", "halo", "halo-staged", "halo-direct", "pair", "pair-64", "pair-256-staged"])
 def test_small_shapes_exact(shape, alpha, kernel):
     x, f = _data(shape, 1000 + sum(shape))
     y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, alpha)
@@ -55,6 +57,8 @@ def test_small_shapes_exact(shape, alpha, kernel):
     dict(kernel_variant=1, block_n=64), dict(kernel_variant=2, block_n=256, max_chunk_slices=7),
     dict(kernel_variant=2, block_n=32, num_ctas=5), dict(kernel_variant=2, block_n=256, halo_loads=2),
     dict(kernel_variant=2, block_n=128, halo_loads=1, num_ctas=7),
+    dict(kernel_variant=3, num_ctas=2), dict(kernel_variant=3, num_ctas=6, max_chunk_slices=3),
+    dict(kernel_variant=3, block_n=128, max_chunk_slices=1), dict(kernel_variant=3, block_n=256, num_ctas=4),
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_plan_options_exact(opts):
     shape = (2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1)
@@ -111,24 +115,24 @@ def test_deterministic_repeat():
 
 
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
-@pytest.mark.parametrize("loads", [0, 1, 2], ids=["auto", "staged", "direct"])
-def test_full_size_workloads(wl, loads):
+@pytest.mark.parametrize("kw", [{}, dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
+                                dict(kernel_variant=3)], ids=["auto", "staged", "direct", "pair"])
+def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
-    benchmark times (auto) and with each halo load form forced: sampled
-    outputs against the oracle point by point, and y == epilogue(acc) at every
-    output element."""
+    benchmark times (auto), with each halo load form forced and on CTA pairs:
+    sampled outputs against the oracle point by point, and y == epilogue(acc)
+    at every output element."""
     import int8_implicit_gemm_gb300 as ext
     shape = wl.shape_tuple()
-    if loads:
+    if kw:
         try:
-            ext.Plan(shape, kernel_variant=2, halo_loads=loads).destroy()
+            ext.Plan(shape, **kw).destroy()
         except ext.I8ConvError as e:
             if e.status == ext.I8C_ERR_UNSUPPORTED:
-                pytest.skip("this halo load form does not fit")
+                pytest.skip("this kernel form does not fit")
             raise
     x = wl.activations_nchw()
     f = wl.filters_kcrs()
-    kw = dict(kernel_variant=2, halo_loads=loads) if loads else {}
     y, acc = gpu_util.gpu_run(shape, x, f, wl.alpha, **kw)
     orc = oracle.Oracle()
     P, Q = orc.out_size(shape)
