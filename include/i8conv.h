@@ -85,6 +85,11 @@ typedef struct {
                                 cp.async ahead of use, 2 = straight into registers (no
                                 staging memory); I8C_ERR_UNSUPPORTED if the forced form
                                 does not fit                                               */
+  int32_t tail_split;        /* halo kernel, tiles of a partial last wave split along the
+                                channel blocks (int32 partial sums combined by the unit that
+                                finishes last; needs plan workspace): 0 = when the estimated
+                                saving clearly exceeds the partial-sum traffic, 1 = never,
+                                2 = whenever the last wave is partial                       */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so
@@ -119,6 +124,8 @@ typedef struct {
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of
                                 one filter row); 1 for the gather kernel       */
   int32_t filter_stages;     /* filter pipeline stages in shared memory        */
+  int32_t tail_split;        /* units each last-wave tile is split into (1: none) */
+  int32_t work_units;        /* units of work the persistent CTAs share          */
 } i8c_plan_info;
 
 /* Output height P and width Q for a shape (formula above).  Returns

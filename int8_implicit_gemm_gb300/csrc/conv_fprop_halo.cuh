@@ -39,6 +39,13 @@ struct HaloParams {
   int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
   uint32_t off_stg, off_b, off_bar;
   int phase_off[9];         // first position of column phase f (f < sw); phase_off[sw] = CW
+  // Work units: tiles [0, full_units) whole; the remaining tiles (the last,
+  // partial wave) each split into ksplit units over ranges of channel blocks,
+  // whose int32 partial sums meet in split_part and are combined by the unit
+  // that finishes last (split_count: arrivals per tile and CTA rank).
+  int num_units, full_units, ksplit;
+  int* split_count;         // [tail tiles][cg], zero between launches
+  int32_t* split_part;      // [tail tiles][ksplit][cg][BN/4][128][4]
 };
 
 
@@ -131,11 +138,41 @@ __device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
   return (pos - hp.phase_off[f]) * hp.c.stride_w + f;
 }
 
-__device__ __forceinline__ uint32_t halo_stage_count(const HaloParams& hp, const TileSched& ts) {
-  const ConvParams& p = hp.c;
-  const int tiles = p.num_tiles > ts.first ? (p.num_tiles - ts.first + ts.step - 1) / ts.step : 0;
-  return static_cast<uint32_t>(tiles) * static_cast<uint32_t>(p.CB);
+// A work unit: channel blocks [cb0, cb1) of one tile; part < 0 for a whole
+// tile, else its index among the ksplit units of a split tile.
+struct WorkUnit {
+  int tile, cb0, cb1, part;
+};
+
+__device__ __forceinline__ WorkUnit decode_unit(int i, const HaloParams& hp) {
+  const int CB = hp.c.CB;
+  if (i < hp.full_units) return {i, 0, CB, -1};
+  const int j = i - hp.full_units, part = j % hp.ksplit;
+  return {hp.full_units + j / hp.ksplit, part * CB / hp.ksplit, (part + 1) * CB / hp.ksplit, part};
 }
+
+// This CTA's channel blocks in order: unit by unit (first, first + step, ...),
+// each unit's blocks cb0 .. cb1 - 1.
+struct StageIter {
+  int unit, cb;
+  WorkUnit wu;
+  __device__ __forceinline__ StageIter(const HaloParams& hp, const TileSched& ts) : unit(ts.first), cb(0) {
+    if (unit < hp.num_units) {
+      wu = decode_unit(unit, hp);
+      cb = wu.cb0;
+    }
+  }
+  __device__ __forceinline__ bool valid(const HaloParams& hp) const { return unit < hp.num_units; }
+  __device__ __forceinline__ void next(const HaloParams& hp, const TileSched& ts) {
+    if (++cb == wu.cb1) {
+      unit += ts.step;
+      if (unit < hp.num_units) {
+        wu = decode_unit(unit, hp);
+        cb = wu.cb0;
+      }
+    }
+  }
+};
 
 __device__ __forceinline__ void halo_store_f16(const HaloParams& hp, uint8_t* halo, int e, int h, const uint4& v) {
   uint4 c0, c1;
@@ -158,14 +195,14 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
   const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
-  int l_tile = ts.first, l_cb = 0;
+  StageIter lit(hp, ts);  // the stage being loaded, nstg - 1 ahead
 
   auto issue_load = [&](uint32_t slot) {
-    if (l_tile < p.num_tiles) {
-      const PatchTile t = decode_patch(l_tile, hp, ts);
+    if (lit.valid(hp)) {
+      const PatchTile t = decode_patch(lit.wu.tile, hp, ts);
       const int hb0 = t.p0 * p.stride_h - p.pad_h;
       const int wb0 = t.q0 * p.stride_w - p.pad_w;
-      const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + l_cb * HW32;
+      const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + lit.cb * HW32;
       const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
       int b = w.b_first, pos = w.pos_first;
       for (int e = w.e_first; e < positions; e += kHaloStep) {
@@ -180,19 +217,16 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
           ++b;
         }
       }
-      if (++l_cb == p.CB) {
-        l_cb = 0;
-        l_tile += ts.step;
-      }
+      lit.next(hp, ts);
     }
     ptx::cp_async_commit();
   };
 
-  const uint32_t total = halo_stage_count(hp, ts);
   const int nstg = hp.nstg;
   for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
   bool ok = true;
-  for (uint32_t s = 0; s < total; ++s) {
+  uint32_t s = 0;
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++s) {
     issue_load((s + nstg - 1) % nstg);
     if (nstg == 3) ptx::cp_async_wait<2>();
     else ptx::cp_async_wait<1>();
@@ -224,13 +258,12 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
   const int positions = hp.HR * hp.CW;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
-  const uint32_t total = halo_stage_count(hp, ts);
-  int tile = ts.first, cb = 0;
-  for (uint32_t s = 0; s < total; ++s) {
-    const PatchTile t = decode_patch(tile, hp, ts);
+  uint32_t s = 0;
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++s) {
+    const PatchTile t = decode_patch(it.wu.tile, hp, ts);
     const int hb0 = t.p0 * p.stride_h - p.pad_h;
     const int wb0 = t.q0 * p.stride_w - p.pad_w;
-    const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + cb * HW32;
+    const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + it.cb * HW32;
     const uint32_t hs = s & 1u;
     uint8_t* halo = smem + hs * hp.halo_bytes;
     int e = w.e_first, b = w.b_first, pos = w.pos_first;
@@ -268,10 +301,6 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     } while (e < positions);
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
-    if (++cb == p.CB) {
-      cb = 0;
-      tile += ts.step;
-    }
   }
   return true;
 }
@@ -300,6 +329,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   uint64_t* drain = h_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 9) + 1;
+  uint64_t* epi_sync = h_full + 10;                                    // the epilogue warps' own barrier
+  volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 11);  // this CTA combines a split tile
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -325,6 +356,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
     ptx::mbar_init(drain, 1);
+    ptx::mbar_init(epi_sync, kEpilogue);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -380,7 +412,6 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       // few hundred cycles even when its phase has completed, so fewer, longer
       // runs keep the tensor core's short instruction queue fed.
       const int runs_per_cb = (p.R * p.S) / G;
-      const int runs_per_tile = p.CB * runs_per_cb;
       // GT > 0 (the host picks it only when S divides GT): a run is GT / S
       // whole filter rows, and the halo offsets of its taps relative to its
       // first row are the same for every run -- computed once, so a K-slice
@@ -406,15 +437,17 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         return __all_sync(0xffffffffu, ptx::mbar_wait<kCW>(bar, parity, p.timeout_ns, abort_flag));
       };
       trace_mark(p, 0, 0, 0);  // whole warp: no lane-dependent code around the issue loop
-      for (int tile = ts.first; ok && tile < p.num_tiles; tile += ts.step) {
-        int kk = 0, next_chunk = 0;
+      for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
+        const WorkUnit wu = decode_unit(unit, hp);
+        const int unit_runs = (wu.cb1 - wu.cb0) * runs_per_cb;
+        int kk = 0, next_chunk = 0;  // slices of this unit issued; where the next chunk starts
         uint32_t buf = 0, d_tmem = tmem_base;
         uint32_t acc_flag = 0;  // 0 for the first MMA of a chunk, then 1
         // tap state: column count tc within the filter row, row trow within
         // the channel block, the halo offset of the row, column phase and index
         // (GT > 0: only the run within the channel block and its first row)
         int tc = 0, trow = 0, rowpos = 0, fph = 0, idx = 0, rcb = 0;
-        for (int run = 0; run < runs_per_tile; ++run) {
+        for (int run = 0; run < unit_runs; ++run) {
           if (GT > 0 ? rcb == 0 : (tc == 0 && trow == 0)) {  // first run of a channel block: its halo
 #if defined(I8C_PIPELINE_TRACE)
             const long long th = tracing ? clock64() : 0;
@@ -571,9 +604,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const uint32_t stage_bytes = static_cast<uint32_t>(G * BNH * 64);
     uint32_t g = 0, st = 0, bph = 0;
     bool ok = true;
-    for (int tile = ts.first; ok && tile < p.num_tiles; tile += ts.step) {
-      const int n0 = (tile % p.num_n_tiles) * BN + ts.rank * BNH;
-      for (int kk = 0; kk < p.num_slices; kk += G, ++g) {
+    const int RS = p.R * p.S;
+    for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
+      const WorkUnit wu = decode_unit(unit, hp);
+      const int n0 = (wu.tile % p.num_n_tiles) * BN + ts.rank * BNH;
+      for (int kk = wu.cb0 * RS; kk < wu.cb1 * RS; kk += G, ++g) {
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_empty[st], bph ^ 1u, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
@@ -647,10 +682,20 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const int col0 = BN >= 64 ? eh * kColsPerWarp : 0;
     const bool col_owner = BN >= 64 || eh == 0;
     uint32_t run[kColsPerWarp];  // running int32 sums of this thread's pixel over its columns
-    uint32_t u = 0;
+    uint32_t u = 0, esync = 0;
     bool ok = true;
-    for (int tile = tile_sched<CG>().first; ok && tile < p.num_tiles; tile += tile_sched<CG>().step) {
-      for (int c = 0; c < p.num_chunks; ++c, ++u) {
+    const int RS = p.R * p.S;
+    // all epilogue threads meet (bounded wait: a warp that gave up cannot hang the others)
+    auto epi_barrier = [&]() -> bool {
+      ptx::mbar_arrive(epi_sync);
+      const bool met = ptx::mbar_wait(epi_sync, esync & 1u, p.timeout_ns, abort_flag);
+      ++esync;
+      return __all_sync(0xffffffffu, met);
+    };
+    for (int unit = tile_sched<CG>().first; ok && unit < hp.num_units; unit += tile_sched<CG>().step) {
+      const WorkUnit wu = decode_unit(unit, hp);
+      const int nch = ((wu.cb1 - wu.cb0) * RS + p.chunk_slices - 1) / p.chunk_slices;
+      for (int c = 0; c < nch; ++c, ++u) {
         const uint32_t buf = u & 1u;
 #if defined(I8C_PIPELINE_TRACE)
         if (warp == 8 && lane == 0) trace_mark(p, 3, 0, u);
@@ -685,8 +730,59 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 #if defined(I8C_PIPELINE_TRACE)
         if (warp == 8 && lane == 0) trace_mark(p, 3, 2, u);
 #endif
-        if (c + 1 < p.num_chunks || !col_owner) continue;
-        const PatchTile t = decode_patch(tile, hp, tile_sched<CG>());
+        if (c + 1 < nch) continue;
+        if (wu.part >= 0) {
+          // A split tile: publish this unit's partial sums; the unit that
+          // arrives last adds the others' and stores the tile.
+          const int tail = wu.tile - hp.full_units;
+          const int rank = tile_sched<CG>().rank;
+          constexpr size_t kBlock = static_cast<size_t>(128) * BN;  // int32 per (tile, part, rank)
+          int32_t* const blocks = hp.split_part + static_cast<size_t>(tail) * hp.ksplit * CG * kBlock;
+          if (col_owner) {
+            int4* mine = reinterpret_cast<int4*>(blocks + (static_cast<size_t>(wu.part) * CG + rank) * kBlock);
+#pragma unroll
+            for (int q = 0; q < kColsPerWarp / 4; ++q)
+              __stcg(mine + (col0 / 4 + q) * 128 + row,
+                     make_int4(static_cast<int>(run[4 * q]), static_cast<int>(run[4 * q + 1]),
+                               static_cast<int>(run[4 * q + 2]), static_cast<int>(run[4 * q + 3])));
+          }
+          __threadfence();
+          if (!epi_barrier()) {
+            ok = false;
+            break;
+          }
+          if (threadIdx.x == 8 * 32) {
+            int* cnt = hp.split_count + tail * CG + rank;
+            const int before = atomicAdd(cnt, 1);
+            const bool last = before == hp.ksplit - 1;
+            if (last) *cnt = 0;  // every part has arrived: ready for the next launch
+            __threadfence();
+            *split_last = last ? 1 : 0;
+          }
+          if (!epi_barrier()) {
+            ok = false;
+            break;
+          }
+          if (*split_last == 0) continue;
+          __threadfence();
+          if (col_owner) {
+            for (int part = 0; part < hp.ksplit; ++part) {
+              if (part == wu.part) continue;
+              const int4* other =
+                  reinterpret_cast<const int4*>(blocks + (static_cast<size_t>(part) * CG + rank) * kBlock);
+#pragma unroll
+              for (int q = 0; q < kColsPerWarp / 4; ++q) {
+                const int4 v = __ldcg(other + (col0 / 4 + q) * 128 + row);
+                run[4 * q] += static_cast<uint32_t>(v.x);
+                run[4 * q + 1] += static_cast<uint32_t>(v.y);
+                run[4 * q + 2] += static_cast<uint32_t>(v.z);
+                run[4 * q + 3] += static_cast<uint32_t>(v.w);
+              }
+            }
+          }
+        }
+        if (!col_owner) continue;
+        const PatchTile t = decode_patch(wu.tile, hp, tile_sched<CG>());
         const int pp = t.p0 + (row >> 3);
         const int qq = t.q0 + (row & 7);
         if (t.valid && pp < p.P && qq < p.Q) {

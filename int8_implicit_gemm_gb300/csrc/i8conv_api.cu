@@ -21,6 +21,7 @@ struct i8c_plan {
   int device;
   int kernel_variant;  // 1 = per-tap gather kernel, 2 = halo kernel, 3 = halo kernel on CTA pairs
   int cta_group;       // CTAs per MMA tile: 2 for variant 3, else 1
+  int split_tiles;     // halo kernel: tiles of the last wave split along the channel blocks
   int block_n, num_n_tiles, num_m_tiles, num_tiles, num_ctas;
   i8c::HaloParams halo;  // geometry and shared-memory layout of the halo kernel
   int num_slices, chunk_slices, num_chunks, acc_buffers;
@@ -33,6 +34,8 @@ struct i8c_plan {
   long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), 16 * kTraceSlots entries
   CUtensorMap tmap;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
+  int* split_count;      // halo kernel, split tail tiles: arrivals per tile and CTA rank
+  int32_t* split_part;   // halo kernel, split tail tiles: int32 partial sums
   size_t x_bytes, f_bytes, y_bytes;
   int64_t workspace_bytes;
   // optional per-launch timing of the convolution kernel
@@ -189,6 +192,8 @@ void free_plan_memory(i8c_plan* p) {
   if (p->stage_x) cudaFree(p->stage_x);
   if (p->stage_f) cudaFree(p->stage_f);
   if (p->stage_y) cudaFree(p->stage_y);
+  if (p->split_count) cudaFree(p->split_count);
+  if (p->split_part) cudaFree(p->split_part);
 }
 
 ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
@@ -331,7 +336,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2)
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 ||
+      o.tail_split > 2)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -423,8 +429,42 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   }
   p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
-  if (p->cta_group == 2) p->num_ctas = 2 * (groups < p->num_tiles ? groups : p->num_tiles);
-  else p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+  int64_t split_bytes = 0;
+  if (p->kernel_variant >= 2) {
+    // The last wave is partial when the tile count is not a multiple of the
+    // persistent CTAs (pairs): its tiles are split along the channel blocks
+    // into ksplit units each, so that the wave's units fill the GPU and take
+    // 1/ksplit of a tile's time.
+    const int g = p->cta_group == 2 ? groups : ctas;
+    const int rem = p->num_tiles % g;
+    int ksplit = 1;
+    if (rem > 0 && o.tail_split != 1) {
+      ksplit = g / rem;
+      if (ksplit > s.C / 32) ksplit = s.C / 32;
+      if (ksplit < 2) ksplit = 1;
+    }
+    if (ksplit > 1 && o.tail_split == 0) {
+      // Auto: split only when the time saved in the last wave clearly exceeds
+      // the cost of the partial sums, which all split units write (and half
+      // read back) at nearly the same moment.  Estimates: a K-slice takes
+      // about BN + 100 cycles at ~1.9 GHz; the partials move at ~8 TB/s
+      // through L2, plus ~2 us for the burst to drain.
+      const double tile_us = static_cast<double>((s.C / 32) * s.R * s.S) * (bn + 100) / 1900.0;
+      const double saved_us = tile_us * (1.0 - 1.0 / ksplit);
+      const double bytes = static_cast<double>(rem) * ksplit * p->cta_group * 128.0 * bn * 4.0 * 1.5;
+      const double cost_us = bytes / 8.0e6 + 2.0;
+      if (saved_us < 1.5 * cost_us) ksplit = 1;
+    }
+    p->halo.ksplit = ksplit;
+    p->halo.full_units = ksplit > 1 ? p->num_tiles - rem : p->num_tiles;
+    p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0);
+    if (ksplit > 1)
+      split_bytes = static_cast<int64_t>(rem) * ksplit * p->cta_group * 128 * bn * static_cast<int64_t>(sizeof(int32_t));
+    p->split_tiles = ksplit > 1 ? rem : 0;
+    p->num_ctas = p->cta_group * (g < p->halo.num_units ? g : p->halo.num_units);
+  } else {
+    p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+  }
   p->num_slices = (s.C / 32) * s.R * s.S;
   int max_chunk = o.max_chunk_slices > 0 ? o.max_chunk_slices : 32;
   if (p->kernel_variant >= 2) {
@@ -462,6 +502,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
   p->workspace_bytes = static_cast<int64_t>(p->f_bytes * 2 + sizeof(int));
+  if (e == cudaSuccess && split_bytes > 0) {
+    const size_t counts = sizeof(int) * static_cast<size_t>(p->split_tiles) * p->cta_group;
+    e = cudaMalloc(&p->split_part, static_cast<size_t>(split_bytes));
+    if (e == cudaSuccess) e = cudaMalloc(&p->split_count, counts);
+    if (e == cudaSuccess) e = cudaMemset(p->split_count, 0, counts);
+    p->workspace_bytes += split_bytes + static_cast<int64_t>(counts);
+    p->halo.split_part = p->split_part;
+    p->halo.split_count = p->split_count;
+  }
   if (e == cudaSuccess && (o.debug_flags & I8C_DEBUG_TRACE)) {
     const size_t tb = sizeof(long long) * 16 * i8c::kTraceSlots;
     e = cudaMalloc(&p->trace, tb);
@@ -534,6 +583,8 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->kernel_variant = pl->kernel_variant;
   info->halo_staging = pl->kernel_variant >= 2 ? pl->halo.nstg : 0;
   info->filter_run = pl->kernel_variant >= 2 ? pl->halo.bgroup : 1;
+  info->tail_split = pl->kernel_variant >= 2 ? pl->halo.ksplit : 1;
+  info->work_units = pl->kernel_variant >= 2 ? pl->halo.num_units : pl->num_tiles;
   info->filter_stages = pl->kernel_variant >= 2 ? pl->halo.nbs
                         : pl->block_n >= 256 ? i8c::TileCfg<256>::kStages
                         : pl->block_n >= 128 ? i8c::TileCfg<128>::kStages
@@ -607,6 +658,9 @@ i8c_status i8c_plan_status(const i8c_plan* pl, cudaStream_t stream) {
   if (e != cudaSuccess) return from_cuda(e);
   if (h != 0) {
     e = cudaMemset(pl->status, 0, sizeof(int));
+    // a launch that gave up may have left split-tile arrivals behind
+    if (e == cudaSuccess && pl->split_count != nullptr)
+      e = cudaMemset(pl->split_count, 0, sizeof(int) * static_cast<size_t>(pl->split_tiles) * pl->cta_group);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return h == 0 ? I8C_OK : static_cast<i8c_status>(h);

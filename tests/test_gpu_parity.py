@@ -142,3 +142,23 @@ def test_full_size_workloads(wl, kw):
     assert np.array_equal(acc.reshape(-1)[idx].astype(np.int64), ref)
     assert np.array_equal(y.reshape(-1)[idx], orc.requantize(ref, wl.alpha))
     assert np.array_equal(y.reshape(-1), orc.requantize(acc.reshape(-1).astype(np.int64), wl.alpha))
+
+
+@pytest.mark.parametrize("kw", [dict(num_ctas=10), dict(num_ctas=16), dict(kernel_variant=3, num_ctas=6),
+                                dict(kernel_variant=2, block_n=32, num_ctas=9, max_chunk_slices=4)],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
+def test_split_tail_exact(kw):
+    """Tiles of a partial last wave split along the channel blocks: the units'
+    int32 partial sums, combined by the unit that finishes last, give the
+    oracle's results exactly (and the same as without splitting)."""
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 512, 7, 6, 64, 3, 3, 1, 1, 1, 1, 1, 1)   # 16 channel blocks, 2 patches
+    plan = ext.Plan(shape, tail_split=2, **kw)
+    assert plan.info["tail_split"] > 1, plan.info
+    plan.destroy()
+    x, f = _data(shape, 4242)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -12)
+    for ts in (2, 1, 2):   # split, unsplit, split again (counters reset between launches)
+        y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -12, tail_split=ts, **kw)
+        assert np.array_equal(acc, acc_ref.astype(np.int32)), ts
+        assert np.array_equal(y, y_ref), ts
