@@ -36,6 +36,7 @@ struct HaloParams {
   uint32_t stg_bytes;       // one int8 staging slot: HR*CW*32 (rounded up to 128)
   int nstg;                 // int8 staging slots: 2 or 3, or 0 (producers load into registers)
   int nbs;                  // filter pipeline stages (<= kMaxBStages)
+  int nhs;                  // fp16 halo stages: 2 or 3
   int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
   uint32_t off_stg, off_b, off_bar;
   int phase_off[9];         // first position of column phase f (f < sw); phase_off[sw] = CW
@@ -154,22 +155,21 @@ __device__ __forceinline__ WorkUnit decode_unit(int i, const HaloParams& hp) {
 // This CTA's channel blocks in order: unit by unit (first, first + step, ...),
 // each unit's blocks cb0 .. cb1 - 1.
 struct StageIter {
-  int unit, cb;
-  WorkUnit wu;
+  int unit, cb, tile, cb_end;
+  __device__ __forceinline__ void load(const HaloParams& hp) {
+    const WorkUnit wu = decode_unit(unit, hp);
+    tile = wu.tile;
+    cb = wu.cb0;
+    cb_end = wu.cb1;
+  }
   __device__ __forceinline__ StageIter(const HaloParams& hp, const TileSched& ts) : unit(ts.first), cb(0) {
-    if (unit < hp.num_units) {
-      wu = decode_unit(unit, hp);
-      cb = wu.cb0;
-    }
+    if (unit < hp.num_units) load(hp);
   }
   __device__ __forceinline__ bool valid(const HaloParams& hp) const { return unit < hp.num_units; }
   __device__ __forceinline__ void next(const HaloParams& hp, const TileSched& ts) {
-    if (++cb == wu.cb1) {
+    if (++cb == cb_end) {
       unit += ts.step;
-      if (unit < hp.num_units) {
-        wu = decode_unit(unit, hp);
-        cb = wu.cb0;
-      }
+      if (unit < hp.num_units) load(hp);
     }
   }
 };
@@ -199,7 +199,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
 
   auto issue_load = [&](uint32_t slot) {
     if (lit.valid(hp)) {
-      const PatchTile t = decode_patch(lit.wu.tile, hp, ts);
+      const PatchTile t = decode_patch(lit.tile, hp, ts);
       const int hb0 = t.p0 * p.stride_h - p.pad_h;
       const int wb0 = t.q0 * p.stride_w - p.pad_w;
       const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + lit.cb * HW32;
@@ -225,14 +225,13 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
   const int nstg = hp.nstg;
   for (int i = 0; i < nstg - 1; ++i) issue_load(static_cast<uint32_t>(i));
   bool ok = true;
-  uint32_t s = 0;
+  uint32_t s = 0, hs = 0, hph = 0;  // stage count; halo stage and its phase parity
   for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++s) {
     issue_load((s + nstg - 1) % nstg);
     if (nstg == 3) ptx::cp_async_wait<2>();
     else ptx::cp_async_wait<1>();
-    const uint32_t hs = s & 1u;
     // warp-uniform outcome: the arrive below is a warp-wide operation
-    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag))) {
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) {
       ok = false;
       break;
     }
@@ -242,6 +241,8 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
       halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
+    hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
+    hph ^= hs == 0 ? 1u : 0u;
   }
   ptx::cp_async_wait_all();
   return ok;
@@ -258,13 +259,13 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
   const int positions = hp.HR * hp.CW;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
-  uint32_t s = 0;
-  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++s) {
-    const PatchTile t = decode_patch(it.wu.tile, hp, ts);
+  uint32_t hs = 0, hph = 0;  // halo stage and its phase parity
+  bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts)) {
+    const PatchTile t = decode_patch(it.tile, hp, ts);
     const int hb0 = t.p0 * p.stride_h - p.pad_h;
     const int wb0 = t.q0 * p.stride_w - p.pad_w;
     const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + it.cb * HW32;
-    const uint32_t hs = s & 1u;
     uint8_t* halo = smem + hs * hp.halo_bytes;
     int e = w.e_first, b = w.b_first, pos = w.pos_first;
     bool stage_free = false;
@@ -291,7 +292,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
       if (!stage_free) {
         // every lane runs the first batch, so the warp is converged here; the
         // outcome is made warp-uniform because the arrive below is warp-wide
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], ((s >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)))
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag)))
           return false;
         stage_free = true;
       }
@@ -300,7 +301,10 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
         if (eb[k] < positions) halo_store_f16(hp, halo, eb[k], h, v[k]);
     } while (e < positions);
     ptx::fence_proxy_async_smem();
-    arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
+    arrive_on_leader(&h_full[hs], ts, !skip);
+    skip = false;
+    hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
+    hph ^= hs == 0 ? 1u : 0u;
   }
   return true;
 }
@@ -323,14 +327,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   uint64_t* b_full = bars;
   uint64_t* b_empty = bars + kMaxBStages;
   uint64_t* h_full = bars + 2 * kMaxBStages;
-  uint64_t* h_empty = h_full + 2;
-  uint64_t* acc_full = h_full + 4;
-  uint64_t* acc_empty = h_full + 6;
-  uint64_t* drain = h_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 9);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 9) + 1;
-  uint64_t* epi_sync = h_full + 10;                                    // the epilogue warps' own barrier
-  volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 11);  // this CTA combines a split tile
+  uint64_t* h_empty = h_full + 3;  // up to three halo stages
+  uint64_t* acc_full = h_full + 6;
+  uint64_t* acc_empty = h_full + 8;
+  uint64_t* drain = h_full + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 11) + 1;
+  uint64_t* epi_sync = h_full + 12;                                    // the epilogue warps' own barrier
+  volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 13);  // this CTA combines a split tile
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -349,9 +353,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&b_full[i], 1);
       ptx::mbar_init(&b_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < hp.nhs; ++i) {
       ptx::mbar_init(&h_full[i], kProducers * CG);  // a pair's rank 0 counts both CTAs' producers
       ptx::mbar_init(&h_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&acc_full[i], 1);
       ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         }
       }
       const int run_rowstep = GT > 0 ? (G / p.S) * row_step : 0;
-      uint32_t u = 0, hseq = 0, st = 0, bph = 0, g = 0;
+      uint32_t u = 0, hst = 0, hph = 0, st = 0, bph = 0, g = 0;  // hst, hph: halo stage and its parity
       bool ok = true;
 #if defined(I8C_PIPELINE_TRACE)
       const bool tracing = p.trace != nullptr && blockIdx.x == 0;
@@ -451,9 +457,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           if (GT > 0 ? rcb == 0 : (tc == 0 && trow == 0)) {  // first run of a channel block: its halo
 #if defined(I8C_PIPELINE_TRACE)
             const long long th = tracing ? clock64() : 0;
-            nr_h += ptx::mbar_test_wait<kCW>(&h_full[hseq & 1u], (hseq >> 1) & 1u) ? 0 : 1;
+            nr_h += ptx::mbar_test_wait<kCW>(&h_full[hst], hph) ? 0 : 1;
 #endif
-            if (!wwait(&h_full[hseq & 1u], (hseq >> 1) & 1u)) {
+            if (!wwait(&h_full[hst], hph)) {
               ok = false;
               break;
             }
@@ -503,7 +509,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           trace_mark(p, 0, 1, g / G);  // filter stage acquired
 #endif
           ptx::tc_fence_after();
-          const uint32_t h_stage = h_lo + (hseq & 1u) * halo_lo;
+          const uint32_t h_stage = h_lo + hst * halo_lo;
           uint32_t b_cur = b_lo + st * stage_lo;
 #pragma unroll
           for (int t = 0; t < G; ++t) {
@@ -561,9 +567,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             rowpos = cb_done ? 0 : rowpos;
           }
           if (cb_done) {  // channel block done: release its halo
-            if (ptx::elect_one()) commit_all(&h_empty[hseq & 1u]);
+            if (ptx::elect_one()) commit_all(&h_empty[hst]);
             __syncwarp();
-            ++hseq;
+            hst = hst + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hst + 1;
+            hph ^= hst == 0 ? 1u : 0u;
           }
         }
         if (!ok) break;

@@ -159,9 +159,12 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
     const bool whole_rows = G % s.S == 0 && RS % G == 0;
     if (!(part_row || whole_rows) || G > 32) continue;
     const int min_stages = part_row ? 3 : 2;
+    // a stage that holds a whole channel block leaves the producers one
+    // stage of slack with two halo stages: give them a third when it fits
+    for (int nhs = G == RS ? 3 : 2; nhs >= 2; --nhs)
     for (int k = first; k <= last; ++k) {
       const int nstg = kSlots[k];
-      const int64_t off_stg = 2LL * h->halo_bytes;
+      const int64_t off_stg = static_cast<int64_t>(nhs) * h->halo_bytes;
       const int64_t off_b = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
       const int64_t room = budget - off_b;
       const int64_t stage = static_cast<int64_t>(G) * (bn / cg) * 64;
@@ -169,6 +172,7 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
       int64_t nbs = room / stage;
       if (nbs > i8c::kMaxBStages) nbs = i8c::kMaxBStages;
       h->bgroup = G;
+      h->nhs = nhs;
       h->nstg = nstg;
       h->nbs = static_cast<int>(nbs);
       h->off_stg = static_cast<uint32_t>(off_stg);
