@@ -80,11 +80,12 @@ def dram_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks, utilisation and throttle reasons sampled every 20 ms;
+    the summary keeps the samples taken while the GPU was busy."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, index: int):
         self.index = index
@@ -95,14 +96,13 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.25)
+        time.sleep(0.2)
 
     def stop(self):
         if self.proc is not None:
-            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -116,6 +116,8 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for r in rows:
             try:
+                if float(r[9]) < 50:  # idle sample (before or after the load)
+                    continue
                 sm.append(float(r[1]))
                 smax.append(float(r[2]))
                 for name, v in zip(names, r[5:9]):
@@ -126,7 +128,8 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "note": "samples at >= 50% utilisation, 20 ms apart, over the timed "
+                                             "steps and the kernel-timing steps that follow them"}
 
 
 def cpu_oracle_rate(wl, budget_s: float, max_images: int | None = None):
@@ -220,10 +223,20 @@ def run_ours(args, wl, rank, world):
     t_wall = time.perf_counter() - t_wall0
     launches = ext.launch_count() - launches0
     total_ms = ev0.elapsed_time(ev1)
+    # kernel timing (event-bracketed plan), repeated for at least ~0.5 s so
+    # that the clock sampler sees the GPU under this load
+    t_k0 = time.perf_counter()
+    kern_ms, kern_n = 0.0, 0
+    while True:
+        for i in range(args.steps):
+            step(i, plan_k)
+        torch.cuda.synchronize()
+        ms_, n_ = plan_k.kernel_time()
+        kern_ms += ms_
+        kern_n += n_
+        if time.perf_counter() - t_k0 > 0.5 or clocks is None:
+            break
     clock_rec = clocks.stop() if clocks else None
-    for i in range(args.steps):
-        step(i, plan_k)
-    kern_ms, kern_n = plan_k.kernel_time()
     st = plan.status(stream) or plan_k.status(stream)
     if st != 0:
         raise RuntimeError(f"device status {ext.status_string(st)}")
