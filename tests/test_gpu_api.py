@@ -117,3 +117,38 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
     y2, _ = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, want_acc=False)
     assert np.array_equal(y2, y_ref)
+
+
+def test_plan_runs_captured_in_a_cuda_graph(torch_cuda):
+    """i8c_plan_run is capturable: a CUDA graph of three runs on different
+    inputs replays to the oracle's outputs (the dependent launch of the
+    convolution after the filter conversion becomes a graph edge)."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 13, 11, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    plan = ext.Plan(shape)
+    P, Q = plan.info["P"], plan.info["Q"]
+    cases = []
+    for seed in (31, 32, 33):
+        x = synth.uniform_int8(seed, 2 * 64 * 13 * 11, -128, 127).reshape(2, 64, 13, 11)
+        f = synth.uniform_int8(seed + 100, 64 * 64 * 9, -128, 127).reshape(64, 64, 3, 3)
+        xp, fp = gpu_util.packed_inputs(x, f)
+        y = torch.zeros(2 * 64 * P * Q, dtype=torch.int8, device="cuda")
+        cases.append((x, f, torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda(), y))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        plan.run(cases[0][2], cases[0][3], cases[0][4], 2.0 ** -10, s)  # warm-up outside the graph
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _, _, xd, fd, y in cases:
+            plan.run(xd, fd, y, 2.0 ** -10, torch.cuda.current_stream())
+    for _, _, _, _, y in cases:
+        y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert plan.status() == ext.I8C_OK
+    for x, f, _, _, y in cases:
+        y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+        assert np.array_equal(y.cpu().numpy().reshape(y_ref.shape), y_ref)
+    plan.destroy()
