@@ -222,7 +222,8 @@ i8c_status i8c_plan_kernel_time(const i8c_plan* plan, double* total_ms, int64_t*
 /* With I8C_DEBUG_TRACE: copies up to `count` entries of the last run's trace
  * (synchronous): entry (role*4 + event)*512 + i is the SM clock at event
  * `event` of step i of role 0 MMA issuer, 1 filter TMA, 2 activation
- * producer, 3 epilogue; 0 where not reached. */
+ * producer, 3 epilogue; 0 where not reached.  Up to 32*512 entries: entries
+ * from 16*512 on are only written by builds made for pipeline analysis. */
 i8c_status i8c_plan_trace(const i8c_plan* plan, long long* out, int64_t count);
 
 /* Frees the plan's device memory.  Synchronises the device first. */

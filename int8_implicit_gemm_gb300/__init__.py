@@ -239,11 +239,14 @@ class Plan:
         return ms.value, n.value
 
     def trace(self):
-        """The clock64 trace of CTA 0 (plan created with I8C_DEBUG_TRACE), shape (4 roles, 4 events, 512)."""
+        """The trace of a plan created with I8C_DEBUG_TRACE, shape (8, 4, 512):
+        [role][event][step] clock64 values of CTA 0 for roles 0-3 (MMA issuer,
+        filter TMA, activation producer, epilogue); rows 4-7 are written only
+        by pipeline-analysis builds."""
         import numpy as np
-        out = np.zeros(16 * 512, dtype=np.int64)
+        out = np.zeros(32 * 512, dtype=np.int64)
         _check(lib.i8c_plan_trace(self.handle, out.ctypes.data, out.size), "i8c_plan_trace")
-        return out.reshape(4, 4, 512)
+        return out.reshape(8, 4, 512)
 
     def status(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status word."""

@@ -67,6 +67,7 @@ struct ConvParams {
 // trace[(r * 4 + e) * kTraceSlots + i].  Roles: 0 MMA, 1 filter TMA,
 // 2 activation producer thread 0, 3 epilogue thread 0.
 constexpr int kTraceSlots = 512;
+constexpr int kTraceRows = 32;  // rows 0-15: role x event; 16-31: pipeline analysis build
 __device__ __forceinline__ void trace_mark(const ConvParams& p, int role, int ev, uint32_t i) {
   if (p.trace != nullptr && blockIdx.x == 0 && i < static_cast<uint32_t>(kTraceSlots))
     p.trace[(role * 4 + ev) * kTraceSlots + i] = clock64();

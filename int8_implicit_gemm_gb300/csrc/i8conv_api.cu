@@ -31,7 +31,7 @@ struct i8c_plan {
   int debug_flags;
   uint16_t* f16;   // fp16 copy of the filter, [C/32][R][S][K][32]
   int* status;     // device status word
-  long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), 16 * kTraceSlots entries
+  long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), kTraceRows * kTraceSlots entries
   CUtensorMap tmap;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
   int* split_count;      // halo kernel, split tail tiles: arrivals per tile and CTA rank
@@ -516,7 +516,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     p->halo.split_count = p->split_count;
   }
   if (e == cudaSuccess && (o.debug_flags & I8C_DEBUG_TRACE)) {
-    const size_t tb = sizeof(long long) * 16 * i8c::kTraceSlots;
+    const size_t tb = sizeof(long long) * i8c::kTraceRows * i8c::kTraceSlots;
     e = cudaMalloc(&p->trace, tb);
     if (e == cudaSuccess) e = cudaMemset(p->trace, 0, tb);
   }
@@ -601,7 +601,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
 i8c_status i8c_plan_trace(const i8c_plan* pl, long long* out, int64_t count) {
   if (pl == nullptr || out == nullptr || count < 0) return I8C_ERR_INVALID_ARG;
   if (pl->trace == nullptr) return I8C_ERR_INVALID_ARG;
-  const int64_t n = count < 16 * i8c::kTraceSlots ? count : 16 * i8c::kTraceSlots;
+  const int64_t n = count < i8c::kTraceRows * i8c::kTraceSlots ? count : i8c::kTraceRows * i8c::kTraceSlots;
   return from_cuda(cudaMemcpy(out, pl->trace, sizeof(long long) * n, cudaMemcpyDeviceToHost));
 }
 
