@@ -7,6 +7,7 @@
 #include <map>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "../../include/i8conv.h"
@@ -372,43 +373,60 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->kernel_variant = 1;
   p->cta_group = 1;
   if (o.kernel_variant != 1) {
-    const int cg = o.kernel_variant == 3 ? 2 : 1;
-    int best_bn = 0, best_groups = 0;
-    double best = -1.0;
-    for (int cand : {256, 128, 64, 32}) {
-      if (o.block_n != 0 && cand != o.block_n) continue;
-      if (cg == 2 && cand < 64) continue;
-      if (o.block_n == 0 && cand > 32 * cg && cand / 2 >= s.K) continue;  // half the tile would be empty
-      i8c::HaloParams h;
-      int sm = 0;
-      if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, &h, &sm)) continue;
-      int g = ctas / cg;
-      if (cg == 2) {
-        // pairs that fit on the GPU at once (clusters need both SMs free)
-        if (i8c::halo_prepare_pair(cand) != cudaSuccess) continue;
-        const int fit = i8c::halo_pair_max_clusters(cand, h.bgroup, s.S, sm);
-        if (fit < 1) continue;
-        if (g > fit) g = fit;
-        if (g < 1) g = 1;
+    // best tile width on cg CTAs per tile: {width, groups} (width 0: none fits)
+    auto search = [&](int cg, int only_bn) -> std::pair<int, int> {
+      int best_bn = 0, best_groups = 0;
+      double best = -1.0;
+      for (int cand : {256, 128, 64, 32}) {
+        if (o.block_n != 0 && cand != o.block_n) continue;
+        if (only_bn != 0 && cand != only_bn) continue;
+        if (cg == 2 && cand < 64) continue;
+        if (o.block_n == 0 && cand > 32 * cg && cand / 2 >= s.K) continue;  // half the tile would be empty
+        i8c::HaloParams h;
+        int sm = 0;
+        if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, &h, &sm)) continue;
+        int g = ctas / cg;
+        if (cg == 2) {
+          // pairs that fit on the GPU at once (clusters need both SMs free)
+          if (i8c::halo_prepare_pair(cand) != cudaSuccess) continue;
+          const int fit = i8c::halo_pair_max_clusters(cand, h.bgroup, s.S, sm);
+          if (fit < 1) continue;
+          if (g > fit) g = fit;
+          if (g < 1) g = 1;
+        }
+        const int nt = (s.K + cand - 1) / cand;
+        const int64_t t = (static_cast<int64_t>(h.num_patches) + cg - 1) / cg * nt;
+        // narrower MMAs leave the issuing warp's per-slice overhead exposed (the
+        // tensor core queues only about two MMAs); measured relative rates
+        double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
+        // runs of one K-slice (no room for longer filter stages) issue poorly
+        if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
+        const double score =
+            wave_efficiency(t, g) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
+        if (score > best * 1.02) {
+          best = score;
+          best_bn = cand;
+          best_groups = g;
+        }
       }
-      const int nt = (s.K + cand - 1) / cand;
-      const int64_t t = (static_cast<int64_t>(h.num_patches) + cg - 1) / cg * nt;
-      // narrower MMAs leave the issuing warp's per-slice overhead exposed (the
-      // tensor core queues only about two MMAs); measured relative rates
-      double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
-      // runs of one K-slice (no room for longer filter stages) issue poorly
-      if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
-      const double score =
-          wave_efficiency(t, g) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
-      if (score > best * 1.02) {
-        best = score;
-        best_bn = cand;
-        best_groups = g;
+      return {best_bn, best_groups};
+    };
+    int cg = o.kernel_variant == 3 ? 2 : 1;
+    std::pair<int, int> best = search(cg, 0);
+    if (o.kernel_variant == 0 && best.first == 64) {
+      // 64-wide tiles issue MMAs at the tensor core's per-instruction floor; a
+      // CTA pair's M = 256 MMAs halve the instructions per SM (measured on the
+      // dilated 5x9 layer: 1042 against 889 TOPS).  At 256 columns single
+      // CTAs are faster.
+      const std::pair<int, int> pair = search(2, 64);
+      if (pair.first != 0) {
+        cg = 2;
+        best = pair;
       }
     }
-    if (best_bn != 0) {
-      bn = best_bn;
-      groups = best_groups;
+    if (best.first != 0) {
+      bn = best.first;
+      groups = best.second;
       p->kernel_variant = cg == 2 ? 3 : 2;
       p->cta_group = cg;
       halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, &p->halo, &halo_smem);
