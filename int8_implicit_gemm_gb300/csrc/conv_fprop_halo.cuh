@@ -62,8 +62,8 @@ constexpr int kHaloThreads = 512;
 // Register budgets per warpgroup after setmaxnreg: the two epilogue warpgroups
 // hold the running sums; 128 * (2 * kWorkerRegs + 2 * kEpilogueRegs) must not
 // exceed the 512 * 128 registers the block is launched with.
-constexpr uint32_t kWorkerRegs = 56;
-constexpr uint32_t kEpilogueRegs = 200;
+constexpr uint32_t kWorkerRegs = 72;
+constexpr uint32_t kEpilogueRegs = 184;
 static_assert(128 * (2 * kWorkerRegs + 2 * kEpilogueRegs) <= 512 * 128, "register split");
 constexpr int kHaloBarBytes = 512;
 
@@ -254,7 +254,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
                                                    uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                    int pt) {
   const ConvParams& p = hp.c;
-  constexpr int kBatch = 4;
+  constexpr int kBatch = 6;  // stride-2 halos: one load round trip per stage instead of two
   const int h = pt & 1;
   const int positions = hp.HR * hp.CW;
   const HaloWalk w = halo_walk(hp, pt);
@@ -275,10 +275,9 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     bool stage_free = false;
     do {
       uint4 v[kBatch];
-      int eb[kBatch];
+      const int e0 = e;  // position of v[k]: e0 + k * kHaloStep
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        eb[k] = e;
         v[k] = make_uint4(0, 0, 0, 0);
         if (e < positions) {
           const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
@@ -306,7 +305,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        if (eb[k] < positions) halo_store_f16(hp, halo, eb[k], h, v[k]);
+        if (e0 + k * kHaloStep < positions) halo_store_f16(hp, halo, e0 + k * kHaloStep, h, v[k]);
     } while (e < positions);
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
