@@ -85,11 +85,18 @@ typedef struct {
                                 cp.async ahead of use, 2 = straight into registers (no
                                 staging memory); I8C_ERR_UNSUPPORTED if the forced form
                                 does not fit                                               */
-  int32_t tail_split;        /* halo kernel, tiles of a partial last wave split along the
+  int32_t tail_split;        /* halo kernel, the tiles of a partial last wave: 0 = auto (split
+                                into their two halves of output channels when the halves fit
+                                in the wave and the tile is 128 or 256 wide, else split along
+                                the channel blocks when the estimated saving clearly exceeds
+                                the partial-sum traffic), 1 = never split, 2 = split along the
                                 channel blocks (int32 partial sums combined by the unit that
-                                finishes last; needs plan workspace): 0 = when the estimated
-                                saving clearly exceeds the partial-sum traffic, 1 = never,
-                                2 = whenever the last wave is partial                       */
+                                finishes last; needs plan workspace) whenever the last wave is
+                                partial, 3 = halve along the output channels when possible  */
+  int32_t tile_shape;        /* halo kernel, the 128 output pixels of a tile: 0 = auto, 1 = a
+                                16x8 patch, 2 = 128 consecutive pixels of the output laid out
+                                with the zero-padded input's row width (stride 1 only; the
+                                pixels past Q in each row are computed and discarded)       */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so
@@ -124,8 +131,10 @@ typedef struct {
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of
                                 one filter row); 1 for the gather kernel       */
   int32_t filter_stages;     /* filter pipeline stages in shared memory        */
-  int32_t tail_split;        /* units each last-wave tile is split into (1: none) */
+  int32_t tail_split;        /* channel-block units per last-wave tile (1: none) */
   int32_t work_units;        /* units of work the persistent CTAs share          */
+  int32_t tail_halves;       /* 2 when last-wave tiles are halved along the output channels */
+  int32_t flat_tiles;        /* 1 when tiles are 128 consecutive padded-row pixels */
 } i8c_plan_info;
 
 /* Output height P and width Q for a shape (formula above).  Returns

@@ -33,7 +33,9 @@ extern "C" {
  * warps storing to shared memory alongside), 11-14 (six MMAs, then 0, 200,
  * 400 or 800 idle cycles: queue depth), 15-18 (mode 8 without its commit,
  * without its wait, with one elected block per run, with one elected block
- * and neither wait nor commit).  iters must be a multiple of 6.
+ * and neither wait nor commit), 19-20 (mode 8's loop on a four-stage ring of
+ * full/empty barriers re-armed each run by a producer warp that sleeps (19)
+ * or spins (20) in its waits).  iters must be a multiple of 6.
  *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles to issue,
  *           SM cycles until all MMAs completed, 1 if the completion wait
  *           succeeded (bounded at 2 s)

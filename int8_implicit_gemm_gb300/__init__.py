@@ -57,7 +57,7 @@ class Options(ctypes.Structure):
                 ("max_chunk_slices", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
                 ("host_staging", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("timing_events", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
-                ("halo_loads", ctypes.c_int32), ("tail_split", ctypes.c_int32)]
+                ("halo_loads", ctypes.c_int32), ("tail_split", ctypes.c_int32), ("tile_shape", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -71,7 +71,7 @@ class PlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("kernel_variant", ctypes.c_int32),
                 ("halo_staging", ctypes.c_int32), ("filter_run", ctypes.c_int32),
                 ("filter_stages", ctypes.c_int32), ("tail_split", ctypes.c_int32),
-                ("work_units", ctypes.c_int32)]
+                ("work_units", ctypes.c_int32), ("tail_halves", ctypes.c_int32), ("flat_tiles", ctypes.c_int32)]
 
     def asdict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -209,10 +209,11 @@ class Plan:
     """A validated convolution plan on the current CUDA device (i8c_plan_*)."""
 
     def __init__(self, shape, block_n=0, num_ctas=0, max_chunk_slices=0, wait_timeout_us=0,
-                 host_staging=False, debug_flags=0, timing_events=0, kernel_variant=0, halo_loads=0, tail_split=0):
+                 host_staging=False, debug_flags=0, timing_events=0, kernel_variant=0, halo_loads=0, tail_split=0,
+                 tile_shape=0):
         self.shape = ConvShape.of(shape)
         opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(bool(host_staging)), debug_flags,
-                       timing_events, kernel_variant, halo_loads, tail_split)
+                       timing_events, kernel_variant, halo_loads, tail_split, tile_shape)
         h = ctypes.c_void_p()
         _check(lib.i8c_plan_create(ctypes.byref(self.shape), ctypes.byref(opts), ctypes.byref(h)),
                "i8c_plan_create")

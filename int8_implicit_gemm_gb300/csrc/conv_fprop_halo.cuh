@@ -28,9 +28,18 @@ namespace i8c {
 
 struct HaloParams {
   ConvParams c;
-  int TPH, TQW;             // patches per image along P (16 rows each) and Q (8 columns each)
-  int num_patches;          // N * TPH * TQW
-  int HR, CW;               // halo rows, halo positions per row
+  // Tile geometry.  2-D patches: 16 x 8 output pixels, TPH x TQW per image.
+  // Flat tiles (stride 1 only): 128 consecutive pixels of the output laid
+  // out row-major with the zero-padded input's row width CW; tpi per image
+  // (the CW - Q pixels at the end of each row are computed and discarded),
+  // and the halo is the contiguous run of `positions` padded input pixels
+  // that the 128 pixels' taps read.
+  int flat;
+  int TPH, TQW;             // 2-D: patches per image along P (16 rows each) and Q (8 columns each)
+  int tpi;                  // flat: tiles per image, ceil(P * CW / 128)
+  int num_patches;          // N * TPH * TQW, or N * tpi
+  int HR, CW;               // halo rows, halo positions per row (flat: CW = padded input width)
+  int positions;            // halo positions: HR * CW, or (flat) 128 + (R-1)*dh*CW + (S-1)*dw
   uint32_t plane_bytes;     // one 8-channel plane: HR*CW*16 (rounded up to 128)
   uint32_t halo_bytes;      // one halo stage: 4 planes
   uint32_t stg_bytes;       // one int8 staging slot: HR*CW*32 (rounded up to 128)
@@ -44,7 +53,10 @@ struct HaloParams {
   // partial wave) each split into ksplit units over ranges of channel blocks,
   // whose int32 partial sums meet in split_part and are combined by the unit
   // that finishes last (split_count: arrivals per tile and CTA rank).
-  int num_units, full_units, ksplit;
+  // Or (nsplit = 2, single CTAs) each remaining tile splits into its two
+  // halves of output channels: two units with disjoint outputs, MMAs of N =
+  // BN/2, no partial sums.
+  int num_units, full_units, ksplit, nsplit;
   int* split_count;         // [tail tiles][cg], zero between launches
   int32_t* split_part;      // [tail tiles][ksplit][cg][BN/4][128][4]
 };
@@ -70,6 +82,7 @@ constexpr int kHaloBarBytes = 512;
 struct PatchTile {
   int n, p0, q0, nt;
   bool valid;  // false for the missing second patch of a CTA pair's last tile
+  int m0;      // flat tiles: first pixel in the padded row-major output (p0 = q0 = 0)
 };
 
 // Tile schedule of one CTA: tiles first, first + step, ...; a tile is
@@ -93,10 +106,11 @@ __device__ __forceinline__ TileSched tile_sched() {
 __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp, const TileSched& ts) {
   const int nt = tile % hp.c.num_n_tiles;
   const int patch = (tile / hp.c.num_n_tiles) * ts.cg + ts.rank;
+  if (hp.flat) return {patch / hp.tpi, 0, 0, nt, patch < hp.num_patches, (patch % hp.tpi) * 128};
   const int qt = patch % hp.TQW;
   const int rest = patch / hp.TQW;
   const int pt = rest % hp.TPH;
-  return {rest / hp.TPH, pt * 16, qt * 8, nt, patch < hp.num_patches};
+  return {rest / hp.TPH, pt * 16, qt * 8, nt, patch < hp.num_patches, 0};
 }
 
 // Arrive on a barrier of the MMA-issuing CTA, called by all 32 lanes of a
@@ -131,6 +145,19 @@ __device__ __forceinline__ HaloWalk halo_walk(const HaloParams& hp, int pt) {
   return w;
 }
 
+// Flat tiles start m0 pixels into the padded image: move a walk's (row,
+// column) there (m0 = 0 for 2-D patches).
+__device__ __forceinline__ void halo_walk_origin(const HaloParams& hp, int m0, int& b, int& pos) {
+  if (m0 == 0) return;
+  const int mq = m0 / hp.CW;
+  pos += m0 - mq * hp.CW;
+  b += mq;
+  if (pos >= hp.CW) {
+    pos -= hp.CW;
+    ++b;
+  }
+}
+
 // Input column (relative to the halo's first column) of halo position pos in
 // its row: positions are ordered by column phase (column mod stride_w).
 __device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
@@ -143,13 +170,16 @@ __device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
 // tile, else its index among the ksplit units of a split tile.
 struct WorkUnit {
   int tile, cb0, cb1, part;
+  int nh;  // half of the tile's output channels (0 or 1), or -1 for all of them
 };
 
 __device__ __forceinline__ WorkUnit decode_unit(int i, const HaloParams& hp) {
   const int CB = hp.c.CB;
-  if (i < hp.full_units) return {i, 0, CB, -1};
-  const int j = i - hp.full_units, part = j % hp.ksplit;
-  return {hp.full_units + j / hp.ksplit, part * CB / hp.ksplit, (part + 1) * CB / hp.ksplit, part};
+  if (i < hp.full_units) return {i, 0, CB, -1, -1};
+  const int j = i - hp.full_units;
+  if (hp.nsplit == 2) return {hp.full_units + j / 2, 0, CB, -1, j % 2};
+  const int part = j % hp.ksplit;
+  return {hp.full_units + j / hp.ksplit, part * CB / hp.ksplit, (part + 1) * CB / hp.ksplit, part, -1};
 }
 
 // This CTA's channel blocks in order: unit by unit (first, first + step, ...),
@@ -191,7 +221,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
                                                    int pt) {
   const ConvParams& p = hp.c;
   const int h = pt & 1;
-  const int positions = hp.HR * hp.CW;
+  const int positions = hp.positions;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
   const uint32_t stg_base = ptx::smem_addr(smem + hp.off_stg);
@@ -205,6 +235,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
       const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + lit.cb * HW32;
       const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
       int b = w.b_first, pos = w.pos_first;
+      halo_walk_origin(hp, t.m0, b, pos);
       for (int e = w.e_first; e < positions; e += kHaloStep) {
         const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
         const bool in = t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
@@ -256,7 +287,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
   const ConvParams& p = hp.c;
   constexpr int kBatch = 6;  // stride-2 halos: one load round trip per stage instead of two
   const int h = pt & 1;
-  const int positions = hp.HR * hp.CW;
+  const int positions = hp.positions;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
   uint32_t hs = 0, hph = 0;  // halo stage and its phase parity
@@ -272,6 +303,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + it.cb * HW32;
     uint8_t* halo = smem + hs * hp.halo_bytes;
     int e = w.e_first, b = w.b_first, pos = w.pos_first;
+    halo_walk_origin(hp, t.m0, b, pos);
     bool stage_free = false;
     do {
       uint4 v[kBatch];
@@ -404,7 +436,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         if constexpr (CG == 2) ptx::mma_commit_pair(bar, kPair);
         else ptx::mma_commit(bar);
       };
-      const uint32_t sbo = static_cast<uint32_t>(p.stride_h * hp.CW * 16);
+      // 8-row groups of A: sh halo rows apart (2-D patches), 8 positions apart (flat)
+      const uint32_t sbo = hp.flat ? 128u : static_cast<uint32_t>(p.stride_h * hp.CW * 16);
       const uint32_t lbo = hp.plane_bytes;
       const uint64_t a_desc0 = ptx::smem_desc_noswizzle_kmajor(0, lbo, sbo);
       const uint64_t b_desc0 = ptx::smem_desc_sw64_kmajor(0);
@@ -459,8 +492,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
         const WorkUnit wu = decode_unit(unit, hp);
         const int unit_runs = (wu.cb1 - wu.cb0) * runs_per_cb;
+        // a half-width unit: N = BN/2 MMAs on its half of the filter rows and
+        // of the accumulator columns
+        const bool half_n = CG == 1 && wu.nh >= 0;
+        const uint32_t idesc_u = half_n ? ptx::idesc_f16_f32(128, BN / 2) : idesc;
+        const uint32_t nh_cols = half_n ? static_cast<uint32_t>(wu.nh) * (BN / 2) : 0u;
+        const uint32_t nh_lo = nh_cols * (64 >> 4);  // those filter rows, 64 bytes each, in 16-byte units
         int kk = 0, next_chunk = 0;  // slices of this unit issued; where the next chunk starts
-        uint32_t buf = 0, d_tmem = tmem_base;
+        uint32_t buf = 0, d_tmem = tmem_base + nh_cols;
         uint32_t acc_flag = 0;  // 0 for the first MMA of a chunk, then 1
         // tap state: column count tc within the filter row, row trow within
         // the channel block, the halo offset of the row, column phase and index
@@ -507,7 +546,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             if (tracing) stall_acc += clock64() - ta;
             trace_mark(p, 0, 3, u);
 #endif
-            d_tmem = tmem_base + buf * BN;
+            d_tmem = tmem_base + buf * BN + nh_cols;
             next_chunk = kk + p.chunk_slices;
             acc_flag = 0;
           }
@@ -538,7 +577,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
               const uint32_t a_c = h_stage + static_cast<uint32_t>(rowpos + tapoff[t]);
               adv0[t] = a_desc0 | static_cast<uint64_t>(a_c & 0x3FFFu);
               adv1[t] = a_desc0 | static_cast<uint64_t>((a_c + chunk2_lo) & 0x3FFFu);
-              bdv[t] = b_desc0 | static_cast<uint64_t>((b_cur + t * slice_lo) & 0x3FFFu);
+              bdv[t] = b_desc0 | static_cast<uint64_t>((b_cur + nh_lo + t * slice_lo) & 0x3FFFu);
             }
             if (ptx::elect_one()) {
 #pragma unroll
@@ -547,8 +586,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
                   ptx::mma_f16_ss_pair(d_tmem, adv0[t], bdv[t], idesc, t == 0 ? acc_flag : 1u);
                   ptx::mma_f16_ss_pair(d_tmem, adv1[t], bdv[t] + 2, idesc, 1u);
                 } else {
-                  ptx::mma_f16_ss(d_tmem, adv0[t], bdv[t], idesc, t == 0 ? acc_flag : 1u);
-                  ptx::mma_f16_ss(d_tmem, adv1[t], bdv[t] + 2, idesc, 1u);
+                  ptx::mma_f16_ss(d_tmem, adv0[t], bdv[t], idesc_u, t == 0 ? acc_flag : 1u);
+                  ptx::mma_f16_ss(d_tmem, adv1[t], bdv[t] + 2, idesc_u, 1u);
                 }
               }
               commit_all(&b_empty[st]);
@@ -563,14 +602,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
                        : h_stage + static_cast<uint32_t>(rowpos + fph * cw_q + min(fph, cw_r) + idx);
             const uint64_t ad0 = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
             const uint64_t ad1 = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
-            const uint64_t bd = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
+            const uint64_t bd = b_desc0 | static_cast<uint64_t>((b_cur + nh_lo) & 0x3FFFu);
             if (ptx::elect_one()) {
               if constexpr (CG == 2) {
                 ptx::mma_f16_ss_pair(d_tmem, ad0, bd, idesc, acc_flag);
                 ptx::mma_f16_ss_pair(d_tmem, ad1, bd + 2, idesc, 1u);
               } else {
-                ptx::mma_f16_ss(d_tmem, ad0, bd, idesc, acc_flag);
-                ptx::mma_f16_ss(d_tmem, ad1, bd + 2, idesc, 1u);
+                ptx::mma_f16_ss(d_tmem, ad0, bd, idesc_u, acc_flag);
+                ptx::mma_f16_ss(d_tmem, ad1, bd + 2, idesc_u, 1u);
               }
             }
             __syncwarp();
@@ -754,6 +793,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     for (int unit = tile_sched<CG>().first; ok && unit < hp.num_units; unit += tile_sched<CG>().step) {
       const WorkUnit wu = decode_unit(unit, hp);
       const int nch = ((wu.cb1 - wu.cb0) * RS + p.chunk_slices - 1) / p.chunk_slices;
+      // a half-width unit's columns belong to one column half of the warps
+      const bool mine = col_owner && (wu.nh < 0 || wu.nh == eh);
       for (int c = 0; c < nch; ++c, ++u) {
         const uint32_t buf = u & 1u;
 #if defined(I8C_PIPELINE_TRACE)
@@ -770,7 +811,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         ptx::tc_fence_after();
         const uint32_t t_acc = tmem_base + lane_addr + buf * BN + col0;
         const bool first = c == 0;
-        if (col_owner) {
+        if (mine) {
 #pragma unroll
           for (int g = 0; g < kColsPerWarp / 32; ++g) {
             uint32_t v[32];
@@ -840,10 +881,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             }
           }
         }
-        if (!col_owner) continue;
+        if (!mine) continue;
         const PatchTile t = decode_patch(wu.tile, hp, tile_sched<CG>());
-        const int pp = t.p0 + (row >> 3);
-        const int qq = t.q0 + (row & 7);
+        const int pp = hp.flat ? (t.m0 + row) / hp.CW : t.p0 + (row >> 3);
+        const int qq = hp.flat ? (t.m0 + row) - pp * hp.CW : t.q0 + (row & 7);
         if (t.valid && pp < p.P && qq < p.Q) {
 #pragma unroll
           for (int g = 0; g < kColsPerWarp / 32; ++g) {

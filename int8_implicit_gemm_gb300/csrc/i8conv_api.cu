@@ -119,21 +119,38 @@ double wave_efficiency(int64_t tiles, int ctas) {
 // stages, the int8 staging ring (if any), the filter stages, the barriers.
 // loads: 0 = auto, 1 = staging ring only, 2 = register loads only.  Returns
 // false when the halo does not fit with at least three filter stages.
-bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int loads, i8c::HaloParams* h,
+bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int loads, bool flat, i8c::HaloParams* h,
                  int* smem_bytes) {
   if (s.stride_w > 8) return false;
+  if (flat && (s.stride_h != 1 || s.stride_w != 1)) return false;
   *h = i8c::HaloParams{};
-  h->TPH = (P + 15) / 16;
-  h->TQW = (Q + 7) / 8;
-  const int64_t patches = static_cast<int64_t>(s.N) * h->TPH * h->TQW;
+  h->flat = flat ? 1 : 0;
+  int64_t HR, CW, npos, patches;
+  if (flat) {
+    // flat tiles: 128 consecutive pixels of the output laid out with the
+    // padded input's row width; their taps read one contiguous run
+    CW = static_cast<int64_t>(s.W) + 2LL * s.pad_w;
+    npos = 128 + static_cast<int64_t>(s.R - 1) * s.dil_h * CW + static_cast<int64_t>(s.S - 1) * s.dil_w;
+    HR = (npos + CW - 1) / CW;
+    const int64_t tpi = (static_cast<int64_t>(P) * CW + 127) / 128;
+    if (tpi > kMaxI32) return false;
+    h->tpi = static_cast<int>(tpi);
+    patches = static_cast<int64_t>(s.N) * tpi;
+  } else {
+    h->TPH = (P + 15) / 16;
+    h->TQW = (Q + 7) / 8;
+    patches = static_cast<int64_t>(s.N) * h->TPH * h->TQW;
+    HR = 15LL * s.stride_h + static_cast<int64_t>(s.R - 1) * s.dil_h + 1;
+    CW = 7LL * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
+    npos = HR * CW;
+  }
   if (patches > kMaxI32) return false;
   h->num_patches = static_cast<int>(patches);
-  const int64_t HR = 15LL * s.stride_h + static_cast<int64_t>(s.R - 1) * s.dil_h + 1;
-  const int64_t CW = 7LL * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
-  if (HR * CW > 65536) return false;
+  if (npos > 65536 || CW > 65536) return false;
   h->HR = static_cast<int>(HR);
   h->CW = static_cast<int>(CW);
-  const uint32_t pos = static_cast<uint32_t>(HR * CW);
+  h->positions = static_cast<int>(npos);
+  const uint32_t pos = static_cast<uint32_t>(npos);
   h->plane_bytes = (pos * 16 + 127) / 128 * 128;
   h->halo_bytes = 4 * h->plane_bytes;
   h->stg_bytes = (pos * 32 + 127) / 128 * 128;
@@ -342,7 +359,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
       o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 ||
-      o.tail_split > 2)
+      o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -374,17 +391,26 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->cta_group = 1;
   if (o.kernel_variant != 1) {
     // best tile width on cg CTAs per tile: {width, groups} (width 0: none fits)
-    auto search = [&](int cg, int only_bn) -> std::pair<int, int> {
-      int best_bn = 0, best_groups = 0;
+    // best {width, groups, flat} on cg CTAs per tile (width 0: none fits);
+    // tile shapes: 16x8 patches, and flat tiles for stride 1 unless forced
+    struct Choice {
+      int bn, groups;
+      bool flat;
+    };
+    auto search = [&](int cg, int only_bn) -> Choice {
+      Choice bestc{0, 0, false};
       double best = -1.0;
+      for (int geo = 0; geo < 2; ++geo)
       for (int cand : {256, 128, 64, 32}) {
+        const bool flat = geo == 1;
+        if ((flat && o.tile_shape == 1) || (!flat && o.tile_shape == 2)) continue;
         if (o.block_n != 0 && cand != o.block_n) continue;
         if (only_bn != 0 && cand != only_bn) continue;
         if (cg == 2 && cand < 64) continue;
         if (o.block_n == 0 && cand > 32 * cg && cand / 2 >= s.K) continue;  // half the tile would be empty
         i8c::HaloParams h;
         int sm = 0;
-        if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, &h, &sm)) continue;
+        if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, flat, &h, &sm)) continue;
         int g = ctas / cg;
         if (cg == 2) {
           // pairs that fit on the GPU at once (clusters need both SMs free)
@@ -401,35 +427,38 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
         double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
         // runs of one K-slice (no room for longer filter stages) issue poorly
         if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
-        const double score =
-            wave_efficiency(t, g) * width_eff * static_cast<double>(s.K) / (static_cast<double>(nt) * cand);
+        // share of a tile's 128 rows that are real output pixels
+        const double m_util =
+            static_cast<double>(p->P) * p->Q /
+            (flat ? 128.0 * h.tpi : 128.0 * h.TPH * h.TQW);
+        const double score = wave_efficiency(t, g) * m_util * width_eff * static_cast<double>(s.K) /
+                             (static_cast<double>(nt) * cand);
         if (score > best * 1.02) {
           best = score;
-          best_bn = cand;
-          best_groups = g;
+          bestc = {cand, g, flat};
         }
       }
-      return {best_bn, best_groups};
+      return bestc;
     };
     int cg = o.kernel_variant == 3 ? 2 : 1;
-    std::pair<int, int> best = search(cg, 0);
-    if (o.kernel_variant == 0 && best.first == 64) {
+    Choice best = search(cg, 0);
+    if (o.kernel_variant == 0 && best.bn == 64) {
       // 64-wide tiles issue MMAs at the tensor core's per-instruction floor; a
       // CTA pair's M = 256 MMAs halve the instructions per SM (measured on the
       // dilated 5x9 layer: 1042 against 889 TOPS).  At 256 columns single
       // CTAs are faster.
-      const std::pair<int, int> pair = search(2, 64);
-      if (pair.first != 0) {
+      const Choice pair = search(2, 64);
+      if (pair.bn != 0) {
         cg = 2;
         best = pair;
       }
     }
-    if (best.first != 0) {
-      bn = best.first;
-      groups = best.second;
+    if (best.bn != 0) {
+      bn = best.bn;
+      groups = best.groups;
       p->kernel_variant = cg == 2 ? 3 : 2;
       p->cta_group = cg;
-      halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, &p->halo, &halo_smem);
+      halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, best.flat, &p->halo, &halo_smem);
     } else if (o.kernel_variant >= 2) {
       delete p;
       return I8C_ERR_UNSUPPORTED;
@@ -459,8 +488,14 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     // 1/ksplit of a tile's time.
     const int g = p->cta_group == 2 ? groups : ctas;
     const int rem = p->num_tiles % g;
-    int ksplit = 1;
-    if (rem > 0 && o.tail_split != 1) {
+    int ksplit = 1, nsplit = 1;
+    // Halving the last wave's tiles along the output channels needs no
+    // partial sums (disjoint outputs); its N = BN/2 MMAs run at a lower rate,
+    // so it is taken for 128- and 256-wide tiles when all halves fit in the
+    // wave.
+    if (rem > 0 && p->cta_group == 1 && bn >= 128 && 2 * rem <= g && (o.tail_split == 0 || o.tail_split == 3))
+      nsplit = 2;
+    if (nsplit == 1 && rem > 0 && o.tail_split != 1 && o.tail_split != 3) {
       ksplit = g / rem;
       if (ksplit > s.C / 32) ksplit = s.C / 32;
       if (ksplit < 2) ksplit = 1;
@@ -478,8 +513,9 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (saved_us < 1.5 * cost_us) ksplit = 1;
     }
     p->halo.ksplit = ksplit;
-    p->halo.full_units = ksplit > 1 ? p->num_tiles - rem : p->num_tiles;
-    p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0);
+    p->halo.nsplit = nsplit;
+    p->halo.full_units = ksplit > 1 || nsplit > 1 ? p->num_tiles - rem : p->num_tiles;
+    p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0) + (nsplit > 1 ? rem * 2 : 0);
     if (ksplit > 1)
       split_bytes = static_cast<int64_t>(rem) * ksplit * p->cta_group * 128 * bn * static_cast<int64_t>(sizeof(int32_t));
     p->split_tiles = ksplit > 1 ? rem : 0;
@@ -606,6 +642,8 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->halo_staging = pl->kernel_variant >= 2 ? pl->halo.nstg : 0;
   info->filter_run = pl->kernel_variant >= 2 ? pl->halo.bgroup : 1;
   info->tail_split = pl->kernel_variant >= 2 ? pl->halo.ksplit : 1;
+  info->tail_halves = pl->kernel_variant >= 2 ? pl->halo.nsplit : 1;
+  info->flat_tiles = pl->kernel_variant >= 2 ? pl->halo.flat : 0;
   info->work_units = pl->kernel_variant >= 2 ? pl->halo.num_units : pl->num_tiles;
   info->filter_stages = pl->kernel_variant >= 2 ? pl->halo.nbs
                         : pl->block_n >= 256 ? i8c::TileCfg<256>::kStages

@@ -71,6 +71,39 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
       else ptx::mbar_try_wait(&never, 0);
     }
   }
+  // modes 19/20: a four-stage ring of full/empty barriers between the MMA
+  // warp (mode 8's run loop, waiting on `full`, committing to `empty`) and a
+  // producer warp that, per run, waits for the stage to be released and
+  // arrives on its `full` barrier (no data moves): the kernel's handshake
+  // without its loads.  19: the producer sleeps in its waits; 20: it spins.
+  __shared__ uint64_t pfull[4], pempty[4];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) {
+      ptx::mbar_init(&pfull[i], 1);
+      ptx::mbar_init(&pempty[i], 1);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const int runs = iters / 6;
+  if ((loop_mode == 19 || loop_mode == 20) && warp == 4) {
+    for (int r = 0; r < runs; ++r) {
+      const int st = r & 3;
+      const uint32_t ph = static_cast<uint32_t>(r >> 2) & 1u;
+      bool got;
+      if (loop_mode == 19) {
+        got = ptx::mbar_wait(&pempty[st], ph ^ 1u, 1000000000ull, nullptr);
+      } else {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        got = false;
+        while (!(got = ptx::mbar_try_wait(&pempty[st], ph ^ 1u)) && ptx::globaltimer_ns() - t0 < 1000000000ull) {
+        }
+      }
+      if (!__all_sync(0xffffffffu, got)) break;
+      if (ptx::elect_one()) ptx::mbar_arrive(&pfull[st]);
+      __syncwarp();
+    }
+  }
   if (loop_mode >= 4 && threadIdx.x < 32) {
     // The same per-K-slice pattern issued from a warp in uniform control
     // flow: the A offset comes from loop counters (mode 4) or from the
@@ -102,6 +135,46 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
         const long long w0 = clock64();
         while (clock64() - w0 < D) {
         }
+      }
+      const long long t1 = clock64();
+      stop = 1;
+      if (ptx::elect_one()) ptx::mma_commit(&bar);
+      __syncwarp();
+      const bool done = ptx::mbar_wait(&bar, 0, 2000000000ull, nullptr);
+      const long long t2 = clock64();
+      if (threadIdx.x == 0) {
+        out[3 * blockIdx.x + 0] = t1 - t0;
+        out[3 * blockIdx.x + 1] = t2 - t0;
+        out[3 * blockIdx.x + 2] = done ? 1 : 0;
+      }
+    } else if (loop_mode == 19 || loop_mode == 20) {
+      const uint64_t a_desc0 = ad & ~static_cast<uint64_t>(0x3FFF);
+      const uint64_t b_desc0 = bd & ~static_cast<uint64_t>(0x3FFF);
+      const uint32_t h_stage = static_cast<uint32_t>(ad & 0x3FFF), b_lo0 = static_cast<uint32_t>(bd & 0x3FFF);
+      const uint32_t chunk2_lo = 2560 >> 4, slice_lo = (N * 64) >> 4;
+      uint32_t acc_flag = 0;
+      const long long t0 = clock64();
+      for (int r = 0; r < runs; ++r) {
+        const int st = r & 3;
+        const uint32_t ph = static_cast<uint32_t>(r >> 2) & 1u;
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(&pfull[st], ph, 1000000000ull, nullptr))) break;
+        ptx::tc_fence_after();
+        uint32_t b_cur = b_lo0 + static_cast<uint32_t>(r & 1) * slice_lo;
+        for (int t = 0; t < 3; ++t) {
+          const uint32_t a_cur = h_stage + static_cast<uint32_t>((r % 3) * 10 + t);
+          const uint64_t ad0 = a_desc0 | static_cast<uint64_t>(a_cur & 0x3FFFu);
+          const uint64_t ad1 = a_desc0 | static_cast<uint64_t>((a_cur + chunk2_lo) & 0x3FFFu);
+          const uint64_t bdd = b_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
+          if (ptx::elect_one()) {
+            ptx::mma_f16_ss(tmem, ad0, bdd, idesc, acc_flag);
+            ptx::mma_f16_ss(tmem, ad1, bdd + 2, idesc, 1u);
+          }
+          __syncwarp();
+          acc_flag = 1;
+          b_cur += slice_lo;
+        }
+        if (ptx::elect_one()) ptx::mma_commit(&pempty[st]);
+        __syncwarp();
       }
       const long long t1 = clock64();
       stop = 1;

@@ -162,3 +162,33 @@ def test_split_tail_exact(kw):
         y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -12, tail_split=ts, **kw)
         assert np.array_equal(acc, acc_ref.astype(np.int32)), ts
         assert np.array_equal(y, y_ref), ts
+
+
+@pytest.mark.parametrize("kw", [dict(block_n=256, num_ctas=9), dict(block_n=128, num_ctas=20), dict(block_n=256, num_ctas=8)],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
+def test_halved_tail_exact(kw):
+    """Tiles of a partial last wave halved along the output channels (two
+    units with N = BN/2 MMAs and disjoint outputs) give the oracle's results."""
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 64, 13, 11, 256, 3, 3, 1, 1, 1, 1, 1, 1)
+    plan = ext.Plan(shape, tail_split=3, **kw)
+    assert plan.info["tail_halves"] == 2, plan.info
+    plan.destroy()
+    x, f = _data(shape, 5151)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -11)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -11, tail_split=3, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+@pytest.mark.parametrize("shape", [s for s in SMALL if s[9] == 1 and s[10] == 1], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kw", [dict(kernel_variant=2), dict(kernel_variant=3), dict(kernel_variant=2, halo_loads=1)],
+                         ids=["single", "pair", "staged"])
+def test_flat_tiles_exact(shape, kw):
+    """Tiles of 128 consecutive pixels of the padded row-major output (stride
+    1): every real output pixel exact, the discarded ones never stored."""
+    x, f = _data(shape, 777 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -9)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -9, tile_shape=2, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
