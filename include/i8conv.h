@@ -97,6 +97,11 @@ typedef struct {
                                 16x8 patch, 2 = 128 consecutive pixels of the output laid out
                                 with the zero-padded input's row width (stride 1 only; the
                                 pixels past Q in each row are computed and discarded)       */
+  int32_t fused_filter;      /* halo kernel on single CTAs: 0 = convert the int8 filter to the
+                                fp16 operand copy in a separate kernel launched first (the
+                                convolution's prologue overlaps its tail), 1 = inside the
+                                convolution kernel (one launch per run; cooperative launch,
+                                all CTAs resident; measured slower)                         */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so

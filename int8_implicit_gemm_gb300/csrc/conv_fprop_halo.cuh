@@ -59,6 +59,14 @@ struct HaloParams {
   int num_units, full_units, ksplit, nsplit;
   int* split_count;         // [tail tiles][cg], zero between launches
   int32_t* split_part;      // [tail tiles][ksplit][cg][BN/4][128][4]
+  // In-kernel filter conversion (single CTAs, cooperative launch): the
+  // epilogue warps of every CTA convert a share of the int8 filter into f16
+  // before their first drain; a grid barrier (gbar: arrivals, generation)
+  // tells the filter TMA warps that the whole copy is written.
+  const int8_t* f_int8;     // null: the conversion kernel ran before this one
+  uint16_t* f16;
+  int64_t f_vecs;           // 16-element vectors of the filter
+  uint32_t* gbar;           // {arrivals, generation}, arrivals zero between launches
 };
 
 
@@ -379,6 +387,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 11) + 1;
   uint64_t* epi_sync = h_full + 12;                                    // the epilogue warps' own barrier
   volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 13);  // this CTA combines a split tile
+  uint64_t* fconv_done = h_full + 14;  // this CTA's share of the filter is converted and announced
+  volatile uint32_t* fconv_gen = reinterpret_cast<volatile uint32_t*>(h_full + 15);  // grid barrier generation seen
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -407,6 +417,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     }
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(epi_sync, kEpilogue);
+    ptx::mbar_init(fconv_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -694,9 +705,29 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
     ptx::setmaxnreg_dec<kWorkerRegs>();
-    // the fp16 filter is written by the conversion kernel launched just
-    // before this one, which this kernel may overlap (dependent launch)
-    ptx::griddep_wait();
+    if (hp.f_int8 != nullptr) {
+      // the filter is converted inside this launch: wait until every CTA's
+      // share is written (grid barrier), then let TMA read it
+      bool fine = __all_sync(0xffffffffu, ptx::mbar_wait(fconv_done, 0, p.timeout_ns, abort_flag));
+      if (fine) {
+        const uint32_t seen = *fconv_gen;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::ld_acquire_gpu(hp.gbar + 1) == seen) {
+          if (ptx::globaltimer_ns() - t0 > p.timeout_ns || *abort_flag) {
+            fine = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        fine = __all_sync(0xffffffffu, fine);
+      }
+      ptx::fence_proxy_async_global();
+      if (!fine && lane == 0) raise_timeout(p, abort_flag);
+    } else {
+      // the fp16 filter is written by the conversion kernel launched just
+      // before this one, which this kernel may overlap (dependent launch)
+      ptx::griddep_wait();
+    }
     const TileSched ts = tile_sched<CG>();
     const int G = GT > 0 ? GT : hp.bgroup;
     const uint32_t stage_bytes = static_cast<uint32_t>(G * BNH * 64);
@@ -771,6 +802,43 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // holds two fp32 chunk accumulators and a drain is one read of the
     // accumulator that overlaps the MMAs of the next chunk.
     ptx::setmaxnreg_inc<kEpilogueRegs>();
+    if (hp.f_int8 != nullptr) {
+      // this CTA's share of the int8 -> f16 filter copy (same layout), then
+      // one arrival per CTA on the grid barrier; the generation it saw goes to
+      // the TMA warp
+      const int64_t per = (hp.f_vecs + gridDim.x - 1) / gridDim.x;
+      const int64_t v0 = per * blockIdx.x;
+      const int64_t v1 = v0 + per < hp.f_vecs ? v0 + per : hp.f_vecs;
+      const uint4* src = reinterpret_cast<const uint4*>(hp.f_int8);
+      uint4* dst = reinterpret_cast<uint4*>(hp.f16);
+      for (int64_t i = v0 + (threadIdx.x - 8 * 32); i < v1; i += kEpilogue) {
+        const uint4 v = __ldg(src + i);
+        uint4 c0, c1;
+        i8x4_to_f16x4(v.x, c0.x, c0.y);
+        i8x4_to_f16x4(v.y, c0.z, c0.w);
+        i8x4_to_f16x4(v.z, c1.x, c1.y);
+        i8x4_to_f16x4(v.w, c1.z, c1.w);
+        dst[2 * i] = c0;
+        dst[2 * i + 1] = c1;
+      }
+      ptx::fence_proxy_async_global();
+      __threadfence();
+      ptx::mbar_arrive(epi_sync);
+      const bool all_done = ptx::mbar_wait(epi_sync, 0, p.timeout_ns, abort_flag);
+      if (threadIdx.x == 8 * 32 && all_done) {
+        const uint32_t gen = *reinterpret_cast<volatile uint32_t*>(hp.gbar + 1);
+        __threadfence();
+        if (atomicAdd(hp.gbar, 1u) == gridDim.x - 1) {
+          // last arrival: reset the count for the next launch, open the barrier
+          atomicExch(hp.gbar, 0u);
+          __threadfence();
+          atomicAdd(hp.gbar + 1, 1u);
+        }
+        *fconv_gen = gen;
+        ptx::mbar_arrive(fconv_done);
+      }
+      if (!__all_sync(0xffffffffu, all_done) && lane == 0) raise_timeout(p, abort_flag);
+    }
     const int qd = warp & 3;
     const int row = 32 * qd + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
@@ -780,7 +848,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const int col0 = BN >= 64 ? eh * kColsPerWarp : 0;
     const bool col_owner = BN >= 64 || eh == 0;
     uint32_t run[kColsPerWarp];  // running int32 sums of this thread's pixel over its columns
-    uint32_t u = 0, esync = 0;
+    uint32_t u = 0, esync = hp.f_int8 != nullptr ? 1u : 0u;  // epi_sync phases used so far
     bool ok = true;
     const int RS = p.R * p.S;
     // all epilogue threads meet (bounded wait: a warp that gave up cannot hang the others)

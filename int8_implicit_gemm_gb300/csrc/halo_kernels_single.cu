@@ -24,4 +24,14 @@ cudaError_t halo_launch_single(int block_n, const CUtensorMap& tmap, const HaloP
   }
 }
 
+int halo_single_max_ctas(int block_n, int bgroup, int S, int smem) {
+  switch (block_n) {
+    case 32: return halo_max_ctas_bn<32>(bgroup, S, smem);
+    case 64: return halo_max_ctas_bn<64>(bgroup, S, smem);
+    case 128: return halo_max_ctas_bn<128>(bgroup, S, smem);
+    case 256: return halo_max_ctas_bn<256>(bgroup, S, smem);
+    default: return 0;
+  }
+}
+
 }  // namespace i8c

@@ -30,12 +30,14 @@ cudaError_t halo_prepare_bn() {
   return cudaSuccess;
 }
 
-// CTA pairs are launched as clusters of two.  Single CTAs are launched as
-// programmatic dependents of the filter conversion kernel: their prologue
-// (barriers, tensor memory, halo loads) overlaps that kernel's tail and only
-// the filter loads wait for it.
+// CTA pairs are launched as clusters of two.  Single CTAs that convert the
+// filter themselves are launched cooperatively (all CTAs resident: their grid
+// barrier cannot wait on a CTA that has not started); otherwise as
+// programmatic dependents of the filter conversion kernel, whose tail their
+// prologue (barriers, tensor memory, halo loads) overlaps.
 template <int CG>
-cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t stream, cudaLaunchAttribute* attr,
+                                      bool cooperative = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
   cfg.blockDim = dim3(kHaloThreads);
@@ -46,6 +48,9 @@ cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t strea
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+  } else if (cooperative) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
   } else {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -59,7 +64,7 @@ template <int BN, int CG>
 cudaError_t halo_launch_bn(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
                            cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr);
+  const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr, p.f_int8 != nullptr);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
@@ -75,6 +80,17 @@ int halo_max_clusters_bn(int bgroup, int S, int smem) {
       cudaSuccess)
     return 0;
   return n;
+}
+
+// CTAs of one kernel instance that fit on the GPU at once (0 if the query fails).
+template <int BN>
+int halo_max_ctas_bn(int bgroup, int S, int smem) {
+  int per_sm = 0, dev = 0, sms = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, halo_kernel_for<BN, 1>(bgroup, S), kHaloThreads,
+                                                    static_cast<size_t>(smem)) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return per_sm * sms;
 }
 
 }  // namespace i8c

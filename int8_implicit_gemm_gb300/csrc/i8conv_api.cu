@@ -35,6 +35,7 @@ struct i8c_plan {
   long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), kTraceRows * kTraceSlots entries
   CUtensorMap tmap;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
+  uint32_t* gbar;        // halo kernel converting the filter itself: grid barrier {arrivals, generation}
   int* split_count;      // halo kernel, split tail tiles: arrivals per tile and CTA rank
   int32_t* split_part;   // halo kernel, split tail tiles: int32 partial sums
   size_t x_bytes, f_bytes, y_bytes;
@@ -215,6 +216,7 @@ void free_plan_memory(i8c_plan* p) {
   if (p->stage_f) cudaFree(p->stage_f);
   if (p->stage_y) cudaFree(p->stage_y);
   if (p->split_count) cudaFree(p->split_count);
+  if (p->gbar) cudaFree(p->gbar);
   if (p->split_part) cudaFree(p->split_part);
 }
 
@@ -258,8 +260,11 @@ ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
 i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t* y, int32_t* acc, float alpha,
                     cudaStream_t stream) {
   const i8c_conv_shape& s = pl->shape;
-  cudaError_t e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
-  if (e != cudaSuccess) return from_cuda(e);
+  cudaError_t e = cudaSuccess;
+  if (pl->gbar == nullptr) {  // else the halo kernel converts the filter itself
+    e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   ConvParams p = make_params(pl, x, alpha);
   p.y = y;
   p.acc = acc;
@@ -272,6 +277,12 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
   if (pl->kernel_variant >= 2) {
     i8c::HaloParams hp = pl->halo;
     hp.c = p;
+    if (pl->gbar != nullptr) {
+      hp.f_int8 = f;
+      hp.f16 = pl->f16;
+      hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
+      hp.gbar = pl->gbar;
+    }
     e = pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
                                 : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
                                                           stream);
@@ -359,7 +370,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
       o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 ||
-      o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2)
+      o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
+      o.fused_filter > 1)
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -559,6 +571,18 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
+  if (e == cudaSuccess && p->kernel_variant == 2 && o.fused_filter == 1) {
+    // Single-CTA halo kernel, on request: the filter conversion moves into the
+    // kernel (one launch per run) when all of its CTAs fit on the GPU at once.
+    // Measured slower than the separate conversion kernel, whose tail the
+    // convolution's prologue overlaps (e.g. 37.0 against 35.0 us per run on
+    // the 8x256x56x56 layer): the grid barrier delays the first filter load.
+    const int fit = i8c::halo_single_max_ctas(bn, p->halo.bgroup, s.S, halo_smem);
+    if (fit >= p->num_ctas) {
+      e = cudaMalloc(&p->gbar, 2 * sizeof(uint32_t));
+      if (e == cudaSuccess) e = cudaMemset(p->gbar, 0, 2 * sizeof(uint32_t));
+    }
+  }
   p->workspace_bytes = static_cast<int64_t>(p->f_bytes * 2 + sizeof(int));
   if (e == cudaSuccess && split_bytes > 0) {
     const size_t counts = sizeof(int) * static_cast<size_t>(p->split_tiles) * p->cta_group;
@@ -637,7 +661,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->chunk_slices = pl->chunk_slices;
   info->acc_buffers = pl->acc_buffers;
   info->smem_bytes = pl->smem_bytes;
-  info->kernels_per_run = 2;
+  info->kernels_per_run = pl->gbar != nullptr ? 1 : 2;
   info->kernel_variant = pl->kernel_variant;
   info->halo_staging = pl->kernel_variant >= 2 ? pl->halo.nstg : 0;
   info->filter_run = pl->kernel_variant >= 2 ? pl->halo.bgroup : 1;
@@ -721,6 +745,8 @@ i8c_status i8c_plan_status(const i8c_plan* pl, cudaStream_t stream) {
     // a launch that gave up may have left split-tile arrivals behind
     if (e == cudaSuccess && pl->split_count != nullptr)
       e = cudaMemset(pl->split_count, 0, sizeof(int) * static_cast<size_t>(pl->split_tiles) * pl->cta_group);
+    // and a grid barrier with missing arrivals
+    if (e == cudaSuccess && pl->gbar != nullptr) e = cudaMemset(pl->gbar, 0, 2 * sizeof(uint32_t));
     if (e != cudaSuccess) return from_cuda(e);
   }
   return h == 0 ? I8C_OK : static_cast<i8c_status>(h);

@@ -30,6 +30,7 @@ cudaError_t halo_prepare_pair(int block_n);
 cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes,
                              int num_ctas, cudaStream_t stream);
 int halo_pair_max_clusters(int block_n, int bgroup, int S, int smem_bytes);
+int halo_single_max_ctas(int block_n, int bgroup, int S, int smem_bytes);  // resident at once
 constexpr int kMaxDynamicSmem = 232448;
 
 // layout_kernels.cu

@@ -152,3 +152,26 @@ def test_plan_runs_captured_in_a_cuda_graph(torch_cuda):
         y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
         assert np.array_equal(y.cpu().numpy().reshape(y_ref.shape), y_ref)
     plan.destroy()
+
+
+def test_filter_conversion_inside_the_kernel(torch_cuda):
+    """fused_filter = 1: the halo kernel converts the filter itself behind a
+    grid barrier (one launch per run); outputs stay exact over repeated runs
+    with different filters."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 13, 11, 256, 3, 3, 1, 1, 1, 1, 1, 1)
+    plan = ext.Plan(shape, kernel_variant=2, fused_filter=1)
+    assert plan.info["kernels_per_run"] == 1
+    P, Q = plan.info["P"], plan.info["Q"]
+    for seed in (41, 42, 43):
+        x = synth.uniform_int8(seed, 2 * 64 * 13 * 11, -128, 127).reshape(2, 64, 13, 11)
+        f = synth.uniform_int8(seed + 7, 256 * 64 * 9, -128, 127).reshape(256, 64, 3, 3)
+        xp, fp = gpu_util.packed_inputs(x, f)
+        y = torch.zeros(2 * 256 * P * Q, dtype=torch.int8, device="cuda")
+        plan.run(torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda(), y, 2.0 ** -11)
+        torch.cuda.synchronize()
+        assert plan.status() == ext.I8C_OK
+        y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -11)
+        assert np.array_equal(y.cpu().numpy().reshape(y_ref.shape), y_ref)
+    plan.destroy()
