@@ -86,13 +86,13 @@ typedef struct {
                                 staging memory); I8C_ERR_UNSUPPORTED if the forced form
                                 does not fit                                               */
   int32_t tail_split;        /* halo kernel, the tiles of a partial last wave: 0 = auto (split
-                                into their two halves of output channels when the halves fit
-                                in the wave and the tile is 128 or 256 wide, else split along
-                                the channel blocks when the estimated saving clearly exceeds
-                                the partial-sum traffic), 1 = never split, 2 = split along the
-                                channel blocks (int32 partial sums combined by the unit that
-                                finishes last; needs plan workspace) whenever the last wave is
-                                partial, 3 = halve along the output channels when possible  */
+                                along the channel blocks when the estimated saving clearly
+                                exceeds the partial-sum traffic), 1 = never split, 2 = split
+                                along the channel blocks (int32 partial sums combined by the
+                                unit that finishes last; needs plan workspace) whenever the
+                                last wave is partial, 3 = halve them along the output channels
+                                (N = BN/2 MMAs, disjoint outputs) when the halves fit in the
+                                wave and the tile is 128 or 256 wide                         */
   int32_t tile_shape;        /* halo kernel, the 128 output pixels of a tile: 0 = auto, 1 = a
                                 16x8 patch, 2 = 128 consecutive pixels of the output laid out
                                 with the zero-padded input's row width (stride 1 only; the

@@ -502,11 +502,11 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     const int rem = p->num_tiles % g;
     int ksplit = 1, nsplit = 1;
     // Halving the last wave's tiles along the output channels needs no
-    // partial sums (disjoint outputs); its N = BN/2 MMAs run at a lower rate,
-    // so it is taken for 128- and 256-wide tiles when all halves fit in the
-    // wave.
-    if (rem > 0 && p->cta_group == 1 && bn >= 128 && 2 * rem <= g && (o.tail_split == 0 || o.tail_split == 3))
-      nsplit = 2;
+    // partial sums (disjoint outputs), but a K-slice costs the MMA warp about
+    // as long at N = BN/2 as at BN (barrier waits and issue work dominate), so
+    // a half unit takes nearly a whole tile's time: measured no faster on the
+    // 8x256x56x56 layer, hence only on request.
+    if (rem > 0 && p->cta_group == 1 && bn >= 128 && 2 * rem <= g && o.tail_split == 3) nsplit = 2;
     if (nsplit == 1 && rem > 0 && o.tail_split != 1 && o.tail_split != 3) {
       ksplit = g / rem;
       if (ksplit > s.C / 32) ksplit = s.C / 32;
