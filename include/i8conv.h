@@ -79,7 +79,10 @@ typedef struct {
   int32_t kernel_variant;    /* 0 = auto, 1 = per-tap gather kernel, 2 = halo kernel (16x8
                                 output patches; I8C_ERR_UNSUPPORTED if its halo does not fit),
                                 3 = halo kernel on CTA pairs (clusters of two SMs sharing one
-                                M = 256 MMA per K-step; block_n 64, 128 or 256)              */
+                                M = 256 MMA per K-step; block_n 64, 128 or 256), 4 = transposed
+                                tiles (128 output channels x tile_px output pixels per tile, the
+                                MMA's M on the channels; stride 1 only, else
+                                I8C_ERR_UNSUPPORTED)                                         */
   int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
                                 (currently the same as 2), 1 = int8 staging ring filled by
                                 cp.async ahead of use, 2 = straight into registers (no
@@ -102,6 +105,12 @@ typedef struct {
                                 convolution's prologue overlaps its tail), 1 = inside the
                                 convolution kernel (one launch per run; cooperative launch,
                                 all CTAs resident; measured slower)                         */
+  int32_t tile_px;           /* transposed tiles: output pixels per tile, 0 = auto (the width
+                                whose tile count fills the SMs' waves best), else a multiple
+                                of 16 from 16 to 256                                          */
+  int32_t filter_run;        /* transposed tiles: K-slices (taps of one channel block) per
+                                filter stage, 0 = auto (the longest that leaves two stages),
+                                else a divisor of R*S; I8C_ERR_UNSUPPORTED if it does not fit */
 } i8c_options;
 
 /* debug_flags: make the activation producers skip their first arrival, so
@@ -130,7 +139,9 @@ typedef struct {
   int64_t ops;               /* 2*N*K*P*Q*C*R*S                                 */
   int64_t workspace_bytes;   /* device memory owned by the plan                */
   int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel,
-                                3 = halo kernel on CTA pairs                   */
+                                3 = halo kernel on CTA pairs, 4 = transposed
+                                tiles (block_m = tile_px pixels, block_n = 128
+                                output channels)                               */
   int32_t halo_staging;      /* halo kernel: int8 staging slots (0 = loads
                                 straight into registers); 0 for the gather kernel */
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of

@@ -17,12 +17,16 @@ extern "C" {
 
 /* One CTA per SM (num_ctas CTAs); in each, one thread issues `iters`
  * tcgen05.mma.cta_group::1.kind::f16 instructions (M = 128, N = n in
- * {32, 64, 128, 256}, K = 16, fp32 accumulate) back to back on zero operands
+ * {32, 64, 128, 176, 224, 256}, K = 16, fp32 accumulate) back to back on zero operands
  * resident in shared memory.  a_swizzled selects A's layout: 1 = 64-byte
  * swizzle; 0 = no swizzle with contiguous 8-row core matrices; 2 = no swizzle
  * with 8-row groups 160 bytes apart (a 10-position halo row); 3 = as 2 but
  * starting 16 bytes into the buffer (a filter tap shifted by one column).
- * B is always 64-byte swizzled.  loop_mode 0 issues bare MMAs; 1-3 issue them
+ * B is 64-byte swizzled, except in loop_mode 0 with a_swizzled 4 or 5 (the
+ * transposed-tile kernel's operands): A 64-byte swizzled, B without swizzle
+ * in 8-channel planes of n*16 bytes with 8-row groups 128 bytes apart,
+ * starting at the buffer (4) or 48 bytes into it (5, a shifted filter tap
+ * whose core matrices straddle 128-byte lines).  loop_mode 0 issues bare MMAs; 1-3 issue them
  * in the convolution's per-K-slice pattern (pairs of MMAs with the A start
  * from a shared-memory table; 2 adds a completed-barrier check every 4
  * slices, 3 also a commit every 4 slices).  Modes 4-18 issue from a whole

@@ -58,7 +58,7 @@ class Options(ctypes.Structure):
                 ("host_staging", ctypes.c_int32), ("debug_flags", ctypes.c_int32),
                 ("timing_events", ctypes.c_int32), ("kernel_variant", ctypes.c_int32),
                 ("halo_loads", ctypes.c_int32), ("tail_split", ctypes.c_int32), ("tile_shape", ctypes.c_int32),
-                ("fused_filter", ctypes.c_int32)]
+                ("fused_filter", ctypes.c_int32), ("tile_px", ctypes.c_int32), ("filter_run", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -211,10 +211,11 @@ class Plan:
 
     def __init__(self, shape, block_n=0, num_ctas=0, max_chunk_slices=0, wait_timeout_us=0,
                  host_staging=False, debug_flags=0, timing_events=0, kernel_variant=0, halo_loads=0, tail_split=0,
-                 tile_shape=0, fused_filter=0):
+                 tile_shape=0, fused_filter=0, tile_px=0, filter_run=0):
         self.shape = ConvShape.of(shape)
         opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(bool(host_staging)), debug_flags,
-                       timing_events, kernel_variant, halo_loads, tail_split, tile_shape, fused_filter)
+                       timing_events, kernel_variant, halo_loads, tail_split, tile_shape, fused_filter, tile_px,
+                       filter_run)
         h = ctypes.c_void_p()
         _check(lib.i8c_plan_create(ctypes.byref(self.shape), ctypes.byref(opts), ctypes.byref(h)),
                "i8c_plan_create")

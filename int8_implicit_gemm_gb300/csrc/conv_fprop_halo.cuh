@@ -36,7 +36,8 @@ struct HaloParams {
   // that the 128 pixels' taps read.
   int flat;
   int TPH, TQW;             // 2-D: patches per image along P (16 rows each) and Q (8 columns each)
-  int tpi;                  // flat: tiles per image, ceil(P * CW / 128)
+  int tpi;                  // flat: tiles per image, ceil(P * CW / tile_px)
+  int tile_px;              // flat: output pixels per tile (128; the transposed-tile kernel: 16..256)
   int num_patches;          // N * TPH * TQW, or N * tpi
   int HR, CW;               // halo rows, halo positions per row (flat: CW = padded input width)
   int positions;            // halo positions: HR * CW, or (flat) 128 + (R-1)*dh*CW + (S-1)*dw
@@ -48,6 +49,7 @@ struct HaloParams {
   int nhs;                  // fp16 halo stages: 2 or 3
   int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
   uint32_t off_stg, off_b, off_bar;
+  uint32_t off_out;         // transposed-tile kernel: the epilogue's output staging rows
   int phase_off[9];         // first position of column phase f (f < sw); phase_off[sw] = CW
   // Work units: tiles [0, full_units) whole; the remaining tiles (the last,
   // partial wave) each split into ksplit units over ranges of channel blocks,
@@ -114,7 +116,7 @@ __device__ __forceinline__ TileSched tile_sched() {
 __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp, const TileSched& ts) {
   const int nt = tile % hp.c.num_n_tiles;
   const int patch = (tile / hp.c.num_n_tiles) * ts.cg + ts.rank;
-  if (hp.flat) return {patch / hp.tpi, 0, 0, nt, patch < hp.num_patches, (patch % hp.tpi) * 128};
+  if (hp.flat) return {patch / hp.tpi, 0, 0, nt, patch < hp.num_patches, (patch % hp.tpi) * hp.tile_px};
   const int qt = patch % hp.TQW;
   const int rest = patch / hp.TQW;
   const int pt = rest % hp.TPH;
@@ -359,6 +361,87 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     hph ^= hs == 0 ? 1u : 0u;
   }
   return true;
+}
+
+// Producer for halos of at most kProducers / 2 * kPipeBatch positions (one
+// batch of 16-byte loads per thread and channel block): the next channel
+// block's loads are issued before the current one is converted and stored,
+// so each load round trip overlaps the MMAs of the channel block before it
+// instead of following them.  Returns false when a wait timed out.
+constexpr int kPipeBatch = 4;
+__device__ __forceinline__ bool halo_produce_pipelined(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                      uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
+                                                      int pt) {
+  const ConvParams& p = hp.c;
+  const int h = pt & 1;
+  const int positions = hp.positions;
+  const HaloWalk w = halo_walk(hp, pt);
+  const int HW32 = p.H * p.W * 32;
+  auto load = [&](const StageIter& it, uint4 (&v)[kPipeBatch]) {
+    const PatchTile t = decode_patch(it.tile, hp, ts);
+    const int hb0 = t.p0 * p.stride_h - p.pad_h;
+    const int wb0 = t.q0 * p.stride_w - p.pad_w;
+    const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + it.cb * HW32;
+    int e = w.e_first, b = w.b_first, pos = w.pos_first;
+    halo_walk_origin(hp, t.m0, b, pos);
+#pragma unroll
+    for (int k = 0; k < kPipeBatch; ++k) {
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (e < positions) {
+        const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+        if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
+          v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
+        e += kHaloStep;
+        b += w.b_step;
+        pos += w.pos_step;
+        if (pos >= hp.CW) {
+          pos -= hp.CW;
+          ++b;
+        }
+      }
+    }
+  };
+  uint32_t hs = 0, hph = 0;  // halo stage and its phase parity
+  bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
+  StageIter it(hp, ts);
+  if (!it.valid(hp)) return true;
+  uint4 cur[kPipeBatch];
+  load(it, cur);
+  while (true) {
+    StageIter nx = it;
+    nx.next(hp, ts);
+    const bool more = nx.valid(hp);
+    uint4 nxt[kPipeBatch];
+    if (more) load(nx, nxt);
+    // warp-uniform outcome: the arrive below is a warp-wide operation
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) return false;
+    uint8_t* halo = smem + hs * hp.halo_bytes;
+#pragma unroll
+    for (int k = 0; k < kPipeBatch; ++k) {
+      const int e = w.e_first + k * kHaloStep;
+      if (e < positions) halo_store_f16(hp, halo, e, h, cur[k]);
+    }
+    ptx::fence_proxy_async_smem();
+    arrive_on_leader(&h_full[hs], ts, !skip);
+    skip = false;
+    hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
+    hph ^= hs == 0 ? 1u : 0u;
+    if (!more) break;
+    it = nx;
+#pragma unroll
+    for (int k = 0; k < kPipeBatch; ++k) cur[k] = nxt[k];
+  }
+  return true;
+}
+
+// Which register producer a halo takes: the pipelined one when a channel
+// block is one batch per thread.
+__device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                      uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
+                                                      int pt) {
+  if (hp.positions <= (kProducers / 2) * kPipeBatch)
+    return halo_produce_pipelined(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+  return halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
 }
 
 // GT > 0 fixes the run length (K-slices per filter stage) at compile time so
@@ -793,7 +876,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
     const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+                                : halo_produce_registers(hp, ts, smem, h_full, h_empty, abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue

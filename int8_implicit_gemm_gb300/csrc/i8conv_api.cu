@@ -136,6 +136,7 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
     const int64_t tpi = (static_cast<int64_t>(P) * CW + 127) / 128;
     if (tpi > kMaxI32) return false;
     h->tpi = static_cast<int>(tpi);
+    h->tile_px = 128;
     patches = static_cast<int64_t>(s.N) * tpi;
   } else {
     h->TPH = (P + 15) / 16;
@@ -200,6 +201,68 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
       *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
       return true;
     }
+  }
+  return false;
+}
+
+// Layout of the transposed-tile kernel for np output pixels per tile
+// (stride 1 only): the flat halo of np + (R-1)*dh*CW + (S-1)*dw padded input
+// positions per channel block, two or three halo stages and at least two
+// filter stages of G K-slices x 128 output channels, and the epilogue's
+// output staging rows (np pixels x 128 channels, int8).  G is want_g if given,
+// else the longest divisor of R*S that fits.  nstg > 0: an int8 staging ring
+// of nstg slots that cp.async fills nstg - 1 channel blocks ahead.  Returns
+// false when nothing fits.
+bool tr_layout(const i8c_conv_shape& s, int P, int np, int want_g, int nstg, i8c::HaloParams* h,
+               int* smem_bytes) {
+  if (s.stride_h != 1 || s.stride_w != 1) return false;
+  if (np < 16 || np > 256 || np % 16 != 0) return false;
+  *h = i8c::HaloParams{};
+  h->flat = 1;
+  h->tile_px = np;
+  const int64_t CW = static_cast<int64_t>(s.W) + 2LL * s.pad_w;
+  const int64_t npos = np + static_cast<int64_t>(s.R - 1) * s.dil_h * CW + static_cast<int64_t>(s.S - 1) * s.dil_w;
+  const int64_t tpi = (static_cast<int64_t>(P) * CW + np - 1) / np;
+  const int64_t patches = static_cast<int64_t>(s.N) * tpi;
+  if (tpi > kMaxI32 || patches > kMaxI32 || npos > 65536 || CW > 65536) return false;
+  h->tpi = static_cast<int>(tpi);
+  h->num_patches = static_cast<int>(patches);
+  h->HR = static_cast<int>((npos + CW - 1) / CW);
+  h->CW = static_cast<int>(CW);
+  h->positions = static_cast<int>(npos);
+  h->plane_bytes = (static_cast<uint32_t>(npos) * 16 + 127) / 128 * 128;
+  h->halo_bytes = 4 * h->plane_bytes;
+  h->stg_bytes = (static_cast<uint32_t>(npos) * 32 + 127) / 128 * 128;
+  h->phase_off[0] = 0;
+  h->phase_off[1] = static_cast<int>(CW);
+  const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
+  const int RS = s.R * s.S;
+  const int64_t stage_unit = 128 * 64;  // one K-slice of 128 output channels, fp16
+  const int64_t out_bytes = static_cast<int64_t>(np) * 128;
+  for (int G = RS < 32 ? RS : 32; G >= 1; --G) {
+    if (RS % G != 0 || (want_g != 0 && G != want_g)) continue;
+    const int64_t stage = G * stage_unit;
+    int64_t nbs_for[4] = {0, 0, 0, 0};
+    const int64_t stg = static_cast<int64_t>(nstg) * h->stg_bytes;
+    for (int nhs = 2; nhs <= 3; ++nhs) {
+      const int64_t off_b = (static_cast<int64_t>(nhs) * h->halo_bytes + stg + 1023) / 1024 * 1024;
+      const int64_t n = (budget - off_b - out_bytes) / stage;
+      nbs_for[nhs] = n > i8c::kMaxBStages ? i8c::kMaxBStages : n;
+    }
+    // a third halo stage gives the producers slack unless it costs a filter stage
+    const int nhs = nbs_for[3] >= 2 && nbs_for[3] >= nbs_for[2] ? 3 : 2;
+    if (nbs_for[nhs] < 2) continue;
+    const int64_t off_b = (static_cast<int64_t>(nhs) * h->halo_bytes + stg + 1023) / 1024 * 1024;
+    h->bgroup = G;
+    h->nhs = nhs;
+    h->nstg = nstg;
+    h->nbs = static_cast<int>(nbs_for[nhs]);
+    h->off_stg = static_cast<uint32_t>(nhs * h->halo_bytes);
+    h->off_b = static_cast<uint32_t>(off_b);
+    h->off_out = static_cast<uint32_t>(off_b + nbs_for[nhs] * stage);
+    h->off_bar = static_cast<uint32_t>(h->off_out + out_bytes);
+    *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
+    return true;
   }
   return false;
 }
@@ -283,9 +346,11 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
       hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
       hp.gbar = pl->gbar;
     }
-    e = pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
-                                : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
-                                                          stream);
+    e = pl->kernel_variant == 4   ? i8c::tr_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
+                                                          stream)
+                                  : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
+                                                            stream);
   } else {
     e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
   }
@@ -369,9 +434,10 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 3 || o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 ||
-      o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
-      o.fused_filter > 1)
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 4 ||
+      o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 ||
+      o.tile_shape > 2 || o.fused_filter < 0 || o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
+      (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)))
     return I8C_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -401,7 +467,36 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   int bn = 0, halo_smem = 0, groups = 0;
   p->kernel_variant = 1;
   p->cta_group = 1;
-  if (o.kernel_variant != 1) {
+  if (o.kernel_variant == 4) {
+    // Transposed tiles: the pixel count per tile whose tile count fills the
+    // waves best.  Model: a K-slice costs the tile width in tensor-core
+    // cycles plus a fixed issue and wait overhead, and a launch takes as many
+    // tile times as its fullest SM runs tiles.
+    const int n_tiles = (s.K + 127) / 128;
+    const int tr_stg = o.halo_loads == 1 ? 3 : 0;  // staging ring on request
+    double best = 0.0;
+    int best_np = 0;
+    for (int np = 256; np >= 16; np -= 16) {
+      if (o.tile_px != 0 && np != o.tile_px) continue;
+      i8c::HaloParams h;
+      int sm = 0;
+      if (!tr_layout(s, p->P, np, o.filter_run, tr_stg, &h, &sm)) continue;
+      const int64_t t = static_cast<int64_t>(h.num_patches) * n_tiles;
+      const int64_t waves = (t + ctas - 1) / ctas;
+      const double cost = static_cast<double>(waves) * (np + 64.0);
+      if (best_np == 0 || cost < best * 0.999) {
+        best = cost;
+        best_np = np;
+      }
+    }
+    if (best_np == 0) {
+      delete p;
+      return I8C_ERR_UNSUPPORTED;
+    }
+    tr_layout(s, p->P, best_np, o.filter_run, tr_stg, &p->halo, &halo_smem);
+    p->kernel_variant = 4;
+    bn = 128;
+  } else if (o.kernel_variant != 1) {
     // best tile width on cg CTAs per tile: {width, groups} (width 0: none fits)
     // best {width, groups, flat} on cg CTAs per tile (width 0: none fits);
     // tile shapes: 16x8 patches, and flat tiles for stride 1 unless forced
@@ -493,7 +588,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
   int64_t split_bytes = 0;
-  if (p->kernel_variant >= 2) {
+  if (p->kernel_variant == 4) {
+    // one unit per tile, no split tail
+    p->halo.ksplit = 1;
+    p->halo.nsplit = 1;
+    p->halo.full_units = p->num_tiles;
+    p->halo.num_units = p->num_tiles;
+    p->split_tiles = 0;
+    p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+  } else if (p->kernel_variant >= 2) {
     // The last wave is partial when the tile count is not a multiple of the
     // persistent CTAs (pairs): its tiles are split along the channel blocks
     // into ksplit units each, so that the wave's units fill the GPU and take
@@ -552,7 +655,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (p->kernel_variant >= 2) {
     // halo kernel: two fp32 chunk accumulators; running sums live in registers
     p->acc_buffers = 2;
-    p->tmem_cols = static_cast<uint32_t>(next_pow2(2 * bn));
+    p->tmem_cols = static_cast<uint32_t>(next_pow2(2 * (p->kernel_variant == 4 ? p->halo.tile_px : bn)));
   } else {
     const int run_cols = p->num_chunks > 1 ? bn : 0;
     p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
@@ -565,7 +668,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
   p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
 
-  e = p->kernel_variant == 3   ? i8c::halo_prepare_pair(bn)
+  e = p->kernel_variant == 4   ? i8c::tr_prepare()
+      : p->kernel_variant == 3 ? i8c::halo_prepare_pair(bn)
       : p->kernel_variant == 2 ? i8c::halo_prepare_single(bn)
                                : i8c::conv_prepare(bn);
   if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
@@ -653,7 +757,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->M = pl->M;
   info->gemm_n = s.K;
   info->gemm_k = s.C * s.R * s.S;
-  info->block_m = 128 * pl->cta_group;
+  info->block_m = pl->kernel_variant == 4 ? pl->halo.tile_px : 128 * pl->cta_group;
   info->block_n = pl->block_n;
   info->num_tiles = pl->num_tiles;
   info->num_ctas = pl->num_ctas;

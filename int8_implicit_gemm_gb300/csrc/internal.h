@@ -31,6 +31,12 @@ cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const HaloPar
                              int num_ctas, cudaStream_t stream);
 int halo_pair_max_clusters(int block_n, int bgroup, int S, int smem_bytes);
 int halo_single_max_ctas(int block_n, int bgroup, int S, int smem_bytes);  // resident at once
+
+// tr_kernels.cu: the transposed-tile kernel (128 output channels x tile_px
+// pixels per tile, stride-1 layers)
+cudaError_t tr_prepare();
+cudaError_t tr_launch(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+                      cudaStream_t stream);
 constexpr int kMaxDynamicSmem = 232448;
 
 // layout_kernels.cu

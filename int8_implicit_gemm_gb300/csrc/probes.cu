@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
     *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
   __shared__ uint64_t bar;
   __shared__ uint32_t slot;
-  constexpr uint32_t cols = N < 32 ? 32 : N;
+  constexpr uint32_t cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;  // a power of two
   if (threadIdx.x == 0) {
     ptx::mbar_init(&bar, 1);
     ptx::fence_mbar_init();
@@ -321,16 +321,24 @@ __global__ void __launch_bounds__(384, 1) mma_rate_kernel(int iters, int a_swizz
     // a_layout: 0 no-swizzle, core matrices contiguous (SBO 128, LBO 2048); 1 64-byte swizzle;
     // 2 no-swizzle with 8-row groups 160 bytes apart (a 10-entry halo row) and LBO 2560;
     // 3 as 2 but starting 16 bytes in (a shifted filter tap)
-    uint64_t ad;
-    if (a_swizzled == 1) ad = ptx::smem_desc_sw64_kmajor(a);
+    // 4, 5: transposed operands -- A 64-byte swizzled (128 filter rows), B
+    // without swizzle, N pixel rows in 8-channel planes of N*16 bytes, 8-row
+    // groups 128 bytes apart; 5 starts B 48 bytes in (a tap shift: core
+    // matrices straddle 128-byte lines)
+    const bool transposed = a_swizzled == 4 || a_swizzled == 5;
+    uint64_t ad, bd;
+    if (a_swizzled == 1 || transposed) ad = ptx::smem_desc_sw64_kmajor(a);
     else if (a_swizzled == 0) ad = ptx::smem_desc_noswizzle_kmajor(a, 2048, 128);
     else ad = ptx::smem_desc_noswizzle_kmajor(a + (a_swizzled == 3 ? 16 : 0), 2560, 160);
-    const uint64_t bd = ptx::smem_desc_sw64_kmajor(b);
+    if (transposed) bd = ptx::smem_desc_noswizzle_kmajor(b + (a_swizzled == 5 ? 48 : 0), N * 16, 128);
+    else bd = ptx::smem_desc_sw64_kmajor(b);
+    const uint64_t b_khalf = transposed ? static_cast<uint64_t>(2 * N) : 2u;  // K = 16..31: 2 planes, or 32 bytes
     long long t0, t1;
     if (loop_mode == 0) {
       t0 = clock64();
       for (int i = 0; i < iters; ++i)
-        ptx::mma_f16_ss(tmem, ad + (a_swizzled == 1 ? (i & 1) * 2 : 0), bd + (i & 1) * 2, idesc, i > 0 ? 1u : 0u);
+        ptx::mma_f16_ss(tmem, ad + (a_swizzled == 1 || transposed ? (i & 1) * 2 : 0), bd + (i & 1) * b_khalf, idesc,
+                        i > 0 ? 1u : 0u);
       t1 = clock64();
     } else {
       // The convolution's per-K-slice pattern: two MMAs (K = 16 each) per
@@ -406,6 +414,8 @@ extern "C" i8c_status i8c_probe_mma_f16(int32_t n, int32_t a_swizzled, int32_t l
     case 64: e = i8c::run_rate<64>(num_ctas, iters, a_swizzled, loop_mode, cycles, elapsed_ms, stream); break;
     case 128: e = i8c::run_rate<128>(num_ctas, iters, a_swizzled, loop_mode, cycles, elapsed_ms, stream); break;
     case 256: e = i8c::run_rate<256>(num_ctas, iters, a_swizzled, loop_mode, cycles, elapsed_ms, stream); break;
+    case 176: e = i8c::run_rate<176>(num_ctas, iters, a_swizzled, loop_mode, cycles, elapsed_ms, stream); break;
+    case 224: e = i8c::run_rate<224>(num_ctas, iters, a_swizzled, loop_mode, cycles, elapsed_ms, stream); break;
     default: return I8C_ERR_INVALID_ARG;
   }
   return e == cudaSuccess ? I8C_OK : I8C_ERR_CUDA;

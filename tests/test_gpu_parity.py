@@ -116,7 +116,8 @@ def test_deterministic_repeat():
 
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
 @pytest.mark.parametrize("kw", [{}, dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
-                                dict(kernel_variant=3)], ids=["auto", "staged", "direct", "pair"])
+                                dict(kernel_variant=3), dict(kernel_variant=4)],
+                         ids=["auto", "staged", "direct", "pair", "transposed"])
 def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
     benchmark times (auto), with each halo load form forced and on CTA pairs:
@@ -192,3 +193,40 @@ def test_flat_tiles_exact(shape, kw):
     y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -9, tile_shape=2, **kw)
     assert np.array_equal(acc, acc_ref.astype(np.int32))
     assert np.array_equal(y, y_ref)
+
+
+TRANSPOSED_EXTRA = [
+    (2, 64, 20, 20, 128, 3, 3, 1, 1, 1, 1, 1, 1),     # 400 pixels per image over several tiles
+    (1, 96, 9, 33, 224, 3, 3, 1, 1, 1, 1, 1, 1),      # K = 224: the second channel tile half empty
+]
+
+
+@pytest.mark.parametrize("shape", [s for s in SMALL if s[9] == 1 and s[10] == 1] + TRANSPOSED_EXTRA,
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kw", [dict(), dict(tile_px=16), dict(tile_px=176), dict(tile_px=256),
+                                dict(tile_px=64, filter_run=3), dict(tile_px=128, filter_run=1, max_chunk_slices=5),
+                                dict(num_ctas=3, tile_px=96), dict(halo_loads=1), dict(tile_px=240, halo_loads=1)],
+                         ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "auto")
+def test_transposed_tiles_exact(shape, kw):
+    """Transposed tiles (128 output channels on the MMA's M, tile_px output
+    pixels on N, stride 1): every output exact for every tile width, filter
+    stage length, chunk length, grid size and load form."""
+    import int8_implicit_gemm_gb300 as ext
+    try:
+        ext.Plan(shape, kernel_variant=4, **kw).destroy()
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED and "filter_run" in kw:
+            pytest.skip("the forced filter stage length does not divide R*S")
+        raise
+    x, f = _data(shape, 2024 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -9)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -9, kernel_variant=4, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+def test_transposed_tiles_rejects_strides():
+    import int8_implicit_gemm_gb300 as ext
+    with pytest.raises(ext.I8ConvError) as ei:
+        ext.Plan((2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1), kernel_variant=4)
+    assert ei.value.status == ext.I8C_ERR_UNSUPPORTED
