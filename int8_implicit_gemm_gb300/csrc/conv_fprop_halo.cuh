@@ -363,84 +363,94 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
   return true;
 }
 
-// Producer for halos of at most kProducers / 2 * kPipeBatch positions (one
-// batch of 16-byte loads per thread and channel block): the next channel
-// block's loads are issued before the current one is converted and stored,
-// so each load round trip overlaps the MMAs of the channel block before it
-// instead of following them.  Returns false when a wait timed out.
-constexpr int kPipeBatch = 4;
-__device__ __forceinline__ bool halo_produce_pipelined(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
-                                                      uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
-                                                      int pt) {
+// Producer for halos of at most kSplitStep * kB positions (one batch of
+// 16-byte loads per thread and channel block), in two groups of 96
+// threads that take alternate channel blocks: warps 1-3 the even ones, 5-7
+// the odd ones.  A group issues a channel block's loads as soon as it has
+// stored its previous one, two channel blocks earlier, so each load round
+// trip (a DRAM miss for the first touch of an input row) has the MMAs of two
+// channel blocks to complete in, with one batch of registers per thread
+// (kB loads: the kernel's register split for the producer warps decides it).
+// Returns false when a wait timed out.
+constexpr int kSplitStep = kProducers / 4;  // positions between a thread's loads: 96 threads, two per position
+template <int kB>
+__device__ __forceinline__ bool halo_split_producers(const HaloParams& hp) {
+  return hp.nstg == 0 && hp.positions <= kSplitStep * kB;
+}
+// Producer arrivals that complete a halo stage (per CTA).
+template <int kB>
+__device__ __forceinline__ uint32_t halo_arrivals(const HaloParams& hp) {
+  return halo_split_producers<kB>(hp) ? kProducers / 2 : kProducers;
+}
+
+template <int kB>
+__device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                  uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
+                                                  int pt) {
   const ConvParams& p = hp.c;
-  const int h = pt & 1;
+  const uint32_t grp = pt >= kProducers / 2 ? 1u : 0u;
+  const int lt = pt - static_cast<int>(grp) * (kProducers / 2);
+  const int h = lt & 1;
+  const int e_first = lt >> 1;
+  const int b_first = e_first / hp.CW, pos_first = e_first - b_first * hp.CW;
+  const int b_step = kSplitStep / hp.CW, pos_step = kSplitStep - b_step * hp.CW;
   const int positions = hp.positions;
-  const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
-  auto load = [&](const StageIter& it, uint4 (&v)[kPipeBatch]) {
+  const uint32_t nhs = static_cast<uint32_t>(hp.nhs);
+  bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
+  uint32_t i = 0;  // channel blocks of this CTA so far, both groups'
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++i) {
+    if ((i & 1u) != grp) continue;
     const PatchTile t = decode_patch(it.tile, hp, ts);
     const int hb0 = t.p0 * p.stride_h - p.pad_h;
     const int wb0 = t.q0 * p.stride_w - p.pad_w;
     const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + it.cb * HW32;
-    int e = w.e_first, b = w.b_first, pos = w.pos_first;
+    int e = e_first, b = b_first, pos = pos_first;
     halo_walk_origin(hp, t.m0, b, pos);
+    uint4 v[kB];
 #pragma unroll
-    for (int k = 0; k < kPipeBatch; ++k) {
+    for (int k = 0; k < kB; ++k) {
       v[k] = make_uint4(0, 0, 0, 0);
       if (e < positions) {
         const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
         if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
           v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
-        e += kHaloStep;
-        b += w.b_step;
-        pos += w.pos_step;
+        e += kSplitStep;
+        b += b_step;
+        pos += pos_step;
         if (pos >= hp.CW) {
           pos -= hp.CW;
           ++b;
         }
       }
     }
-  };
-  uint32_t hs = 0, hph = 0;  // halo stage and its phase parity
-  bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
-  StageIter it(hp, ts);
-  if (!it.valid(hp)) return true;
-  uint4 cur[kPipeBatch];
-  load(it, cur);
-  while (true) {
-    StageIter nx = it;
-    nx.next(hp, ts);
-    const bool more = nx.valid(hp);
-    uint4 nxt[kPipeBatch];
-    if (more) load(nx, nxt);
+    // channel block i uses halo stage i % nhs for the (i / nhs)-th time
+    const uint32_t hs = i % nhs;
+    const uint32_t hph = (i / nhs) & 1u;
     // warp-uniform outcome: the arrive below is a warp-wide operation
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) return false;
     uint8_t* halo = smem + hs * hp.halo_bytes;
 #pragma unroll
-    for (int k = 0; k < kPipeBatch; ++k) {
-      const int e = w.e_first + k * kHaloStep;
-      if (e < positions) halo_store_f16(hp, halo, e, h, cur[k]);
+    for (int k = 0; k < kB; ++k) {
+      const int ek = e_first + k * kSplitStep;
+      if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
     skip = false;
-    hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
-    hph ^= hs == 0 ? 1u : 0u;
-    if (!more) break;
-    it = nx;
-#pragma unroll
-    for (int k = 0; k < kPipeBatch; ++k) cur[k] = nxt[k];
   }
   return true;
 }
 
-// Which register producer a halo takes: the pipelined one when a channel
-// block is one batch per thread.
+// Which register producer a halo takes: two alternating groups when a channel
+// block is one batch of kB loads per thread, else all producers on every
+// channel block.
+constexpr int kHaloSplitBatch = 5;  // the halo kernel's producers: the most that fits 72 registers
+template <int kB>
 __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                       uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                       int pt) {
-  if (hp.positions <= (kProducers / 2) * kPipeBatch)
-    return halo_produce_pipelined(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+  if (halo_split_producers<kB>(hp)) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt);
   return halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
 }
 
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < hp.nhs; ++i) {
-      ptx::mbar_init(&h_full[i], kProducers * CG);  // a pair's rank 0 counts both CTAs' producers
+      ptx::mbar_init(&h_full[i], halo_arrivals<kHaloSplitBatch>(hp) * CG);  // a pair's rank 0 counts both CTAs'
       ptx::mbar_init(&h_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -876,7 +886,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
     const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_registers(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+                                : halo_produce_registers<kHaloSplitBatch>(hp, ts, smem, h_full, h_empty,
+                                                                           abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue

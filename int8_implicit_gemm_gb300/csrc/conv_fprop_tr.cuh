@@ -33,15 +33,28 @@ namespace i8c {
 
 constexpr int kTrRows = 128;   // output channels per tile: the MMA's M
 constexpr int kTrMaxPx = 256;  // output pixels per tile: the MMA's N, at most
-constexpr int kTrMaxGroupsPerWarp = kTrMaxPx / 16;  // 8-column groups of one epilogue warp
+
+// Register split by the widest tile an instantiation serves: MAXPX = 192
+// leaves an epilogue thread 96 running sums, so its warps need fewer
+// registers and the producer warps get enough for batches of eight loads;
+// MAXPX = 256 keeps the halo kernel's split and batches of five.
+template <int MAXPX>
+struct TrRegs {
+  static constexpr uint32_t kWorker = MAXPX <= 192 ? 104 : kWorkerRegs;
+  static constexpr uint32_t kEpi = MAXPX <= 192 ? 152 : kEpilogueRegs;
+  static constexpr int kBatch = MAXPX <= 192 ? 8 : kHaloSplitBatch;
+  static_assert(128 * (2 * kWorker + 2 * kEpi) <= 512 * 128, "register split");
+};
 
 // GT > 0: filter stages of GT K-slices that are whole filter rows (S divides
 // GT), their taps' halo offsets precomputed and all their MMAs issued by one
 // elected lane in one block; GT == 0: any stage length, taps advanced slice
-// by slice.
-template <int GT>
+// by slice.  MAXPX: the widest tile (tile_px) the instantiation serves.
+template <int GT, int MAXPX>
 __global__ void __launch_bounds__(kHaloThreads, 1)
     conv_fprop_tr_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+  using Regs = TrRegs<MAXPX>;
+  constexpr int kMaxGroupsPerWarp = MAXPX / 16;  // 8-column groups of one epilogue warp
   const ConvParams& p = hp.c;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -74,7 +87,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < hp.nhs; ++i) {
-      ptx::mbar_init(&h_full[i], kProducers);
+      ptx::mbar_init(&h_full[i], halo_arrivals<Regs::kBatch>(hp));
       ptx::mbar_init(&h_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -97,7 +110,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
-    ptx::setmaxnreg_dec<kWorkerRegs>();
+    ptx::setmaxnreg_dec<Regs::kWorker>();
     const TileSched ts = tile_sched<1>();
     // The whole warp runs the loop in uniform control flow; one elected lane
     // issues each MMA and commit.
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
-    ptx::setmaxnreg_dec<kWorkerRegs>();
+    ptx::setmaxnreg_dec<Regs::kWorker>();
     // the fp16 filter is written by the conversion kernel launched just
     // before this one, which this kernel may overlap (dependent launch)
     ptx::griddep_wait();
@@ -321,11 +334,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // 32-channel block, loaded into registers (or through the int8 staging
     // ring), converted to fp16 and stored as four 8-channel planes: the same
     // producers as the halo kernel's flat tiles, with tile_px pixels per tile.
-    ptx::setmaxnreg_dec<kWorkerRegs>();
+    ptx::setmaxnreg_dec<Regs::kWorker>();
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<1>();
     const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_registers(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+                                : halo_produce_registers<Regs::kBatch>(hp, ts, smem, h_full, h_empty, abort_flag,
+                                                                       pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue
@@ -333,14 +347,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // channel block 4*kt + qd of the tile) and column half eh; its lane l
     // keeps the int32 running sums of channel 32*qd + l over that half's
     // pixels in registers.
-    ptx::setmaxnreg_inc<kEpilogueRegs>();
+    ptx::setmaxnreg_inc<Regs::kEpi>();
     const int qd = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
     const int eh = (warp - 8) >> 2;
     const int gh = NP / 16;  // 8-column groups per warp half
     const int c0 = eh * gh * 8;  // first column of this warp
     const int nch = (p.CB * RS + p.chunk_slices - 1) / p.chunk_slices;
-    uint32_t run[kTrMaxGroupsPerWarp * 8];
+    uint32_t run[kMaxGroupsPerWarp * 8];
     uint32_t u = 0;
     bool ok = true;
     for (int unit = tile_sched<1>().first; ok && unit < hp.num_units; unit += tile_sched<1>().step) {
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         const uint32_t t_acc = tmem_base + lane_addr + buf * (p.tmem_cols / 2) + static_cast<uint32_t>(c0);
         const bool first = c == 0;
 #pragma unroll
-        for (int q = 0; q < kTrMaxGroupsPerWarp / 4; ++q) {
+        for (int q = 0; q < kMaxGroupsPerWarp / 4; ++q) {
           if (4 * q >= gh) break;
           uint32_t v[4][8];
 #pragma unroll
@@ -405,7 +419,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         // their address arithmetic would not stay in the instruction cache.
         uint8_t* wbuf = smem + hp.off_out + (warp - 8) * (NP * 16);
 #pragma unroll
-        for (int g = 0; g < kTrMaxGroupsPerWarp; ++g) {
+        for (int g = 0; g < kMaxGroupsPerWarp; ++g) {
           if (g >= gh) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -430,7 +444,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         int pp = m / hp.CW;
         int qq = m - pp * hp.CW;
 #pragma unroll
-        for (int g = 0; g < kTrMaxGroupsPerWarp; ++g) {
+        for (int g = 0; g < kMaxGroupsPerWarp; ++g) {
           if (g >= gh) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {

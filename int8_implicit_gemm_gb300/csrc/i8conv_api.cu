@@ -467,13 +467,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   int bn = 0, halo_smem = 0, groups = 0;
   p->kernel_variant = 1;
   p->cta_group = 1;
-  if (o.kernel_variant == 4) {
-    // Transposed tiles: the pixel count per tile whose tile count fills the
-    // waves best.  Model: a K-slice costs the tile width in tensor-core
-    // cycles plus a fixed issue and wait overhead, and a launch takes as many
-    // tile times as its fullest SM runs tiles.
+  // Transposed tiles: the pixel count per tile whose tile count fills the
+  // waves best.  Model (measured on the 3x3 layers): a K-slice of a tile
+  // costs its width in tensor-core cycles plus about 130 cycles of issue,
+  // wait and halo overhead, and a launch takes as many tile times as its
+  // fullest SM runs tiles.  Returns the width (0: nothing fits) and its cost
+  // in cycles per K-slice of the launch.
+  const int tr_stg = o.halo_loads == 1 ? 3 : 0;  // staging ring on request
+  auto pick_tr = [&](double* cost_out) -> int {
     const int n_tiles = (s.K + 127) / 128;
-    const int tr_stg = o.halo_loads == 1 ? 3 : 0;  // staging ring on request
     double best = 0.0;
     int best_np = 0;
     for (int np = 256; np >= 16; np -= 16) {
@@ -483,17 +485,23 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (!tr_layout(s, p->P, np, o.filter_run, tr_stg, &h, &sm)) continue;
       const int64_t t = static_cast<int64_t>(h.num_patches) * n_tiles;
       const int64_t waves = (t + ctas - 1) / ctas;
-      const double cost = static_cast<double>(waves) * (np + 64.0);
+      const double cost = static_cast<double>(waves) * (np + 130.0);
       if (best_np == 0 || cost < best * 0.999) {
         best = cost;
         best_np = np;
       }
     }
-    if (best_np == 0) {
+    *cost_out = best;
+    return best_np;
+  };
+  if (o.kernel_variant == 4) {
+    double cost = 0.0;
+    const int np = pick_tr(&cost);
+    if (np == 0) {
       delete p;
       return I8C_ERR_UNSUPPORTED;
     }
-    tr_layout(s, p->P, best_np, o.filter_run, tr_stg, &p->halo, &halo_smem);
+    tr_layout(s, p->P, np, o.filter_run, tr_stg, &p->halo, &halo_smem);
     p->kernel_variant = 4;
     bn = 128;
   } else if (o.kernel_variant != 1) {
@@ -560,7 +568,33 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
         best = pair;
       }
     }
-    if (best.bn != 0) {
+    // Auto: transposed tiles instead of 256-wide single-CTA halo tiles when
+    // the model says they fill the waves enough better (a K-slice of a
+    // 128-pixel x 256-channel halo tile costs about 345 cycles).  E.g. the
+    // 8x256x56x56 layer: 224 halo tiles on 152 SMs take two tile times
+    // (2 x 345); 304 transposed tiles of 176 pixels fill two waves exactly
+    // (2 x 306).
+    bool use_tr = false;
+    if (o.kernel_variant == 0 && o.block_n == 0 && o.halo_loads == 0 && o.tile_shape == 0 && o.tail_split == 0 &&
+        o.fused_filter == 0 && best.bn == 256 && cg == 1) {
+      i8c::HaloParams h;
+      int sm = 0;
+      if (halo_layout(s, p->P, p->Q, 256, 1, 0, best.flat, &h, &sm)) {
+        const int64_t t = static_cast<int64_t>(h.num_patches) * ((s.K + 255) / 256);
+        const double halo_cost = static_cast<double>((t + ctas - 1) / ctas) * 345.0;
+        double tr_cost = 0.0;
+        const int np = pick_tr(&tr_cost);
+        if (np != 0 && tr_cost < 0.95 * halo_cost) {
+          tr_layout(s, p->P, np, o.filter_run, tr_stg, &p->halo, &halo_smem);
+          p->kernel_variant = 4;
+          bn = 128;
+          use_tr = true;
+        }
+      }
+    }
+    if (use_tr) {
+      // chosen above
+    } else if (best.bn != 0) {
       bn = best.bn;
       groups = best.groups;
       p->kernel_variant = cg == 2 ? 3 : 2;
