@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<Regs::kWorker>();
     const TileSched ts = tile_sched<1>();
     // The whole warp runs the loop in uniform control flow; one elected lane
-    // issues each MMA and commit.
+    // issues each MMA and commit (measured no slower than lane 0 alone).
     const uint32_t idesc = ptx::idesc_f16_f32(kTrRows, NP);
     const uint64_t f_desc0 = ptx::smem_desc_sw64_kmajor(0);
     // the halo as B: 8-pixel groups 128 bytes apart, 8-channel planes plane_bytes apart
@@ -142,12 +142,19 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, p.timeout_ns, abort_flag));
     };
+    // one elected lane's tcgen05 issue (MMAs or a commit)
+    auto issue = [&](auto&& f) {
+      if (ptx::elect_one()) f();
+      __syncwarp();
+    };
 #if defined(I8C_PIPELINE_TRACE)
     // CTA 0: cycles spent in each kind of wait and in the MMA issue blocks
     const bool tracing = p.trace != nullptr && blockIdx.x == 0;
-    long long stall_acc = 0, stall_b = 0, stall_h = 0, t_issue = 0, t_first = 0;
+    long long stall_acc = 0, stall_b = 0, stall_h = 0, t_issue = 0, t_first = 0, t_post = 0, t_end = 0;
     uint32_t slices = 0;
     if (tracing) t_first = clock64();
+    if (p.trace != nullptr && lane == 0 && blockIdx.x < kTraceSlots)
+      p.trace[24 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::globaltimer_ns());
 #endif
     for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
       const int unit_stages = p.CB * stages_per_cb;
@@ -159,6 +166,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       for (int stg = 0; stg < unit_stages; ++stg) {
 #if defined(I8C_PIPELINE_TRACE)
         const long long th = tracing ? clock64() : 0;
+        if (tracing && t_end != 0) t_post += th - t_end;
 #endif
         if (sc == 0 && !wwait(&h_full[hst], hph)) {  // first stage of a channel block: its halo
           ok = false;
@@ -169,8 +177,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 #endif
         if (kk == next_chunk) {
           if (kk != 0) {
-            if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
-            __syncwarp();
+            issue([&] { ptx::mma_commit(&acc_full[buf]); });
 #if defined(I8C_PIPELINE_TRACE)
             if (tracing && lane == 0) trace_mark(p, 0, 2, u);
 #endif
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           // 2^18 bytes)
           const uint64_t hd_base = h_desc0 | static_cast<uint64_t>((h_stage + static_cast<uint32_t>(toff)) & 0x3FFFu);
           const uint64_t fd_base = f_desc0 | static_cast<uint64_t>(f_cur & 0x3FFFu);
-          if (ptx::elect_one()) {
+          issue([&] {
 #pragma unroll
             for (int t = 0; t < GT; ++t) {
               const uint64_t hd = hd_base + static_cast<uint64_t>(tapoff[t]);
@@ -221,8 +228,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
               ptx::mma_f16_ss(d_tmem, fd + 2, hd + chunk2_lo, idesc, 1u);
             }
             ptx::mma_commit(&b_empty[st]);
-          }
-          __syncwarp();
+          });
           acc_flag = 1;
           toff += stage_rowstep;
         }
@@ -231,11 +237,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           const uint64_t fd = f_desc0 | static_cast<uint64_t>(f_cur & 0x3FFFu);
           const uint64_t hd0 = h_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
           const uint64_t hd1 = h_desc0 | static_cast<uint64_t>((b_cur + chunk2_lo) & 0x3FFFu);
-          if (ptx::elect_one()) {
+          issue([&] {
             ptx::mma_f16_ss(d_tmem, fd, hd0, idesc, acc_flag);
             ptx::mma_f16_ss(d_tmem, fd + 2, hd1, idesc, 1u);  // filter channels 16-31: 32 bytes on
-          }
-          __syncwarp();
+          });
           acc_flag = 1;
           f_cur += slice_lo;
           // next tap: the next filter column, or the first of the next row
@@ -245,12 +250,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           tcol = row_end ? 0 : tcol;
           toff += row_end ? row_step - p.S * p.dil_w : 0;
         }
-        if constexpr (GT == 0) {
-          if (ptx::elect_one()) ptx::mma_commit(&b_empty[st]);
-          __syncwarp();
-        }
+        if constexpr (GT == 0) issue([&] { ptx::mma_commit(&b_empty[st]); });
 #if defined(I8C_PIPELINE_TRACE)
-        if (tracing) t_issue += clock64() - ti;
+        if (tracing) t_end = clock64();
+        if (tracing) t_issue += t_end - ti;
         slices += G;
 #endif
         st = st + 1 == static_cast<uint32_t>(nbs) ? 0u : st + 1;
@@ -260,21 +263,21 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           sc = 0;
           tcol = 0;
           toff = 0;
-          if (ptx::elect_one()) ptx::mma_commit(&h_empty[hst]);
-          __syncwarp();
+          issue([&] { ptx::mma_commit(&h_empty[hst]); });
           hst = hst + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hst + 1;
           hph ^= hst == 0 ? 1u : 0u;
         }
       }
       if (!ok) break;
-      if (ptx::elect_one()) ptx::mma_commit(&acc_full[buf]);
-      __syncwarp();
+      issue([&] { ptx::mma_commit(&acc_full[buf]); });
 #if defined(I8C_PIPELINE_TRACE)
       if (tracing && lane == 0) trace_mark(p, 0, 2, u);
 #endif
       ++u;
     }
 #if defined(I8C_PIPELINE_TRACE)
+    if (p.trace != nullptr && lane == 0 && blockIdx.x < kTraceSlots)
+      p.trace[25 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::globaltimer_ns());
     if (tracing && lane == 0) {
       p.trace[0] = t_first;
       p.trace[1] = clock64();
@@ -283,12 +286,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       p.trace[4 * kTraceSlots + 2] = stall_b;
       p.trace[4 * kTraceSlots + 3] = stall_h;
       p.trace[4 * kTraceSlots + 7] = t_issue;
+      p.trace[4 * kTraceSlots + 8] = t_post;
     }
 #endif
     if (!ok && lane == 0) raise_timeout(p, abort_flag);
     // every MMA issued by this warp has completed before TMEM is freed
-    if (ptx::elect_one()) ptx::mma_commit(drain);
-    __syncwarp();
+    issue([&] { ptx::mma_commit(drain); });
     if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
