@@ -298,7 +298,8 @@ def run_ours(args, wl, rank, world):
     plan_h.destroy()
 
     peak, peak_note = tensor_peak()
-    kernel_name = {1: "conv_fprop_tc_kernel", 4: "conv_fprop_tr_kernel"}.get(plan.info["kernel_variant"],
+    kernel_name = {1: "conv_fprop_tc_kernel", 4: "conv_fprop_tr_kernel", 5: "conv_fprop_tr_kernel"}.get(
+        plan.info["kernel_variant"],
                                                                            "conv_fprop_halo_kernel")
     kern_avg_ms = kern_ms / max(1, kern_n)
     achieved = ops / (kern_avg_ms * 1e-3) / 1e12

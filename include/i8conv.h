@@ -82,7 +82,9 @@ typedef struct {
                                 M = 256 MMA per K-step; block_n 64, 128 or 256), 4 = transposed
                                 tiles (128 output channels x tile_px output pixels per tile, the
                                 MMA's M on the channels; stride 1 only, else
-                                I8C_ERR_UNSUPPORTED)                                         */
+                                I8C_ERR_UNSUPPORTED), 5 = transposed tiles on CTA pairs (256
+                                output channels, 128 per CTA, x tile_px pixels, each CTA
+                                building the halo of half of them; stride 1 only)            */
   int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
                                 (currently the same as 2), 1 = int8 staging ring filled by
                                 cp.async ahead of use, 2 = straight into registers (no
@@ -105,9 +107,10 @@ typedef struct {
                                 convolution's prologue overlaps its tail), 1 = inside the
                                 convolution kernel (one launch per run; cooperative launch,
                                 all CTAs resident; measured slower)                         */
-  int32_t tile_px;           /* transposed tiles: output pixels per tile, 0 = auto (the width
-                                whose tile count fills the SMs' waves best), else a multiple
-                                of 16 from 16 to 256                                          */
+  int32_t tile_px;           /* transposed tiles: output pixels per tile (the MMA's N; on
+                                pairs split between the two CTAs), 0 = auto (the width whose
+                                tile count fills the SMs' waves best), else a multiple of 16
+                                from 16 to 256                                                */
   int32_t filter_run;        /* transposed tiles: K-slices (taps of one channel block) per
                                 filter stage, 0 = auto (the longest that leaves two stages),
                                 else a divisor of R*S; I8C_ERR_UNSUPPORTED if it does not fit */
@@ -141,7 +144,8 @@ typedef struct {
   int32_t kernel_variant;    /* 1 = per-tap gather kernel, 2 = halo kernel,
                                 3 = halo kernel on CTA pairs, 4 = transposed
                                 tiles (block_m = tile_px pixels, block_n = 128
-                                output channels)                               */
+                                output channels), 5 = transposed tiles on CTA
+                                pairs (block_n = 256)                          */
   int32_t halo_staging;      /* halo kernel: int8 staging slots (0 = loads
                                 straight into registers); 0 for the gather kernel */
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of

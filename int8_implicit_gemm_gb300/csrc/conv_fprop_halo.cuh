@@ -363,44 +363,51 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
   return true;
 }
 
-// Producer for halos of at most kSplitStep * kB positions (one batch of
-// 16-byte loads per thread and channel block), in two groups of 96
-// threads that take alternate channel blocks: warps 1-3 the even ones, 5-7
-// the odd ones.  A group issues a channel block's loads as soon as it has
-// stored its previous one, two channel blocks earlier, so each load round
-// trip (a DRAM miss for the first touch of an input row) has the MMAs of two
-// channel blocks to complete in, with one batch of registers per thread
-// (kB loads: the kernel's register split for the producer warps decides it).
-// Returns false when a wait timed out.
-constexpr int kSplitStep = kProducers / 4;  // positions between a thread's loads: 96 threads, two per position
+// Producer for halos of at most (kProducers / ng / 2) * kB positions (one
+// batch of 16-byte loads per thread and channel block), in ng groups of
+// kProducers / ng threads (whole warps) that take channel blocks in turn:
+// group g the blocks i with i % ng == g.  A group issues a channel block's
+// loads as soon as it has stored its previous one, ng channel blocks
+// earlier, so each load round trip (a DRAM miss for the first touch of an
+// input row) has the MMAs of ng channel blocks to complete in, with one
+// batch of registers per thread (kB loads: the kernel's register split for
+// the producer warps decides it).  Three groups when the halo fits and there
+// are three halo stages (one each), else two.  Returns false when a wait
+// timed out.
 template <int kB>
-__device__ __forceinline__ bool halo_split_producers(const HaloParams& hp) {
-  return hp.nstg == 0 && hp.positions <= kSplitStep * kB;
+__device__ __forceinline__ int halo_groups(const HaloParams& hp) {
+  if (hp.nstg != 0) return 0;
+  if (hp.nhs >= 3 && hp.positions <= (kProducers / 6) * kB) return 3;
+  if (hp.positions <= (kProducers / 4) * kB) return 2;
+  return 0;
 }
 // Producer arrivals that complete a halo stage (per CTA).
 template <int kB>
 __device__ __forceinline__ uint32_t halo_arrivals(const HaloParams& hp) {
-  return halo_split_producers<kB>(hp) ? kProducers / 2 : kProducers;
+  const int ng = halo_groups<kB>(hp);
+  return ng > 0 ? kProducers / ng : kProducers;
 }
 
 template <int kB>
 __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                   uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
-                                                  int pt) {
+                                                  int pt, int ng) {
   const ConvParams& p = hp.c;
-  const uint32_t grp = pt >= kProducers / 2 ? 1u : 0u;
-  const int lt = pt - static_cast<int>(grp) * (kProducers / 2);
+  const int gsize = kProducers / ng;  // threads per group: 96 or 64 (whole warps)
+  const uint32_t grp = static_cast<uint32_t>(pt / gsize);
+  const int lt = pt - static_cast<int>(grp) * gsize;
+  const int step = gsize / 2;  // positions between a thread's loads, two threads per position
   const int h = lt & 1;
   const int e_first = lt >> 1;
   const int b_first = e_first / hp.CW, pos_first = e_first - b_first * hp.CW;
-  const int b_step = kSplitStep / hp.CW, pos_step = kSplitStep - b_step * hp.CW;
+  const int b_step = step / hp.CW, pos_step = step - b_step * hp.CW;
   const int positions = hp.positions;
   const int HW32 = p.H * p.W * 32;
   const uint32_t nhs = static_cast<uint32_t>(hp.nhs);
   bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
-  uint32_t i = 0;  // channel blocks of this CTA so far, both groups'
-  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++i) {
-    if ((i & 1u) != grp) continue;
+  uint32_t i = 0, gi = 0;  // channel blocks of this CTA so far (all groups'); i % ng
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++i, gi = gi + 1 == static_cast<uint32_t>(ng) ? 0u : gi + 1) {
+    if (gi != grp) continue;
     const PatchTile t = decode_patch(it.tile, hp, ts);
     const int hb0 = t.p0 * p.stride_h - p.pad_h;
     const int wb0 = t.q0 * p.stride_w - p.pad_w;
@@ -415,7 +422,7 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
         const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
         if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
           v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
-        e += kSplitStep;
+        e += step;
         b += b_step;
         pos += pos_step;
         if (pos >= hp.CW) {
@@ -432,7 +439,7 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
     uint8_t* halo = smem + hs * hp.halo_bytes;
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
-      const int ek = e_first + k * kSplitStep;
+      const int ek = e_first + k * step;
       if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
     }
     ptx::fence_proxy_async_smem();
@@ -442,15 +449,16 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
   return true;
 }
 
-// Which register producer a halo takes: two alternating groups when a channel
-// block is one batch of kB loads per thread, else all producers on every
-// channel block.
-constexpr int kHaloSplitBatch = 5;  // the halo kernel's producers: the most that fits 72 registers
+// Which register producer a halo takes: groups taking channel blocks in turn
+// when a channel block is one batch of kB loads per thread, else all
+// producers on every channel block.
+constexpr int kHaloSplitBatch = 4;  // the halo kernel's producers: the most that fits 72 registers
 template <int kB>
 __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                       uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                       int pt) {
-  if (halo_split_producers<kB>(hp)) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+  const int ng = halo_groups<kB>(hp);
+  if (ng > 0) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt, ng);
   return halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
 }
 

@@ -19,6 +19,12 @@
 // count is free, so the plan can pick the width whose tile count fills the
 // SMs' waves best.
 //
+// CTA pairs (CG = 2, clusters of two): M = 256 MMAs whose rows are 128
+// output channels from each CTA's own filter stage and whose N pixel columns
+// are split in halves, each CTA building the halo of its half -- half the
+// halo production per tensor-core cycle of a single CTA.  Rank 0 issues; both
+// drain their own 128 channels over all N columns.
+//
 // Warp roles (512 threads) as in the halo kernel: warp 0 MMA issuer and TMEM
 // owner, warp 4 filter TMA, warps 1-3 and 5-7 halo producers, warps 8-15
 // epilogue.  TMEM lane i of the accumulator is output channel 128*kt + i, so
@@ -34,10 +40,10 @@ namespace i8c {
 constexpr int kTrRows = 128;   // output channels per tile: the MMA's M
 constexpr int kTrMaxPx = 256;  // output pixels per tile: the MMA's N, at most
 
-// Register split by the widest tile an instantiation serves: MAXPX = 192
+// Register split by the widest MMA N an instantiation serves: MAXPX = 192
 // leaves an epilogue thread 96 running sums, so its warps need fewer
 // registers and the producer warps get enough for batches of eight loads;
-// MAXPX = 256 keeps the halo kernel's split and batches of five.
+// MAXPX = 256 keeps the halo kernel's split and batches of four.
 template <int MAXPX>
 struct TrRegs {
   static constexpr uint32_t kWorker = MAXPX <= 192 ? 104 : kWorkerRegs;
@@ -49,10 +55,12 @@ struct TrRegs {
 // GT > 0: filter stages of GT K-slices that are whole filter rows (S divides
 // GT), their taps' halo offsets precomputed and all their MMAs issued by one
 // elected lane in one block; GT == 0: any stage length, taps advanced slice
-// by slice.  MAXPX: the widest tile (tile_px) the instantiation serves.
-template <int GT, int MAXPX>
+// by slice.  MAXPX: the widest MMA N (CG * tile_px) the instantiation
+// serves.  CG: CTAs per MMA tile (1, or 2 for pairs).
+template <int GT, int MAXPX, int CG>
 __global__ void __launch_bounds__(kHaloThreads, 1)
     conv_fprop_tr_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+  static_assert(CG == 1 || CG == 2, "CTA group");
   using Regs = TrRegs<MAXPX>;
   constexpr int kMaxGroupsPerWarp = MAXPX / 16;  // 8-column groups of one epilogue warp
   const ConvParams& p = hp.c;
@@ -72,7 +80,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
   const int nbs = hp.nbs;
-  const int NP = hp.tile_px;
+  const int NP = CG * hp.tile_px;  // the MMA's N: pixels per tile over the CTA group
   const int RS = p.R * p.S;
   const int G = GT > 0 ? GT : hp.bgroup;  // K-slices (taps of one channel block) per filter stage
 #if defined(I8C_PIPELINE_TRACE)
@@ -87,12 +95,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&b_empty[i], 1);
     }
     for (int i = 0; i < hp.nhs; ++i) {
-      ptx::mbar_init(&h_full[i], halo_arrivals<Regs::kBatch>(hp));
+      ptx::mbar_init(&h_full[i], halo_arrivals<Regs::kBatch>(hp) * CG);  // rank 0 counts both CTAs'
       ptx::mbar_init(&h_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&acc_full[i], 1);
-      ptx::mbar_init(&acc_empty[i], kEpilogue);
+      ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -100,21 +108,23 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   }
   if (warp == kTmaWarp && lane == 0) ptx::prefetch_tensormap(&tmap_f);
   if (warp == 0) {
-    ptx::tmem_alloc(tmem_slot, p.tmem_cols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_cg<CG>(tmem_slot, p.tmem_cols);
+    ptx::tmem_relinquish_cg<CG>();
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     ptx::setmaxnreg_dec<Regs::kWorker>();
-    const TileSched ts = tile_sched<1>();
+    const TileSched ts = tile_sched<CG>();
+    if (CG == 1 || ts.rank == 0) {
     // The whole warp runs the loop in uniform control flow; one elected lane
     // issues each MMA and commit (measured no slower than lane 0 alone).
-    const uint32_t idesc = ptx::idesc_f16_f32(kTrRows, NP);
+    const uint32_t idesc = ptx::idesc_f16_f32(kTrRows * CG, NP);
     const uint64_t f_desc0 = ptx::smem_desc_sw64_kmajor(0);
     // the halo as B: 8-pixel groups 128 bytes apart, 8-channel planes plane_bytes apart
     const uint64_t h_desc0 = ptx::smem_desc_noswizzle_kmajor(0, hp.plane_bytes, 128);
@@ -139,13 +149,23 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const int stage_rowstep = GT > 0 ? (GT / p.S) * row_step : 0;
     uint32_t u = 0, hst = 0, hph = 0, st = 0, bph = 0;
     bool ok = true;
+    // barriers with arrivals from the peer CTA: cluster-scope acquire
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, p.timeout_ns, abort_flag));
+      return __all_sync(0xffffffffu, ptx::mbar_wait<CG == 2>(bar, parity, p.timeout_ns, abort_flag));
     };
     // one elected lane's tcgen05 issue (MMAs or a commit)
     auto issue = [&](auto&& f) {
       if (ptx::elect_one()) f();
       __syncwarp();
+    };
+    // a pair's MMAs and commits: both CTAs' accumulators and barriers
+    auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+      if constexpr (CG == 2) ptx::mma_f16_ss_pair(d, a, b, idesc, accumulate);
+      else ptx::mma_f16_ss(d, a, b, idesc, accumulate);
+    };
+    auto commit = [&](uint64_t* bar) {
+      if constexpr (CG == 2) ptx::mma_commit_pair(bar, 3);
+      else ptx::mma_commit(bar);
     };
 #if defined(I8C_PIPELINE_TRACE)
     // CTA 0: cycles spent in each kind of wait and in the MMA issue blocks
@@ -177,7 +197,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 #endif
         if (kk == next_chunk) {
           if (kk != 0) {
-            issue([&] { ptx::mma_commit(&acc_full[buf]); });
+            issue([&] { commit(&acc_full[buf]); });
 #if defined(I8C_PIPELINE_TRACE)
             if (tracing && lane == 0) trace_mark(p, 0, 2, u);
 #endif
@@ -224,10 +244,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             for (int t = 0; t < GT; ++t) {
               const uint64_t hd = hd_base + static_cast<uint64_t>(tapoff[t]);
               const uint64_t fd = fd_base + static_cast<uint64_t>(t * slice_lo);
-              ptx::mma_f16_ss(d_tmem, fd, hd, idesc, t == 0 ? acc_flag : 1u);
-              ptx::mma_f16_ss(d_tmem, fd + 2, hd + chunk2_lo, idesc, 1u);
+              mma(d_tmem, fd, hd, t == 0 ? acc_flag : 1u);
+              mma(d_tmem, fd + 2, hd + chunk2_lo, 1u);
             }
-            ptx::mma_commit(&b_empty[st]);
+            commit(&b_empty[st]);
           });
           acc_flag = 1;
           toff += stage_rowstep;
@@ -238,8 +258,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           const uint64_t hd0 = h_desc0 | static_cast<uint64_t>(b_cur & 0x3FFFu);
           const uint64_t hd1 = h_desc0 | static_cast<uint64_t>((b_cur + chunk2_lo) & 0x3FFFu);
           issue([&] {
-            ptx::mma_f16_ss(d_tmem, fd, hd0, idesc, acc_flag);
-            ptx::mma_f16_ss(d_tmem, fd + 2, hd1, idesc, 1u);  // filter channels 16-31: 32 bytes on
+            mma(d_tmem, fd, hd0, acc_flag);
+            mma(d_tmem, fd + 2, hd1, 1u);  // filter channels 16-31: 32 bytes on
           });
           acc_flag = 1;
           f_cur += slice_lo;
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           tcol = row_end ? 0 : tcol;
           toff += row_end ? row_step - p.S * p.dil_w : 0;
         }
-        if constexpr (GT == 0) issue([&] { ptx::mma_commit(&b_empty[st]); });
+        if constexpr (GT == 0) issue([&] { commit(&b_empty[st]); });
 #if defined(I8C_PIPELINE_TRACE)
         if (tracing) t_end = clock64();
         if (tracing) t_issue += t_end - ti;
@@ -263,13 +283,13 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           sc = 0;
           tcol = 0;
           toff = 0;
-          issue([&] { ptx::mma_commit(&h_empty[hst]); });
+          issue([&] { commit(&h_empty[hst]); });
           hst = hst + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hst + 1;
           hph ^= hst == 0 ? 1u : 0u;
         }
       }
       if (!ok) break;
-      issue([&] { ptx::mma_commit(&acc_full[buf]); });
+      issue([&] { commit(&acc_full[buf]); });
 #if defined(I8C_PIPELINE_TRACE)
       if (tracing && lane == 0) trace_mark(p, 0, 2, u);
 #endif
@@ -290,30 +310,45 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     }
 #endif
     if (!ok && lane == 0) raise_timeout(p, abort_flag);
-    // every MMA issued by this warp has completed before TMEM is freed
-    issue([&] { ptx::mma_commit(drain); });
+    // every MMA issued by this warp has completed before TMEM is freed (a
+    // pair's rank 1 learns it through the final cluster barrier)
+    issue([&] {
+      if constexpr (CG == 2) ptx::mma_commit_pair(drain, 1);
+      else ptx::mma_commit(drain);
+    });
     if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
+    }  // rank 0
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
     ptx::setmaxnreg_dec<Regs::kWorker>();
     // the fp16 filter is written by the conversion kernel launched just
     // before this one, which this kernel may overlap (dependent launch)
     ptx::griddep_wait();
-    const TileSched ts = tile_sched<1>();
+    const TileSched ts = tile_sched<CG>();
     const uint32_t stage_bytes = static_cast<uint32_t>(G * kTrRows * 64);
     uint32_t g = 0, st = 0, bph = 0;
     bool ok = true;
     for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
-      const int k0 = (unit % p.num_n_tiles) * kTrRows;  // first output channel of the tile
+      // first output channel of this CTA's 128 rows of the tile
+      const int k0 = (unit % p.num_n_tiles) * (kTrRows * CG) + ts.rank * kTrRows;
       for (int kk = 0; kk < p.CB * RS; kk += G, ++g) {
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&b_empty[st], bph ^ 1u, p.timeout_ns, abort_flag))) {
           ok = false;
           break;
         }
-        // G consecutive K-slices of 128 output channels; channels past K read as zeros
+        // G consecutive K-slices of 128 output channels; channels past K read as
+        // zeros.  A pair's two stages both complete on rank 0's barrier.
         if (ptx::elect_one()) {
-          ptx::mbar_arrive_expect_tx(&b_full[st], stage_bytes);
-          ptx::tma_load_3d(smem + hp.off_b + st * stage_bytes, &tmap_f, &b_full[st], 0, k0, kk);
+          uint8_t* dst = smem + hp.off_b + st * stage_bytes;
+          if constexpr (CG == 1) {
+            ptx::mbar_arrive_expect_tx(&b_full[st], stage_bytes);
+            ptx::tma_load_3d(dst, &tmap_f, &b_full[st], 0, k0, kk);
+          } else if (ts.rank == 0) {
+            ptx::mbar_arrive_expect_tx(&b_full[st], 2 * stage_bytes);
+            ptx::tma_load_3d_pair(dst, &tmap_f, ptx::smem_addr(&b_full[st]), 0, k0, kk);
+          } else {
+            ptx::tma_load_3d_pair(dst, &tmap_f, ptx::mapa(ptx::smem_addr(&b_full[st]), 0), 0, k0, kk);
+          }
         }
         __syncwarp();
         if (++st == static_cast<uint32_t>(nbs)) {
@@ -323,10 +358,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       }
     }
     if (!ok && lane == 0) raise_timeout(p, abort_flag);
-    // wait for the loads still in flight (at most one per stage)
+    // wait for the loads still in flight (at most one per stage); rank 0 of a
+    // pair waits for both CTAs' stages, which rank 1 cannot observe
     const uint32_t first = g > static_cast<uint32_t>(nbs) ? g - nbs : 0u;
-    for (uint32_t i = first; i < g; ++i) {
-      if (!ptx::mbar_wait(&b_full[i % nbs], (i / nbs) & 1u, p.timeout_ns, nullptr)) {
+    for (uint32_t i = (CG == 2 && ts.rank != 0) ? g : first; i < g; ++i) {
+      if (!ptx::mbar_wait<CG == 2>(&b_full[i % nbs], (i / nbs) & 1u, p.timeout_ns, nullptr)) {
         if (lane == 0) raise_timeout(p, abort_flag);
         break;
       }
@@ -339,7 +375,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // producers as the halo kernel's flat tiles, with tile_px pixels per tile.
     ptx::setmaxnreg_dec<Regs::kWorker>();
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
-    const TileSched ts = tile_sched<1>();
+    const TileSched ts = tile_sched<CG>();
     const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
                                 : halo_produce_registers<Regs::kBatch>(hp, ts, smem, h_full, h_empty, abort_flag,
                                                                        pt);
@@ -347,9 +383,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp 8 + 4*eh + qd reads TMEM lanes 32*qd .. 32*qd + 31 (output
-    // channel block 4*kt + qd of the tile) and column half eh; its lane l
-    // keeps the int32 running sums of channel 32*qd + l over that half's
-    // pixels in registers.
+    // channel block 4*(CG*kt + rank) + qd of the tile) and column half eh;
+    // its lane l keeps the int32 running sums of channel 32*qd + l over that
+    // half's pixels in registers.  In a pair the column halves are the two
+    // CTAs' pixel halves, i.e. two flat tiles of tile_px pixels.
     ptx::setmaxnreg_inc<Regs::kEpi>();
     const int qd = warp & 3;
     const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
@@ -360,7 +397,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     uint32_t run[kMaxGroupsPerWarp * 8];
     uint32_t u = 0;
     bool ok = true;
-    for (int unit = tile_sched<1>().first; ok && unit < hp.num_units; unit += tile_sched<1>().step) {
+    for (int unit = tile_sched<CG>().first; ok && unit < hp.num_units; unit += tile_sched<CG>().step) {
       for (int c = 0; c < nch; ++c, ++u) {
         const uint32_t buf = u & 1u;
 #if defined(I8C_PIPELINE_TRACE)
@@ -397,9 +434,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             }
           }
         }
-        // the accumulator buffer is free once read
+        // the accumulator buffer is free once read (a pair's rank 0 waits for both CTAs)
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&acc_empty[buf]);
+        arrive_on_leader(&acc_empty[buf], tile_sched<CG>());
 #if defined(I8C_PIPELINE_TRACE)
         if (warp == 8 && lane == 0) trace_mark(p, 3, 2, u);
         if (warp == 15 && lane == 0) trace_mark(p, 3, 3, u);
@@ -409,9 +446,13 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       // Store: column j is the pixel at flat position m0 + j of the padded
       // row-major output, and this warp holds its 32 channels of output
       // block cbk -- one contiguous 32-byte NCxHWx<32> vector per pixel.
-      const PatchTile t = decode_patch(unit, hp, tile_sched<1>());
-      const int cbk = t.nt * 4 + qd;
-      if (cbk >= p.KB) continue;
+      const TileSched ts = tile_sched<CG>();
+      // the flat tile of these columns: in a pair, column half eh is the
+      // pixel half (tile) of CTA eh; a single CTA's halves split one tile
+      const PatchTile t = decode_patch(unit, hp, TileSched{ts.first, ts.step, CG == 2 ? eh : 0, CG});
+      const int coff = CG == 2 ? 0 : c0;  // this warp's first column within its flat tile
+      const int cbk = t.nt * (4 * CG) + ts.rank * 4 + qd;
+      if (!t.valid || cbk >= p.KB) continue;
       const int64_t plane = (static_cast<int64_t>(t.n) * p.KB + cbk) * p.P;
       const int ncols = gh * 8;
       if (p.out_mode == 0) {
@@ -431,7 +472,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         __syncwarp();
         for (int e = lane; e < 2 * ncols; e += 32) {
           const int col = e >> 1;
-          const int m = t.m0 + c0 + col;
+          const int m = t.m0 + coff + col;
           const int pp = m / hp.CW;
           const int qq = m - pp * hp.CW;
           if (pp < p.P && qq < p.Q) {
@@ -443,7 +484,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       } else {
         // int32 accumulators (parity checks): one coalesced 128-byte warp
         // store per pixel
-        const int m = t.m0 + c0;
+        const int m = t.m0 + coff;
         int pp = m / hp.CW;
         int qq = m - pp * hp.CW;
 #pragma unroll
@@ -465,13 +506,17 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // A pair's CTAs leave together: no remote arrive, multicast commit or MMA
+  // operand read targets a CTA that has exited, and both free their tensor
+  // memory together.
+  if (CG == 2) ptx::cluster_sync();
 #if defined(I8C_PIPELINE_TRACE)
   if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < kTraceSlots)
     p.trace[9 * kTraceSlots + blockIdx.x] = static_cast<long long>(ptx::globaltimer_ns());
 #endif
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, p.tmem_cols);
+    ptx::tmem_dealloc_cg<CG>(tmem_base, p.tmem_cols);
   }
 }
 

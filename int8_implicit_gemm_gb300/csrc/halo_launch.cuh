@@ -32,9 +32,10 @@ cudaError_t halo_prepare_bn() {
 
 // CTA pairs are launched as clusters of two.  Single CTAs that convert the
 // filter themselves are launched cooperatively (all CTAs resident: their grid
-// barrier cannot wait on a CTA that has not started); otherwise as
-// programmatic dependents of the filter conversion kernel, whose tail their
-// prologue (barriers, tensor memory, halo loads) overlaps.
+// barrier cannot wait on a CTA that has not started).  Otherwise (pairs too)
+// the kernel is a programmatic dependent of the filter conversion kernel,
+// whose tail its prologue (barriers, tensor memory, halo loads) overlaps.
+// attr: room for two attributes.
 template <int CG>
 cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t stream, cudaLaunchAttribute* attr,
                                       bool cooperative = false) {
@@ -43,27 +44,31 @@ cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t strea
   cfg.blockDim = dim3(kHaloThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
+  unsigned n = 0;
   if (CG == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-  } else if (cooperative) {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-  } else {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
   }
+  if (cooperative) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+  } else {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+  }
+  ++n;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cfg;
 }
 
 template <int BN, int CG>
 cudaError_t halo_launch_bn(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
                            cudaStream_t stream) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr, p.f_int8 != nullptr);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -73,7 +78,7 @@ cudaError_t halo_launch_bn(const CUtensorMap& tmap, const HaloParams& p, int sme
 // Clusters of two that can be resident at once (0 if the query fails).
 template <int BN>
 int halo_max_clusters_bn(int bgroup, int S, int smem) {
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = halo_launch_config<2>(smem, 2, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(halo_kernel_for<BN, 2>(bgroup, S)), &cfg) !=

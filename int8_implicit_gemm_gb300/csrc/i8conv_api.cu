@@ -205,18 +205,20 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
   return false;
 }
 
-// Layout of the transposed-tile kernel for np output pixels per tile
-// (stride 1 only): the flat halo of np + (R-1)*dh*CW + (S-1)*dw padded input
-// positions per channel block, two or three halo stages and at least two
-// filter stages of G K-slices x 128 output channels, and the epilogue's
-// output staging rows (np pixels x 128 channels, int8).  G is want_g if given,
+// Layout of the transposed-tile kernel for np output pixels per CTA and cg
+// CTAs per MMA tile (stride 1 only): the flat halo of np + (R-1)*dh*CW +
+// (S-1)*dw padded input positions per channel block, two or three halo
+// stages and at least two filter stages of G K-slices x 128 output channels,
+// and the epilogue's output staging rows (the MMA's cg * np pixels x 128
+// channels, int8).  G is want_g if given,
 // else the longest divisor of R*S that fits.  nstg > 0: an int8 staging ring
 // of nstg slots that cp.async fills nstg - 1 channel blocks ahead.  Returns
 // false when nothing fits.
-bool tr_layout(const i8c_conv_shape& s, int P, int np, int want_g, int nstg, i8c::HaloParams* h,
+bool tr_layout(const i8c_conv_shape& s, int P, int np, int cg, int want_g, int nstg, i8c::HaloParams* h,
                int* smem_bytes) {
   if (s.stride_h != 1 || s.stride_w != 1) return false;
-  if (np < 16 || np > 256 || np % 16 != 0) return false;
+  const int mma_n = cg * np;
+  if (mma_n < 16 || mma_n > 256 || mma_n % 16 != 0 || np % 8 != 0) return false;
   *h = i8c::HaloParams{};
   h->flat = 1;
   h->tile_px = np;
@@ -238,7 +240,7 @@ bool tr_layout(const i8c_conv_shape& s, int P, int np, int want_g, int nstg, i8c
   const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
   const int RS = s.R * s.S;
   const int64_t stage_unit = 128 * 64;  // one K-slice of 128 output channels, fp16
-  const int64_t out_bytes = static_cast<int64_t>(np) * 128;
+  const int64_t out_bytes = static_cast<int64_t>(mma_n) * 128;
   for (int G = RS < 32 ? RS : 32; G >= 1; --G) {
     if (RS % G != 0 || (want_g != 0 && G != want_g)) continue;
     const int64_t stage = G * stage_unit;
@@ -346,7 +348,8 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
       hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
       hp.gbar = pl->gbar;
     }
-    e = pl->kernel_variant == 4   ? i8c::tr_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+    e = pl->kernel_variant == 5   ? i8c::tr_launch_pair(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 4 ? i8c::tr_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
         : pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
                                                           stream)
                                   : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
@@ -434,7 +437,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
     return I8C_ERR_INVALID_ARG;
   if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 4 ||
+      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 5 ||
       o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 ||
       o.tile_shape > 2 || o.fused_filter < 0 || o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
       (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)))
@@ -467,43 +470,63 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   int bn = 0, halo_smem = 0, groups = 0;
   p->kernel_variant = 1;
   p->cta_group = 1;
-  // Transposed tiles: the pixel count per tile whose tile count fills the
-  // waves best.  Model (measured on the 3x3 layers): a K-slice of a tile
-  // costs its width in tensor-core cycles plus about 130 cycles of issue,
-  // wait and halo overhead, and a launch takes as many tile times as its
-  // fullest SM runs tiles.  Returns the width (0: nothing fits) and its cost
-  // in cycles per K-slice of the launch.
+  // Transposed tiles on cg CTAs per MMA tile: the MMA width (pixels per
+  // tile, cg halves of tile_px each) whose tile count fills the waves best.
+  // Model (measured on the 3x3 layers): a K-slice of a tile costs its width
+  // in tensor-core cycles plus a fixed issue, wait and halo overhead, and a
+  // launch takes as many tile times as its fullest SM (pair) runs tiles.
+  // Returns the width (0: nothing fits), its cost in cycles per K-slice of
+  // the launch and the concurrent CTA groups.
   const int tr_stg = o.halo_loads == 1 ? 3 : 0;  // staging ring on request
-  auto pick_tr = [&](double* cost_out) -> int {
-    const int n_tiles = (s.K + 127) / 128;
+  auto pick_tr = [&](int cg, double* cost_out, int* groups_out) -> int {
+    const int n_tiles = (s.K + 128 * cg - 1) / (128 * cg);
+    // a pair's MMA queue hides more of the per-stage waits, but both CTAs'
+    // producers gate every channel block (measured: 2 x 144 K-slices of 240
+    // pixels on the 64x512x28x28 layer at ~310 cycles each)
+    const double overhead = cg == 2 ? 80.0 : 130.0;
     double best = 0.0;
-    int best_np = 0;
-    for (int np = 256; np >= 16; np -= 16) {
-      if (o.tile_px != 0 && np != o.tile_px) continue;
+    int best_n = 0;
+    for (int n = 256; n >= 16; n -= 16) {
+      if (o.tile_px != 0 && n != o.tile_px) continue;
       i8c::HaloParams h;
       int sm = 0;
-      if (!tr_layout(s, p->P, np, o.filter_run, tr_stg, &h, &sm)) continue;
-      const int64_t t = static_cast<int64_t>(h.num_patches) * n_tiles;
-      const int64_t waves = (t + ctas - 1) / ctas;
-      const double cost = static_cast<double>(waves) * (np + 130.0);
-      if (best_np == 0 || cost < best * 0.999) {
+      if (!tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &h, &sm)) continue;
+      // A pair's CTA builds the halo of n / 2 pixels plus the filter's overhang
+      // for every channel block; when the overhang outweighs the pixels the
+      // producers, not the tensor core, set the pace (8x256x56x56 layer: 88
+      // pixels + 118 positions, 34.5 us on pairs against 31.3 us on single CTAs).
+      if (cg == 2 && o.kernel_variant != 5 && h.positions > 1.6 * (n / 2)) continue;
+      int g = ctas / cg;
+      if (cg == 2) {
+        if (i8c::tr_prepare_pair() != cudaSuccess) continue;
+        const int fit = i8c::tr_pair_max_clusters(h.bgroup, s.S, n, sm);
+        if (fit < 1) continue;
+        if (g > fit) g = fit;
+      }
+      const int64_t t = (static_cast<int64_t>(h.num_patches) + cg - 1) / cg * n_tiles;
+      const int64_t waves = (t + g - 1) / g;
+      const double cost = static_cast<double>(waves) * (n + overhead);
+      if (best_n == 0 || cost < best * 0.999) {
         best = cost;
-        best_np = np;
+        best_n = n;
+        *groups_out = g;
       }
     }
     *cost_out = best;
-    return best_np;
+    return best_n;
   };
-  if (o.kernel_variant == 4) {
+  if (o.kernel_variant == 4 || o.kernel_variant == 5) {
+    const int cg = o.kernel_variant == 5 ? 2 : 1;
     double cost = 0.0;
-    const int np = pick_tr(&cost);
-    if (np == 0) {
+    const int n = pick_tr(cg, &cost, &groups);
+    if (n == 0) {
       delete p;
       return I8C_ERR_UNSUPPORTED;
     }
-    tr_layout(s, p->P, np, o.filter_run, tr_stg, &p->halo, &halo_smem);
-    p->kernel_variant = 4;
-    bn = 128;
+    tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &p->halo, &halo_smem);
+    p->kernel_variant = o.kernel_variant;
+    p->cta_group = cg;
+    bn = 128 * cg;
   } else if (o.kernel_variant != 1) {
     // best tile width on cg CTAs per tile: {width, groups} (width 0: none fits)
     // best {width, groups, flat} on cg CTAs per tile (width 0: none fits);
@@ -582,12 +605,20 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (halo_layout(s, p->P, p->Q, 256, 1, 0, best.flat, &h, &sm)) {
         const int64_t t = static_cast<int64_t>(h.num_patches) * ((s.K + 255) / 256);
         const double halo_cost = static_cast<double>((t + ctas - 1) / ctas) * 345.0;
-        double tr_cost = 0.0;
-        const int np = pick_tr(&tr_cost);
-        if (np != 0 && tr_cost < 0.95 * halo_cost) {
-          tr_layout(s, p->P, np, o.filter_run, tr_stg, &p->halo, &halo_smem);
-          p->kernel_variant = 4;
-          bn = 128;
+        double tr_cost = 0.0, pair_cost = 0.0;
+        int tr_groups = 0, pair_groups = 0;
+        const int n1 = pick_tr(1, &tr_cost, &tr_groups);
+        const int n2 = pick_tr(2, &pair_cost, &pair_groups);
+        const bool pair = n2 != 0 && (n1 == 0 || pair_cost < tr_cost);
+        const double cost = pair ? pair_cost : tr_cost;
+        if ((n1 != 0 || n2 != 0) && cost < 0.97 * halo_cost) {
+          const int cgt = pair ? 2 : 1;
+          const int n = pair ? n2 : n1;
+          tr_layout(s, p->P, n / cgt, cgt, o.filter_run, tr_stg, &p->halo, &halo_smem);
+          p->kernel_variant = pair ? 5 : 4;
+          p->cta_group = cgt;
+          groups = pair ? pair_groups : tr_groups;
+          bn = 128 * cgt;
           use_tr = true;
         }
       }
@@ -622,14 +653,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
   int64_t split_bytes = 0;
-  if (p->kernel_variant == 4) {
+  if (p->kernel_variant >= 4) {
     // one unit per tile, no split tail
     p->halo.ksplit = 1;
     p->halo.nsplit = 1;
     p->halo.full_units = p->num_tiles;
     p->halo.num_units = p->num_tiles;
     p->split_tiles = 0;
-    p->num_ctas = ctas < p->num_tiles ? ctas : p->num_tiles;
+    const int g = p->kernel_variant == 5 ? groups : ctas;
+    p->num_ctas = p->cta_group * (g < p->num_tiles ? g : p->num_tiles);
   } else if (p->kernel_variant >= 2) {
     // The last wave is partial when the tile count is not a multiple of the
     // persistent CTAs (pairs): its tiles are split along the channel blocks
@@ -689,7 +721,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   if (p->kernel_variant >= 2) {
     // halo kernel: two fp32 chunk accumulators; running sums live in registers
     p->acc_buffers = 2;
-    p->tmem_cols = static_cast<uint32_t>(next_pow2(2 * (p->kernel_variant == 4 ? p->halo.tile_px : bn)));
+    p->tmem_cols = static_cast<uint32_t>(
+        next_pow2(2 * (p->kernel_variant >= 4 ? p->cta_group * p->halo.tile_px : bn)));
   } else {
     const int run_cols = p->num_chunks > 1 ? bn : 0;
     p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
@@ -702,7 +735,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
   p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
 
-  e = p->kernel_variant == 4   ? i8c::tr_prepare()
+  e = p->kernel_variant == 5   ? i8c::tr_prepare_pair()
+      : p->kernel_variant == 4 ? i8c::tr_prepare()
       : p->kernel_variant == 3 ? i8c::halo_prepare_pair(bn)
       : p->kernel_variant == 2 ? i8c::halo_prepare_single(bn)
                                : i8c::conv_prepare(bn);
@@ -791,7 +825,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->M = pl->M;
   info->gemm_n = s.K;
   info->gemm_k = s.C * s.R * s.S;
-  info->block_m = pl->kernel_variant == 4 ? pl->halo.tile_px : 128 * pl->cta_group;
+  info->block_m = pl->kernel_variant >= 4 ? pl->cta_group * pl->halo.tile_px : 128 * pl->cta_group;
   info->block_n = pl->block_n;
   info->num_tiles = pl->num_tiles;
   info->num_ctas = pl->num_ctas;

@@ -37,6 +37,12 @@ int halo_single_max_ctas(int block_n, int bgroup, int S, int smem_bytes);  // re
 cudaError_t tr_prepare();
 cudaError_t tr_launch(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
                       cudaStream_t stream);
+// tr_kernels_pair.cu: the same on CTA pairs (clusters of two; tile_px is each
+// CTA's half of the MMA's N); max_clusters is the number of pairs that fit
+cudaError_t tr_prepare_pair();
+cudaError_t tr_launch_pair(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+                           cudaStream_t stream);
+int tr_pair_max_clusters(int bgroup, int S, int mma_n, int smem_bytes);
 constexpr int kMaxDynamicSmem = 232448;
 
 // layout_kernels.cu

@@ -99,7 +99,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     """A producer skips one arrival on purpose: the MMA warp's wait runs out
     after 20 ms, every role stops, the kernel returns and the plan reports
     I8C_ERR_TIMEOUT (gather kernel, halo kernel, halo kernel on CTA pairs,
-    transposed tiles).
+    transposed tiles, on single CTAs and on pairs).
     The same context then runs a correct convolution."""
     import int8_implicit_gemm_gb300 as ext
     torch = torch_cuda
@@ -109,7 +109,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     xp, fp = gpu_util.packed_inputs(x, f)
     xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
     y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
-    for kernel in (1, 2, 3, 4):
+    for kernel in (1, 2, 3, 4, 5):
         bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE,
                        kernel_variant=kernel)
         bad.run(xd, fd, y, 1.0)

@@ -116,8 +116,8 @@ def test_deterministic_repeat():
 
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
 @pytest.mark.parametrize("kw", [{}, dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
-                                dict(kernel_variant=3), dict(kernel_variant=4)],
-                         ids=["auto", "staged", "direct", "pair", "transposed"])
+                                dict(kernel_variant=3), dict(kernel_variant=4), dict(kernel_variant=5)],
+                         ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair"])
 def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
     benchmark times (auto), with each halo load form forced and on CTA pairs:
@@ -207,26 +207,31 @@ TRANSPOSED_EXTRA = [
                                 dict(tile_px=64, filter_run=3), dict(tile_px=128, filter_run=1, max_chunk_slices=5),
                                 dict(num_ctas=3, tile_px=96), dict(halo_loads=1), dict(tile_px=240, halo_loads=1)],
                          ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "auto")
-def test_transposed_tiles_exact(shape, kw):
-    """Transposed tiles (128 output channels on the MMA's M, tile_px output
-    pixels on N, stride 1): every output exact for every tile width, filter
-    stage length, chunk length, grid size and load form."""
+@pytest.mark.parametrize("variant", [4, 5], ids=["single", "pair"])
+def test_transposed_tiles_exact(shape, kw, variant):
+    """Transposed tiles (128 output channels per CTA on the MMA's M, tile_px
+    output pixels on N, stride 1; on CTA pairs M = 256 and each CTA builds
+    the halo of half the pixels): every output exact for every tile width,
+    filter stage length, chunk length, grid size and load form."""
     import int8_implicit_gemm_gb300 as ext
+    if variant == 5 and "num_ctas" in kw:
+        kw = dict(kw, num_ctas=2 * kw["num_ctas"])
     try:
-        ext.Plan(shape, kernel_variant=4, **kw).destroy()
+        ext.Plan(shape, kernel_variant=variant, **kw).destroy()
     except ext.I8ConvError as e:
         if e.status == ext.I8C_ERR_UNSUPPORTED and "filter_run" in kw:
             pytest.skip("the forced filter stage length does not divide R*S")
         raise
     x, f = _data(shape, 2024 + sum(shape))
     y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -9)
-    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -9, kernel_variant=4, **kw)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -9, kernel_variant=variant, **kw)
     assert np.array_equal(acc, acc_ref.astype(np.int32))
     assert np.array_equal(y, y_ref)
 
 
-def test_transposed_tiles_rejects_strides():
+@pytest.mark.parametrize("variant", [4, 5])
+def test_transposed_tiles_rejects_strides(variant):
     import int8_implicit_gemm_gb300 as ext
     with pytest.raises(ext.I8ConvError) as ei:
-        ext.Plan((2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1), kernel_variant=4)
+        ext.Plan((2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1), kernel_variant=variant)
     assert ei.value.status == ext.I8C_ERR_UNSUPPORTED
