@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // CTA 0: cycles spent in each kind of wait and in the MMA issue blocks
     const bool tracing = p.trace != nullptr && blockIdx.x == 0;
     long long stall_acc = 0, stall_b = 0, stall_h = 0, t_issue = 0, t_first = 0, t_post = 0, t_end = 0;
+    long long stall_h_first = 0;  // halo waits during the CTA's first tile
     uint32_t slices = 0;
     if (tracing) t_first = clock64();
     if (p.trace != nullptr && lane == 0 && blockIdx.x < kTraceSlots)
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         }
 #if defined(I8C_PIPELINE_TRACE)
         if (tracing) stall_h += clock64() - th;
+        if (tracing && unit == ts.first) stall_h_first += clock64() - th;
 #endif
         if (kk == next_chunk) {
           if (kk != 0) {
@@ -239,6 +241,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           // 2^18 bytes)
           const uint64_t hd_base = h_desc0 | static_cast<uint64_t>((h_stage + static_cast<uint32_t>(toff)) & 0x3FFFu);
           const uint64_t fd_base = f_desc0 | static_cast<uint64_t>(f_cur & 0x3FFFu);
+          // the stage's MMAs, the filter stage's release and, when the stage
+          // ends a channel block, the halo's release in one elected block
+          const bool cb_last = sc + 1 == stages_per_cb;
           issue([&] {
 #pragma unroll
             for (int t = 0; t < GT; ++t) {
@@ -248,6 +253,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
               mma(d_tmem, fd + 2, hd + chunk2_lo, 1u);
             }
             commit(&b_empty[st]);
+            if (cb_last) commit(&h_empty[hst]);
           });
           acc_flag = 1;
           toff += stage_rowstep;
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           sc = 0;
           tcol = 0;
           toff = 0;
-          issue([&] { commit(&h_empty[hst]); });
+          if constexpr (GT == 0) issue([&] { commit(&h_empty[hst]); });  // GT > 0: released above
           hst = hst + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hst + 1;
           hph ^= hst == 0 ? 1u : 0u;
         }
@@ -307,6 +313,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       p.trace[4 * kTraceSlots + 3] = stall_h;
       p.trace[4 * kTraceSlots + 7] = t_issue;
       p.trace[4 * kTraceSlots + 8] = t_post;
+      p.trace[4 * kTraceSlots + 9] = stall_h_first;
     }
 #endif
     if (!ok && lane == 0) raise_timeout(p, abort_flag);
