@@ -71,6 +71,8 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
             lib.oracle_conv2d_acc_points.argtypes = [p, p, ctypes.POINTER(_Shape), p, i64, p]
             lib.oracle_requantize.restype = ctypes.c_int
             lib.oracle_requantize.argtypes = [p, i64, ctypes.c_float, p]
+            lib.oracle_requantize_channels.restype = ctypes.c_int
+            lib.oracle_requantize_channels.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, ctypes.c_int, p]
             lib.oracle_mutation_id.restype = ctypes.c_int
             _libs[mutation] = lib
         return _libs[mutation]
@@ -140,6 +142,26 @@ class Oracle:
         """(int8 NKPQ output, int64 NKPQ accumulators)."""
         acc = self.conv_acc(x_nchw, f_kcrs, shape, threads)
         return self.requantize(acc, alpha), acc
+
+    # -- per-output-channel epilogue: scale, bias, ReLU, clamp -------------
+    def requantize_channels(self, acc_nkpq: np.ndarray, alpha: float, alpha_k=None, bias_k=None,
+                            relu: bool = False) -> np.ndarray:
+        """int8 NKPQ output of clamp(rint(relu(alpha_k*float(acc) + bias_k)))."""
+        a = np.ascontiguousarray(acc_nkpq, dtype=np.int64)
+        N, K = a.shape[0], a.shape[1]
+        PQ = int(np.prod(a.shape[2:])) if a.ndim > 2 else 1
+        ak = None if alpha_k is None else np.ascontiguousarray(alpha_k, dtype=np.float32).reshape(K)
+        bk = None if bias_k is None else np.ascontiguousarray(bias_k, dtype=np.float32).reshape(K)
+        y = np.zeros(a.shape, dtype=np.int8)
+        rc = self.lib.oracle_requantize_channels(a.ctypes.data, N, K, PQ, ctypes.c_float(alpha),
+                                                 None if ak is None else ak.ctypes.data,
+                                                 None if bk is None else bk.ctypes.data, int(bool(relu)),
+                                                 y.ctypes.data)
+        if rc == 2:
+            raise OverflowError("accumulator outside int32")
+        if rc != 0:
+            raise ValueError(f"oracle_requantize_channels failed ({rc})")
+        return y
 
 
 # -- layouts ---------------------------------------------------------------

@@ -24,6 +24,15 @@
  *    the product is one single-precision multiply (no FMA, no double), and
  *    rint rounds half to even.
  *
+ *  - The per-output-channel epilogue (the "row-wise scaling" of the
+ *    weight-only quantisation issue on page 2, with a bias and a ReLU fused
+ *    before the clamp):
+ *        y = clamp(rint(relu(alpha_k * (float)acc32 + bias_k)), -128, 127)
+ *    alpha_k the scale of output channel k (or the one alpha), one fp32
+ *    multiply, then one fp32 add of bias_k (round to nearest even each, no
+ *    FMA), relu(v) = max(v, 0) when asked for.  With alpha_k = alpha, no bias
+ *    and no ReLU it is the clamp epilogue above.
+ *
  * Built with -ffp-contract=off and without fast-math so the epilogue is the
  * IEEE single-precision sequence described above on both x86-64 and AArch64.
  */
@@ -198,6 +207,46 @@ int oracle_requantize(const int64_t *acc, int64_t count, float alpha, int8_t *y)
 #endif
         y[i] = (int8_t)(int32_t)r;
     }
+    return ORACLE_OK;
+}
+
+/* The per-output-channel epilogue on int32 accumulators held as int64 in
+ * NKPQ order (count = N*K*PQ): alpha_k / bias_k are K floats each (alpha_k
+ * NULL: the scalar alpha; bias_k NULL: no bias), relu non-zero: max(v, 0)
+ * before the clamp.  ORACLE_ERANGE if an accumulator does not fit in int32. */
+int oracle_requantize_channels(const int64_t *acc, int64_t N, int64_t K, int64_t PQ, float alpha,
+                               const float *alpha_k, const float *bias_k, int relu, int8_t *y)
+{
+    if ((!acc || !y) && N * K * PQ > 0) return ORACLE_EINVAL;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+#if ORACLE_MUTATION == 11
+            const int64_t kk = n % K;              /* planted: the channel's scale indexed by the image */
+#else
+            const int64_t kk = k;
+#endif
+            const float a = alpha_k ? alpha_k[kk] : alpha;
+            const float b = bias_k ? bias_k[kk] : 0.0f;
+            for (int64_t i = 0; i < PQ; ++i) {
+                const int64_t idx = (n * K + k) * PQ + i;
+                if (acc[idx] > INT32_MAX || acc[idx] < INT32_MIN) return ORACLE_ERANGE;
+                volatile float v = (float)(int32_t)acc[idx];   /* int32 -> fp32, round to nearest even */
+#if ORACLE_MUTATION == 9
+                volatile float sum = a * (v + b);                /* planted: bias added before the scale */
+#elif ORACLE_MUTATION == 12
+                volatile float sum = fmaf(a, v, b);              /* planted: one fused multiply-add */
+#else
+                volatile float prod = a * v;                     /* one fp32 multiply */
+                volatile float sum = prod + b;                   /* then one fp32 add */
+#endif
+                float r = sum;
+                if (relu && r < 0.0f) r = 0.0f;
+                r = rintf(r);                                    /* round half to even */
+                if (r > 127.0f) r = 127.0f;
+                if (r < -128.0f) r = -128.0f;
+                y[idx] = (int8_t)(int32_t)r;
+            }
+        }
     return ORACLE_OK;
 }
 

@@ -251,4 +251,50 @@ def pin_epilogue_int32_guard(orc):
         raise AssertionError("int32 overflow not detected")
 
 
+# --- per-output-channel epilogue: scale, bias, ReLU --------------------------
+
+def pin_channel_epilogue_hand_values(orc):
+    """clamp(rint(relu(alpha_k*acc + bias_k))) worked by hand: alpha_k =
+    (0.5, 0.25, 2), bias_k = (0, -30.5, 1.5); every product and sum below is
+    exact in fp32, and the .5 cases round half to even."""
+    acc = np.array([[[3, 5, -7, 1000], [100, 142, 0, -1000], [10, -1, 63, -64]],
+                    [[-3, 1, 255, -255], [122, 123, 126, -2], [0, 1, -2, 20]]], np.int64)
+    alpha_k = np.array([0.5, 0.25, 2.0], np.float32)
+    bias_k = np.array([0.0, -30.5, 1.5], np.float32)
+    # n=0: 1.5->2, 2.5->2, -3.5->-4, 500->127 | 25-30.5=-5.5->-6, 35.5-30.5=5, -30.5->-30, -280.5->-128
+    #      20+1.5=21.5->22, -2+1.5=-0.5->0, 127.5->127, -126.5->-126
+    # n=1: -1.5->-2, 0.5->0, 127.5->127, -127.5->-128 | 0, 0.25->0, 1, -31
+    #      1.5->2, 3.5->4, -2.5->-2, 41.5->42
+    want = np.array([[[2, 2, -4, 127], [-6, 5, -30, -128], [22, 0, 127, -126]],
+                     [[-2, 0, 127, -128], [0, 0, 1, -31], [2, 4, -2, 42]]], np.int8)
+    want_relu = np.array([[[2, 2, 0, 127], [0, 5, 0, 0], [22, 0, 127, 0]],
+                          [[0, 0, 127, 0], [0, 0, 1, 0], [2, 4, 0, 42]]], np.int8)
+    assert np.array_equal(orc.requantize_channels(acc, 1.0, alpha_k, bias_k, relu=False), want)
+    assert np.array_equal(orc.requantize_channels(acc, 1.0, alpha_k, bias_k, relu=True), want_relu)
+    # no bias: the scale alone; no per-channel scale: the scalar alpha
+    assert np.array_equal(orc.requantize_channels(acc[:, :1], 1.0, alpha_k[:1]), np.array([[[2, 2, -4, 127]], [[-2, 0, 127, -128]]], np.int8))
+    assert np.array_equal(orc.requantize_channels(acc[:, 1:2], 0.25, None, bias_k[1:2]), np.array([[[-6, 5, -30, -128]], [[0, 0, 1, -31]]], np.int8))
+
+
+def pin_channel_epilogue_separate_roundings(orc):
+    """One fp32 multiply, then one fp32 add, each rounded: alpha = fp32(1/3) =
+    11184811 * 2^-25 and acc = 6 give the exact product 2 + 2^-24, which
+    rounds to 2.0 (a quarter of an ulp above it); 2.0 - 1.5 = 0.5 and rint
+    gives 0.  A fused multiply-add would keep 0.5 + 2^-24 (representable)
+    and give 1."""
+    acc = np.array([[[6]]], np.int64)
+    y = orc.requantize_channels(acc, 1.0, np.array([1.0 / 3.0], np.float32), np.array([-1.5], np.float32))
+    assert y.reshape(-1)[0] == 0
+
+
+def pin_channel_epilogue_reduces_to_alpha_only(orc):
+    """Equal scales, no bias, no ReLU: the alpha-only clamp epilogue."""
+    rng = np.random.default_rng(17)
+    acc = rng.integers(-2**31, 2**31, (3, 4, 50), dtype=np.int64)
+    for alpha in (2.0 ** -9, 0.3, 1.0 / 3.0):
+        ak = np.full(4, alpha, np.float32)
+        assert np.array_equal(orc.requantize_channels(acc, 5.0, ak), orc.requantize(acc, alpha).reshape(acc.shape))
+        assert np.array_equal(orc.requantize_channels(acc, alpha), orc.requantize(acc, alpha).reshape(acc.shape))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -16,6 +16,9 @@ MUTATIONS = {
     6: "symmetric clamp range",
     7: "last input channel dropped",
     8: "output extent off by one dilation",
+    9: "bias added before the per-channel scale",
+    11: "per-channel scale indexed by the image",
+    12: "fused multiply-add in the per-channel epilogue",
 }
 
 
