@@ -126,6 +126,22 @@ typedef struct {
 
 typedef struct i8c_plan i8c_plan;
 
+
+/* Per-output-channel epilogue of i8c_plan_run_ex / i8c_conv2d_fprop_ex (the
+ * row-wise scaling of the weight-only quantisation issue, with a bias and a
+ * ReLU fused before the clamp):
+ *     y[n][k][p][q] = clamp(rint(relu(alpha_k * (float)acc + bias_k)), -128, 127)
+ * one fp32 multiply, then one fp32 add, each rounded to nearest even (never
+ * fused), relu(v) = max(v, 0) when asked for, rint half to even.  With
+ * alpha = NULL and bias = NULL and relu = 0 this is the alpha-only epilogue of
+ * i8c_plan_run.  Both arrays are DEVICE memory of K floats, 16-byte aligned,
+ * read by the kernel (owned by the caller; not modified). */
+typedef struct {
+  const float* alpha;  /* per-channel scales, or NULL: the scalar alpha argument */
+  const float* bias;   /* per-channel biases added after the scale, or NULL: none */
+  int32_t relu;        /* 1: clamp below at 0 (ReLU) before the int8 clamp      */
+} i8c_epilogue;
+
 /* Read-only facts about a plan (for benchmarks and tests). */
 typedef struct {
   int32_t P, Q;              /* output height and width                        */
@@ -184,6 +200,11 @@ i8c_status i8c_conv2d_fprop(const int8_t* x, const int8_t* f, int8_t* y, const i
 i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, const i8c_conv_shape* shape,
                                 cudaStream_t stream);
 
+/* As i8c_conv2d_fprop, with the per-output-channel epilogue `ep` (see
+ * i8c_epilogue; NULL: the alpha-only epilogue). */
+i8c_status i8c_conv2d_fprop_ex(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape,
+                               float alpha, const i8c_epilogue* ep, cudaStream_t stream);
+
 /* Same convolution and arguments as i8c_conv2d_fprop, for callers that must
  * not allocate device memory.  The pages have no counterpart to this entry
  * point; it exists for code whose device memory is owned by someone else
@@ -223,6 +244,12 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
  * filter staging buffer. */
 i8c_status i8c_plan_run(const i8c_plan* plan, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
                         cudaStream_t stream);
+
+/* i8c_plan_run with the per-output-channel epilogue `ep` (NULL: the
+ * alpha-only epilogue).  I8C_ERR_MISALIGNED if ep->alpha or ep->bias is not
+ * 16-byte aligned.  Same scheduling rules as i8c_plan_run. */
+i8c_status i8c_plan_run_ex(const i8c_plan* plan, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
+                           const i8c_epilogue* ep, cudaStream_t stream);
 
 /* Unchecked run that writes int32 accumulators (layout as in _acc above). */
 i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t* f, int32_t* acc,

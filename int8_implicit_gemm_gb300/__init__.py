@@ -52,6 +52,11 @@ class ConvShape(ctypes.Structure):
         return tuple(getattr(self, n) for n, _ in self._fields_)
 
 
+class Epilogue(ctypes.Structure):
+    """i8c_epilogue: per-output-channel scale and bias (device pointers) and ReLU."""
+    _fields_ = [("alpha", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("relu", ctypes.c_int32)]
+
+
 class Options(ctypes.Structure):
     _fields_ = [("block_n", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("max_chunk_slices", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
@@ -93,6 +98,8 @@ def _load() -> ctypes.CDLL:
         "i8c_conv2d_fprop_noalloc": [P, P, P, S, F, P],
         "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
         "i8c_plan_run": [P, P, P, P, F, P],
+        "i8c_plan_run_ex": [P, P, P, P, F, ctypes.POINTER(Epilogue), P],
+        "i8c_conv2d_fprop_ex": [P, P, P, S, F, ctypes.POINTER(Epilogue), P],
         "i8c_plan_run_acc": [P, P, P, P, P],
         "i8c_plan_run_host": [P, P, P, P, F, P],
         "i8c_plan_status": [P, P],
@@ -167,6 +174,15 @@ def i8c_conv2d_fprop(x, f, y, shape, alpha: float, stream=None) -> None:
                                 ctypes.c_float(alpha), _stream(stream)), "i8c_conv2d_fprop")
 
 
+def i8c_conv2d_fprop_ex(x, f, y, shape, alpha: float, alpha_k=None, bias=None, relu: bool = False,
+                        stream=None) -> None:
+    """One-shot run with the per-output-channel epilogue (alpha_k, bias: CUDA
+    float32 tensors of K values or None)."""
+    ep = Epilogue(None if alpha_k is None else _ptr(alpha_k), None if bias is None else _ptr(bias), int(bool(relu)))
+    _check(lib.i8c_conv2d_fprop_ex(_ptr(x), _ptr(f), _ptr(y), ctypes.byref(ConvShape.of(shape)),
+                                   ctypes.c_float(alpha), ctypes.byref(ep), _stream(stream)), "i8c_conv2d_fprop_ex")
+
+
 def i8c_conv2d_fprop_acc(x, f, acc, shape, stream=None) -> None:
     _check(lib.i8c_conv2d_fprop_acc(_ptr(x), _ptr(f), _ptr(acc), ctypes.byref(ConvShape.of(shape)),
                                     _stream(stream)), "i8c_conv2d_fprop_acc")
@@ -224,9 +240,16 @@ class Plan:
         _check(lib.i8c_plan_get_info(self.handle, ctypes.byref(info)), "i8c_plan_get_info")
         self.info = info.asdict()
 
-    def run(self, x, f, y, alpha: float, stream=None) -> None:
-        _check(lib.i8c_plan_run(self.handle, _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha), _stream(stream)),
-               "i8c_plan_run")
+    def run(self, x, f, y, alpha: float, stream=None, alpha_k=None, bias=None, relu: bool = False) -> None:
+        """y = clamp(rint(alpha * acc)); with alpha_k / bias (CUDA float32 tensors
+        of K values) or relu, the per-output-channel epilogue (i8c_plan_run_ex)."""
+        if alpha_k is None and bias is None and not relu:
+            _check(lib.i8c_plan_run(self.handle, _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha), _stream(stream)),
+                   "i8c_plan_run")
+            return
+        ep = Epilogue(None if alpha_k is None else _ptr(alpha_k), None if bias is None else _ptr(bias), int(bool(relu)))
+        _check(lib.i8c_plan_run_ex(self.handle, _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha), ctypes.byref(ep),
+                                   _stream(stream)), "i8c_plan_run_ex")
 
     def run_acc(self, x, f, acc, stream=None) -> None:
         _check(lib.i8c_plan_run_acc(self.handle, _ptr(x), _ptr(f), _ptr(acc), _stream(stream)), "i8c_plan_run_acc")

@@ -1063,12 +1063,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
               const int64_t off = ((static_cast<int64_t>(t.n) * p.KB + (k0 >> 5)) * p.P + pp) * p.Q + qq;
               if (p.out_mode == 0) {
                 uint32_t o[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  o[i] = pack4_s8(requant(static_cast<int>(run[g * 32 + 4 * i]), p.alpha),
-                                  requant(static_cast<int>(run[g * 32 + 4 * i + 1]), p.alpha),
-                                  requant(static_cast<int>(run[g * 32 + 4 * i + 2]), p.alpha),
-                                  requant(static_cast<int>(run[g * 32 + 4 * i + 3]), p.alpha));
+                requant32(p, k0, [&](int i) { return static_cast<int>(run[g * 32 + i]); }, o);
                 uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 dst[1] = make_uint4(o[4], o[5], o[6], o[7]);

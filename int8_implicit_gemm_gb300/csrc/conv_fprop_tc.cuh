@@ -43,6 +43,10 @@ struct ConvParams {
   int32_t* acc;    // int32 accumulators (out_mode 1)
   int* status;     // device status word (0 = ok)
   float alpha;
+  // per-output-channel epilogue (null / 0: the scalar alpha, no bias, no ReLU)
+  const float* alpha_k;  // K scales, 16-byte aligned
+  const float* bias_k;   // K biases added after the scale, 16-byte aligned
+  int relu;              // 1: max(v, 0) before the clamp
   int H, W, K;
   int pad_h, pad_w, stride_h, stride_w, dil_h, dil_w;
   int R, S;
@@ -123,9 +127,53 @@ __device__ __forceinline__ int requant(int a, float alpha) {
   return __float2int_rn(fminf(fmaxf(prod, -128.0f), 127.0f));
 }
 
+// The per-output-channel epilogue: one fp32 multiply by the channel's scale
+// and one fp32 add of its bias, each rounded to nearest even and never fused
+// (a fused multiply-add rounds once and can land on the other side of a .5),
+// then ReLU as a lower bound of 0 (lo = 0, else lo = -128), the clamp to the
+// int8 range and round half to even.  With scale = alpha, bias = 0 and
+// lo = -128 it equals requant(): adding 0 changes at most the sign of a zero.
+__device__ __forceinline__ int requant_ch(int a, float scale, float bias, float lo) {
+  const float v = __fadd_rn(__fmul_rn(__int2float_rn(a), scale), bias);
+  return __float2int_rn(fminf(fmaxf(v, lo), 127.0f));
+}
+
 __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
   return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
          ((static_cast<uint32_t>(c) & 0xFFu) << 16) | (static_cast<uint32_t>(d) << 24);
+}
+
+// One pixel's 32 consecutive output channels k0 .. k0 + 31 (a(i) the
+// accumulator of channel k0 + i) requantised into eight packed words, with
+// the channels' scales and biases, or the scalar alpha and no bias.
+template <typename Acc>
+__device__ __forceinline__ void requant32(const ConvParams& p, int k0, Acc&& a, uint32_t (&o)[8]) {
+  const float lo = p.relu ? 0.0f : -128.0f;
+  if (p.alpha_k == nullptr && p.bias_k == nullptr) {  // one scale, no bias: no loads
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      o[i] = pack4_s8(requant_ch(a(4 * i), p.alpha, 0.0f, lo), requant_ch(a(4 * i + 1), p.alpha, 0.0f, lo),
+                      requant_ch(a(4 * i + 2), p.alpha, 0.0f, lo), requant_ch(a(4 * i + 3), p.alpha, 0.0f, lo));
+    return;
+  }
+  // per-channel scales or biases, loaded channel by channel where they are
+  // used (every lane of the warp reads the same addresses): volatile loads
+  // the compiler keeps in place, so the 256-wide kernels' epilogue (128
+  // running sums per thread) stays within its register budget
+  const float* sa = p.alpha_k != nullptr ? p.alpha_k + k0 : nullptr;
+  const float* sb = p.bias_k != nullptr ? p.bias_k + k0 : nullptr;
+  auto ld = [](const float* q) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(q));
+    return v;
+  };
+  auto ch = [&](int i) {
+    const float sc = sa != nullptr ? ld(sa + i) : p.alpha;
+    const float bi = sb != nullptr ? ld(sb + i) : 0.0f;
+    return requant_ch(a(i), sc, bi, lo);
+  };
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i] = pack4_s8(ch(4 * i), ch(4 * i + 1), ch(4 * i + 2), ch(4 * i + 3));
 }
 
 template <int BN>
@@ -391,18 +439,11 @@ __global__ void __launch_bounds__(TileCfg<BN>::kThreads, 1)
             const int kb = k0 >> 5;
             const int64_t off = (static_cast<int64_t>(n_img) * p.KB + kb) * p.PQ + pq;
             if (p.out_mode == 0) {
-              uint4 o0, o1;
-              o0.x = pack4_s8(requant(a[0], p.alpha), requant(a[1], p.alpha), requant(a[2], p.alpha), requant(a[3], p.alpha));
-              o0.y = pack4_s8(requant(a[4], p.alpha), requant(a[5], p.alpha), requant(a[6], p.alpha), requant(a[7], p.alpha));
-              o0.z = pack4_s8(requant(a[8], p.alpha), requant(a[9], p.alpha), requant(a[10], p.alpha), requant(a[11], p.alpha));
-              o0.w = pack4_s8(requant(a[12], p.alpha), requant(a[13], p.alpha), requant(a[14], p.alpha), requant(a[15], p.alpha));
-              o1.x = pack4_s8(requant(a[16], p.alpha), requant(a[17], p.alpha), requant(a[18], p.alpha), requant(a[19], p.alpha));
-              o1.y = pack4_s8(requant(a[20], p.alpha), requant(a[21], p.alpha), requant(a[22], p.alpha), requant(a[23], p.alpha));
-              o1.z = pack4_s8(requant(a[24], p.alpha), requant(a[25], p.alpha), requant(a[26], p.alpha), requant(a[27], p.alpha));
-              o1.w = pack4_s8(requant(a[28], p.alpha), requant(a[29], p.alpha), requant(a[30], p.alpha), requant(a[31], p.alpha));
+              uint32_t o[8];
+              requant32(p, k0, [&](int i) { return a[i]; }, o);
               uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
-              dst[0] = o0;
-              dst[1] = o1;
+              dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+              dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
             } else {
               int4* dst = reinterpret_cast<int4*>(p.acc + off * 32);
 #pragma unroll

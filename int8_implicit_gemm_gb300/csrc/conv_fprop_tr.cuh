@@ -469,12 +469,18 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         // per-column code runs once per tile, and fully unrolled stores with
         // their address arithmetic would not stay in the instruction cache.
         uint8_t* wbuf = smem + hp.off_out + (warp - 8) * (NP * 16);
+        // this lane's output channel: its scale and bias (or the scalar alpha and 0)
+        const int kch = cbk * 32 + lane;
+        const float scale = p.alpha_k != nullptr ? __ldg(p.alpha_k + kch) : p.alpha;
+        const float bias = p.bias_k != nullptr ? __ldg(p.bias_k + kch) : 0.0f;
+        const float lo = p.relu ? 0.0f : -128.0f;
 #pragma unroll
         for (int g = 0; g < kMaxGroupsPerWarp; ++g) {
           if (g >= gh) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            wbuf[(g * 8 + i) * 32 + lane] = static_cast<uint8_t>(requant(static_cast<int>(run[g * 8 + i]), p.alpha));
+            wbuf[(g * 8 + i) * 32 + lane] =
+                static_cast<uint8_t>(requant_ch(static_cast<int>(run[g * 8 + i]), scale, bias, lo));
         }
         __syncwarp();
         for (int e = lane; e < 2 * ncols; e += 32) {

@@ -323,7 +323,7 @@ ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
 }
 
 i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t* y, int32_t* acc, float alpha,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, const i8c_epilogue* ep = nullptr) {
   const i8c_conv_shape& s = pl->shape;
   cudaError_t e = cudaSuccess;
   if (pl->gbar == nullptr) {  // else the halo kernel converts the filter itself
@@ -334,6 +334,11 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
   p.y = y;
   p.acc = acc;
   p.out_mode = acc != nullptr ? 1 : 0;
+  if (ep != nullptr) {
+    p.alpha_k = ep->alpha;
+    p.bias_k = ep->bias;
+    p.relu = ep->relu != 0 ? 1 : 0;
+  }
   const size_t nev = pl->ev_start.size();
   if (nev > 0) {
     e = cudaEventRecord(pl->ev_start[pl->ev_recorded % nev], stream);
@@ -886,6 +891,15 @@ i8c_status i8c_plan_run(const i8c_plan* plan, const int8_t* x, const int8_t* f, 
   return run_plan(plan, x, f, y, nullptr, alpha, stream);
 }
 
+i8c_status i8c_plan_run_ex(const i8c_plan* plan, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
+                           const i8c_epilogue* ep, cudaStream_t stream) {
+  if (plan == nullptr || x == nullptr || f == nullptr || y == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  if (ep != nullptr && ((ep->alpha != nullptr && !aligned16(ep->alpha)) || (ep->bias != nullptr && !aligned16(ep->bias))))
+    return I8C_ERR_MISALIGNED;
+  return run_plan(plan, x, f, y, nullptr, alpha, stream, ep);
+}
+
 i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t* f, int32_t* acc,
                             cudaStream_t stream) {
   if (plan == nullptr || x == nullptr || f == nullptr || acc == nullptr) return I8C_ERR_INVALID_ARG;
@@ -932,6 +946,18 @@ i8c_status i8c_conv2d_fprop(const int8_t* x, const int8_t* f, int8_t* y, const i
   i8c_status st = cached_plan(shape, stream, &p);
   if (st != I8C_OK) return st;
   return run_plan(p, x, f, y, nullptr, alpha, stream);
+}
+
+i8c_status i8c_conv2d_fprop_ex(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape,
+                               float alpha, const i8c_epilogue* ep, cudaStream_t stream) {
+  if (x == nullptr || f == nullptr || y == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(f) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  if (ep != nullptr && ((ep->alpha != nullptr && !aligned16(ep->alpha)) || (ep->bias != nullptr && !aligned16(ep->bias))))
+    return I8C_ERR_MISALIGNED;
+  i8c_plan* p = nullptr;
+  i8c_status st = cached_plan(shape, stream, &p);
+  if (st != I8C_OK) return st;
+  return run_plan(p, x, f, y, nullptr, alpha, stream, ep);
 }
 
 i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, const i8c_conv_shape* shape,

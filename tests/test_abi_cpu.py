@@ -79,7 +79,7 @@ def test_null_pointers_rejected(ext):
 
 
 @pytest.mark.parametrize("ctype,cls_name", [("i8c_conv_shape", "ConvShape"), ("i8c_options", "Options"),
-                                            ("i8c_plan_info", "PlanInfo")])
+                                            ("i8c_plan_info", "PlanInfo"), ("i8c_epilogue", "Epilogue")])
 def test_binding_structs_match_header(ext, tmp_path, ctype, cls_name):
     """The binding's ctypes structures have the header's size and field offsets
     (compiled with the host C compiler against include/i8conv.h)."""

@@ -176,3 +176,23 @@ def test_filter_conversion_inside_the_kernel(torch_cuda):
         y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -11)
         assert np.array_equal(y.cpu().numpy().reshape(y_ref.shape), y_ref)
     plan.destroy()
+
+
+def test_channel_epilogue_misaligned_rejected(torch_cuda):
+    """Per-channel scale or bias arrays must be 16-byte aligned (the kernels
+    read them with vector loads): a 4-byte offset is refused before launch."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (1, 32, 8, 8, 32, 3, 3, 1, 1, 1, 1, 1, 1)
+    plan = ext.Plan(shape)
+    x = torch.zeros(32 * 64, dtype=torch.int8, device="cuda")
+    f = torch.zeros(32 * 32 * 9, dtype=torch.int8, device="cuda")
+    y = torch.zeros(32 * 64, dtype=torch.int8, device="cuda")
+    ones = torch.ones(40, dtype=torch.float32, device="cuda")
+    for kw in (dict(alpha_k=ones[1:33]), dict(bias=ones[1:33])):
+        with pytest.raises(ext.I8ConvError) as ei:
+            plan.run(x, f, y, 1.0, **kw)
+        assert ei.value.status == ext.I8C_ERR_MISALIGNED
+    plan.run(x, f, y, 1.0, alpha_k=ones[:32], bias=ones[4:36], relu=True)
+    assert plan.status() == ext.I8C_OK
+    plan.destroy()

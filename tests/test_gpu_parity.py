@@ -235,3 +235,81 @@ def test_transposed_tiles_rejects_strides(variant):
     with pytest.raises(ext.I8ConvError) as ei:
         ext.Plan((2, 128, 23, 23, 256, 3, 3, 1, 1, 2, 2, 1, 1), kernel_variant=variant)
     assert ei.value.status == ext.I8C_ERR_UNSUPPORTED
+
+
+def _channel_params(K, seed):
+    """Per-channel scales (powers of two and arbitrary values) and biases
+    (quarter steps that make .5 ties, and arbitrary values)."""
+    rng = np.random.default_rng(seed)
+    scale = np.where(rng.random(K) < 0.5, 2.0 ** rng.integers(-13, -6, K),
+                     rng.uniform(1e-4, 4e-3, K)).astype(np.float32)
+    bias = np.where(rng.random(K) < 0.5, rng.integers(-80, 81, K) / 4.0,
+                    rng.uniform(-40.0, 40.0, K)).astype(np.float32)
+    return scale, bias
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4, 5], ids=["gather", "halo", "halo-pair", "transposed",
+                                                          "transposed-pair"])
+@pytest.mark.parametrize("ep", [dict(scale=True), dict(bias=True), dict(scale=True, bias=True, relu=True),
+                                dict(relu=True)], ids=["scale", "bias", "scale-bias-relu", "relu"])
+def test_channel_epilogue_exact(variant, ep):
+    """The per-output-channel epilogue (scale, bias, ReLU before the clamp)
+    on every kernel form: every int8 output equals the oracle's."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 64, 13, 11, 256, 3, 3, 1, 1, 1, 1, 1, 1)
+    N, C, H, W, K = shape[:5]
+    x, f = _data(shape, 4321)
+    orc = oracle.Oracle()
+    acc = orc.conv_acc(x, f, shape)
+    scale, bias = _channel_params(K, 99)
+    alpha = 2.0 ** -10
+    y_ref = orc.requantize_channels(acc, alpha, scale if ep.get("scale") else None,
+                                    bias if ep.get("bias") else None, ep.get("relu", False))
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    plan = ext.Plan(shape, kernel_variant=variant)
+    P, Q = plan.info["P"], plan.info["Q"]
+    y = torch.full((N, K // 32, P, Q, 32), 77, dtype=torch.int8, device="cuda")
+    sd = torch.from_numpy(scale).cuda() if ep.get("scale") else None
+    bd = torch.from_numpy(bias).cuda() if ep.get("bias") else None
+    plan.run(xd, fd, y, alpha, alpha_k=sd, bias=bd, relu=ep.get("relu", False))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    plan.destroy()
+    assert np.array_equal(y.cpu().numpy(), oracle.nchw_to_ncxhwx32(y_ref))
+
+
+def test_channel_epilogue_full_size_bench_workload():
+    """The benchmark workload at full size with per-channel scales, biases and
+    ReLU, in its auto launch configuration: the int32 accumulators against
+    the oracle at sampled points, and y == the oracle's per-channel epilogue
+    of those accumulators at every output element."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    wl = synth.WORKLOADS_BY_NAME["n8c256h56k256r3s1"]
+    shape = wl.shape_tuple()
+    x = wl.activations_nchw()
+    f = wl.filters_kcrs()
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    plan = ext.Plan(shape)
+    P, Q = plan.info["P"], plan.info["Q"]
+    N, K = wl.N, wl.K
+    scale, bias = _channel_params(K, 7)
+    y = torch.empty((N, K // 32, P, Q, 32), dtype=torch.int8, device="cuda")
+    acc = torch.empty((N, K // 32, P, Q, 32), dtype=torch.int32, device="cuda")
+    plan.run(xd, fd, y, wl.alpha, alpha_k=torch.from_numpy(scale).cuda(), bias=torch.from_numpy(bias).cuda(),
+             relu=True)
+    plan.run_acc(xd, fd, acc)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    plan.destroy()
+    orc = oracle.Oracle()
+    acc_np = acc.cpu().numpy()
+    pts = gpu_util.sample_points(shape, P, Q, 2000, seed=5)
+    idx = gpu_util.packed_index(shape, P, Q, pts)
+    assert np.array_equal(acc_np.reshape(-1)[idx].astype(np.int64), orc.conv_acc_points(x, f, shape, pts))
+    acc_nkpq = oracle.ncxhwx32_to_nchw(acc_np, N, K, P, Q).astype(np.int64)
+    y_ref = orc.requantize_channels(acc_nkpq, wl.alpha, scale, bias, relu=True)
+    assert np.array_equal(y.cpu().numpy(), oracle.nchw_to_ncxhwx32(y_ref))
