@@ -31,6 +31,7 @@
 // and frees its tensor memory before returning.
 #pragma once
 
+#include <climits>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -119,28 +120,39 @@ __device__ __forceinline__ void raise_timeout(const ConvParams& p, volatile int*
 }
 
 // Epilogue arithmetic of the LinearCombinationClamp / alpha-only configuration:
-// int32 -> fp32 (round to nearest even), one fp32 multiply, clamp to the int8
-// range, round half to even.  Clamping before rounding gives the same result
-// as after because both bounds are integers.
-__device__ __forceinline__ int requant(int a, float alpha) {
-  const float prod = __fmul_rn(__int2float_rn(a), alpha);
-  return __float2int_rn(fminf(fmaxf(prod, -128.0f), 127.0f));
+// int32 -> fp32 (round to nearest even), one fp32 multiply, round half to even
+// to int32.  The clamp to the int8 range is left to the saturating packs
+// below: both bounds are integers, so clamping before rounding and saturating
+// after it give the same byte (a float -> int32 conversion itself saturates,
+// so no product is out of reach of the clamp).
+__device__ __forceinline__ int requant_rn(int a, float alpha) {
+  return __float2int_rn(__fmul_rn(__int2float_rn(a), alpha));
 }
 
 // The per-output-channel epilogue: one fp32 multiply by the channel's scale
 // and one fp32 add of its bias, each rounded to nearest even and never fused
 // (a fused multiply-add rounds once and can land on the other side of a .5),
-// then ReLU as a lower bound of 0 (lo = 0, else lo = -128), the clamp to the
-// int8 range and round half to even.  With scale = alpha, bias = 0 and
-// lo = -128 it equals requant(): adding 0 changes at most the sign of a zero.
-__device__ __forceinline__ int requant_ch(int a, float scale, float bias, float lo) {
-  const float v = __fadd_rn(__fmul_rn(__int2float_rn(a), scale), bias);
-  return __float2int_rn(fminf(fmaxf(v, lo), 127.0f));
+// round half to even, then ReLU as a lower bound of 0 (lo = 0, else lo =
+// INT_MIN, no bound); the clamp to [-128, 127] again in the pack.  max(rint(v),
+// 0) = rint(max(v, 0)) because 0 is an integer.  With scale = alpha, bias = 0
+// and no ReLU it equals requant_rn(): adding 0 changes at most the sign of a
+// zero.
+__device__ __forceinline__ int requant_ch(int a, float scale, float bias, int lo) {
+  return max(__float2int_rn(__fadd_rn(__fmul_rn(__int2float_rn(a), scale), bias)), lo);
 }
 
-__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
-  return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
-         ((static_cast<uint32_t>(c) & 0xFFu) << 16) | (static_cast<uint32_t>(d) << 24);
+// Saturating packs of int32 values into int8 bytes (the packed-conversion
+// instruction: each source clamped to [-128, 127]); a is the lowest byte.
+__device__ __forceinline__ uint32_t pack4_sat_s8(int a, int b, int c, int d) {
+  uint32_t hi, r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(d), "r"(c));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ uint32_t sat_s8(int a) {
+  uint32_t r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, 0, %1, 0;" : "=r"(r) : "r"(a));
+  return r;
 }
 
 // One pixel's 32 consecutive output channels k0 .. k0 + 31 (a(i) the
@@ -148,18 +160,18 @@ __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
 // the channels' scales and biases, or the scalar alpha and no bias.
 template <typename Acc>
 __device__ __forceinline__ void requant32(const ConvParams& p, int k0, Acc&& a, uint32_t (&o)[8]) {
-  const float lo = p.relu ? 0.0f : -128.0f;
-  if (p.alpha_k == nullptr && p.bias_k == nullptr) {  // one scale, no bias: no loads
+  if (p.alpha_k == nullptr && p.bias_k == nullptr && !p.relu) {  // one scale, no bias: no loads
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      o[i] = pack4_s8(requant_ch(a(4 * i), p.alpha, 0.0f, lo), requant_ch(a(4 * i + 1), p.alpha, 0.0f, lo),
-                      requant_ch(a(4 * i + 2), p.alpha, 0.0f, lo), requant_ch(a(4 * i + 3), p.alpha, 0.0f, lo));
+      o[i] = pack4_sat_s8(requant_rn(a(4 * i), p.alpha), requant_rn(a(4 * i + 1), p.alpha),
+                          requant_rn(a(4 * i + 2), p.alpha), requant_rn(a(4 * i + 3), p.alpha));
     return;
   }
   // per-channel scales or biases, loaded channel by channel where they are
   // used (every lane of the warp reads the same addresses): volatile loads
   // the compiler keeps in place, so the 256-wide kernels' epilogue (128
   // running sums per thread) stays within its register budget
+  const int lo = p.relu ? 0 : INT_MIN;
   const float* sa = p.alpha_k != nullptr ? p.alpha_k + k0 : nullptr;
   const float* sb = p.bias_k != nullptr ? p.bias_k + k0 : nullptr;
   auto ld = [](const float* q) {
@@ -173,7 +185,7 @@ __device__ __forceinline__ void requant32(const ConvParams& p, int k0, Acc&& a, 
     return requant_ch(a(i), sc, bi, lo);
   };
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i] = pack4_s8(ch(4 * i), ch(4 * i + 1), ch(4 * i + 2), ch(4 * i + 3));
+  for (int i = 0; i < 8; ++i) o[i] = pack4_sat_s8(ch(4 * i), ch(4 * i + 1), ch(4 * i + 2), ch(4 * i + 3));
 }
 
 template <int BN>

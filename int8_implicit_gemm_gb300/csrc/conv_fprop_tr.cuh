@@ -473,14 +473,14 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         const int kch = cbk * 32 + lane;
         const float scale = p.alpha_k != nullptr ? __ldg(p.alpha_k + kch) : p.alpha;
         const float bias = p.bias_k != nullptr ? __ldg(p.bias_k + kch) : 0.0f;
-        const float lo = p.relu ? 0.0f : -128.0f;
+        const int lo = p.relu ? 0 : INT_MIN;
 #pragma unroll
         for (int g = 0; g < kMaxGroupsPerWarp; ++g) {
           if (g >= gh) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             wbuf[(g * 8 + i) * 32 + lane] =
-                static_cast<uint8_t>(requant_ch(static_cast<int>(run[g * 8 + i]), scale, bias, lo));
+                static_cast<uint8_t>(sat_s8(requant_ch(static_cast<int>(run[g * 8 + i]), scale, bias, lo)));
         }
         __syncwarp();
         for (int e = lane; e < 2 * ncols; e += 32) {
