@@ -285,6 +285,40 @@ i8c_status i8c_plan_trace(const i8c_plan* plan, long long* out, int64_t count);
 /* Frees the plan's device memory.  Synchronises the device first. */
 i8c_status i8c_plan_destroy(i8c_plan* plan);
 
+/* One candidate of i8c_plan_autotune: its options, the status of creating
+ * and running its plan (I8C_OK, or why the candidate was skipped: e.g.
+ * I8C_ERR_UNSUPPORTED for a kernel form the shape cannot use), and its mean
+ * device time per i8c_plan_run in microseconds (0 unless status is I8C_OK). */
+typedef struct {
+  i8c_options options;
+  int32_t status;
+  float us;
+} i8c_tune_entry;
+
+/* Plan selection by measurement, the search step of the "[BYOC] CUTLASS
+ * integration" pull request (apache/tvm #9261, tune_cutlass_kernels):
+ * creates each plan of a fixed candidate list for `shape` (i8c_plan_create's
+ * own choice first, then forced kernel forms, tile widths and CTA pairing),
+ * runs it twice untimed and `iters` times between CUDA events on `stream`,
+ * on the caller's tensors (layouts as for i8c_conv2d_fprop), and returns in
+ * *best the options of the fastest and in *best_us its mean time per run
+ * (filter staging + convolution).  Candidates whose plan cannot be created
+ * for the shape, or whose bounded waits ran out, are skipped.  Since the
+ * default comes first and ties keep the earlier candidate, the result is
+ * never slower than the default on these inputs (within timing noise).
+ *   entries / max_entries: optional (NULL, 0): the first max_entries
+ *     candidates' results, in order; *num_entries (optional) gets how many
+ *     were written.
+ *   On return y holds the chosen plan's output.
+ * Not for the hot path: it allocates and frees plans, synchronises the
+ * device, and cannot be captured in a graph.  Pass *best to i8c_plan_create
+ * to get the tuned plan.  Errors: I8C_ERR_INVALID_ARG (null pointer,
+ * iters < 1), I8C_ERR_MISALIGNED, the i8c_supported status of the shape, or
+ * the default candidate's status if no candidate could run. */
+i8c_status i8c_plan_autotune(const i8c_conv_shape* shape, const int8_t* x, const int8_t* f, int8_t* y, float alpha,
+                             int32_t iters, cudaStream_t stream, i8c_options* best, float* best_us,
+                             i8c_tune_entry* entries, int32_t max_entries, int32_t* num_entries);
+
 /* Layout helpers (device, byte permutations, not part of the timed path).
  * C (resp. K for filters) must be a multiple of 32 where it is interleaved. */
 i8c_status i8c_pack_nchw_to_ncxhwx32(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,

@@ -66,6 +66,11 @@ class Options(ctypes.Structure):
                 ("fused_filter", ctypes.c_int32), ("tile_px", ctypes.c_int32), ("filter_run", ctypes.c_int32)]
 
 
+class TuneEntry(ctypes.Structure):
+    """i8c_tune_entry: one candidate of i8c_plan_autotune."""
+    _fields_ = [("options", Options), ("status", ctypes.c_int32), ("us", ctypes.c_float)]
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [("P", ctypes.c_int32), ("Q", ctypes.c_int32), ("M", ctypes.c_int64),
                 ("gemm_n", ctypes.c_int32), ("gemm_k", ctypes.c_int32),
@@ -107,6 +112,8 @@ def _load() -> ctypes.CDLL:
         "i8c_plan_kernel_time": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
         "i8c_plan_trace": [P, P, I64],
         "i8c_plan_destroy": [P],
+        "i8c_plan_autotune": [S, P, P, P, F, I32, P, ctypes.POINTER(Options), ctypes.POINTER(F),
+                              ctypes.POINTER(TuneEntry), I32, ctypes.POINTER(I32)],
         "i8c_pack_nchw_to_ncxhwx32": [P, P, I32, I32, I32, I32, P],
         "i8c_unpack_ncxhwx32_to_nchw": [P, P, I32, I32, I32, I32, P],
         "i8c_pack_kcrs_to_cxrskx32": [P, P, I32, I32, I32, I32, P],
@@ -193,6 +200,25 @@ def i8c_conv2d_fprop_noalloc(x, f, y, shape, alpha: float, stream=None) -> None:
     library's fixed static device array (see include/i8conv.h)."""
     _check(lib.i8c_conv2d_fprop_noalloc(_ptr(x), _ptr(f), _ptr(y), ctypes.byref(ConvShape.of(shape)),
                                         ctypes.c_float(alpha), _stream(stream)), "i8c_conv2d_fprop_noalloc")
+
+
+def i8c_plan_autotune(x, f, y, shape, alpha: float, iters: int = 10, stream=None):
+    """Time the candidate plans of `shape` on these tensors (i8c_plan_autotune).
+    Returns (options, us, entries): the fastest candidate's plan options as a
+    dict of Plan keyword arguments, its mean time per run in microseconds, and
+    every candidate as (options dict, status, us).  y holds the chosen plan's
+    output afterwards."""
+    best, best_us = Options(), ctypes.c_float()
+    cap = 64
+    entries, n = (TuneEntry * cap)(), ctypes.c_int32()
+    _check(lib.i8c_plan_autotune(ctypes.byref(ConvShape.of(shape)), _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha),
+                                 int(iters), _stream(stream), ctypes.byref(best), ctypes.byref(best_us), entries, cap,
+                                 ctypes.byref(n)), "i8c_plan_autotune")
+
+    def opts(o):
+        return {name: getattr(o, name) for name, _ in Options._fields_}
+
+    return opts(best), best_us.value, [(opts(e.options), e.status, e.us) for e in entries[:n.value]]
 
 
 def i8c_pack_nchw_to_ncxhwx32(src, dst, N, C, H, W, stream=None) -> None:

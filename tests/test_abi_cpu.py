@@ -78,8 +78,29 @@ def test_null_pointers_rejected(ext):
     assert st == ext.I8C_ERR_INVALID_ARG
 
 
+def test_autotune_argument_checks(ext):
+    """The tuner rejects bad arguments on the host, before touching a device."""
+    shape = ctypes.byref(ext.ConvShape.of((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1)))
+    best, us, n = ext.Options(), ctypes.c_float(), ctypes.c_int32()
+    buf = ctypes.create_string_buffer(64)
+    a = (ctypes.addressof(buf) + 15) & ~15
+    call = ext.lib.i8c_plan_autotune
+    assert call(shape, None, a, a, 1.0, 4, None, ctypes.byref(best), ctypes.byref(us), None, 0, None) == \
+        ext.I8C_ERR_INVALID_ARG
+    assert call(shape, a, a, a, 1.0, 0, None, ctypes.byref(best), ctypes.byref(us), None, 0, None) == \
+        ext.I8C_ERR_INVALID_ARG                                                  # iters < 1
+    assert call(shape, a, a, a, 1.0, 4, None, ctypes.byref(best), ctypes.byref(us), None, 3, ctypes.byref(n)) == \
+        ext.I8C_ERR_INVALID_ARG                                                  # entries NULL, max_entries > 0
+    assert call(shape, a + 1, a, a, 1.0, 4, None, ctypes.byref(best), ctypes.byref(us), None, 0, None) == \
+        ext.I8C_ERR_MISALIGNED
+    bad = ctypes.byref(ext.ConvShape.of((1, 48, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1)))
+    assert call(bad, a, a, a, 1.0, 4, None, ctypes.byref(best), ctypes.byref(us), None, 0, None) == \
+        ext.I8C_ERR_UNSUPPORTED                                                  # C not a multiple of 32
+
+
 @pytest.mark.parametrize("ctype,cls_name", [("i8c_conv_shape", "ConvShape"), ("i8c_options", "Options"),
-                                            ("i8c_plan_info", "PlanInfo"), ("i8c_epilogue", "Epilogue")])
+                                            ("i8c_plan_info", "PlanInfo"), ("i8c_epilogue", "Epilogue"),
+                                            ("i8c_tune_entry", "TuneEntry")])
 def test_binding_structs_match_header(ext, tmp_path, ctype, cls_name):
     """The binding's ctypes structures have the header's size and field offsets
     (compiled with the host C compiler against include/i8conv.h)."""

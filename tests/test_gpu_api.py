@@ -196,3 +196,38 @@ def test_channel_epilogue_misaligned_rejected(torch_cuda):
     plan.run(x, f, y, 1.0, alpha_k=ones[:32], bias=ones[4:36], relu=True)
     assert plan.status() == ext.I8C_OK
     plan.destroy()
+
+
+@pytest.mark.parametrize("shape", [(2, 64, 20, 20, 128, 3, 3, 1, 1, 1, 1, 1, 1),
+                                   (1, 64, 23, 23, 64, 3, 3, 1, 1, 2, 2, 1, 1)], ids=["stride1", "stride2"])
+def test_autotune_picks_an_exact_plan(torch_cuda, shape):
+    """The tuner times every candidate that the shape supports, returns the
+    fastest, leaves that plan's (bit-exact) output in y, and its options give
+    a plan whose output is bit-exact too."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    N, C, H, W, K, R, S = shape[:7]
+    x = synth.uniform_int8(40, N * C * H * W, -128, 127).reshape(N, C, H, W)
+    f = synth.uniform_int8(41, K * C * R * S, -128, 127).reshape(K, C, R, S)
+    alpha = 2.0 ** -11
+    y_ref, _ = gpu_util.oracle_packed(shape, x, f, alpha)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    y = torch.full(y_ref.shape, 77, dtype=torch.int8, device="cuda")
+    best, best_us, entries = ext.i8c_plan_autotune(xd, fd, y, shape, alpha, iters=3)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), y_ref)
+    ok = [e for e in entries if e[1] == 0]
+    assert entries[0][0]["kernel_variant"] == 0 and entries[0][1] == 0      # the default runs first
+    assert len(ok) >= 3 and all(e[2] > 0 for e in ok)
+    assert best_us == pytest.approx(min(e[2] for e in ok))
+    assert best in [e[0] for e in ok]
+    if shape[9] == 2:  # transposed tiles are stride-1 only
+        assert all(e[1] == ext.I8C_ERR_UNSUPPORTED for e in entries if e[0]["kernel_variant"] in (4, 5))
+    plan = ext.Plan(shape, **best)
+    y2 = torch.empty_like(y)
+    plan.run(xd, fd, y2, alpha)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    assert np.array_equal(y2.cpu().numpy(), y_ref)
+    plan.destroy()
