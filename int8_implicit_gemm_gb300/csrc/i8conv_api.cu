@@ -612,10 +612,33 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
         const double halo_cost = static_cast<double>((t + ctas - 1) / ctas) * 345.0;
         double tr_cost = 0.0, pair_cost = 0.0;
         int tr_groups = 0, pair_groups = 0;
-        const int n1 = pick_tr(1, &tr_cost, &tr_groups);
-        const int n2 = pick_tr(2, &pair_cost, &pair_groups);
+        int n1 = pick_tr(1, &tr_cost, &tr_groups);
+        int n2 = pick_tr(2, &pair_cost, &pair_groups);
         const bool pair = n2 != 0 && (n1 == 0 || pair_cost < tr_cost);
         const double cost = pair ? pair_cost : tr_cost;
+        // Halo tiles on CTA pairs (256 pixels x 256 channels per pair): a
+        // K-slice costs about 256 + 53 cycles, fitted to the 64x512x28x28
+        // layer (143 us against 148 us for transposed pairs), provided the
+        // halo stays close to its 128 pixels per CTA -- on strided layers the
+        // producers set the pace (stride-2 112x112 layer: 82 us on pairs
+        // against 69 us on single CTAs).  Taken when at least 2% cheaper than
+        // both other choices.
+        if (s.stride_h == 1 && s.stride_w == 1) {
+          const Choice hc = search(2, 256);
+          i8c::HaloParams h2;
+          int sm2 = 0;
+          if (hc.bn == 256 && halo_layout(s, p->P, p->Q, 256, 2, 0, hc.flat, &h2, &sm2) &&
+              h2.positions <= 1.6 * 128) {
+            const int64_t t2 = (static_cast<int64_t>(h2.num_patches) + 1) / 2 * ((s.K + 255) / 256);
+            const double hp_cost = static_cast<double>((t2 + hc.groups - 1) / hc.groups) * (256.0 + 53.0);
+            const double other = (n1 != 0 || n2 != 0) && cost < halo_cost ? cost : halo_cost;
+            if (hp_cost < 0.98 * other) {
+              cg = 2;
+              best = hc;
+              n1 = n2 = 0;  // keep the halo kernel
+            }
+          }
+        }
         if ((n1 != 0 || n2 != 0) && cost < 0.97 * halo_cost) {
           const int cgt = pair ? 2 : 1;
           const int n = pair ? n2 : n1;
