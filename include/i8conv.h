@@ -171,6 +171,9 @@ typedef struct {
   int32_t work_units;        /* units of work the persistent CTAs share          */
   int32_t tail_halves;       /* 2 when last-wave tiles are halved along the output channels */
   int32_t flat_tiles;        /* 1 when tiles are 128 consecutive padded-row pixels */
+  int32_t filter_resident;   /* halo kernel: 1 when the filter stages are loaded
+                                once per CTA and kept (one output-channel tile,
+                                whole-tile units, every stage fits)           */
 } i8c_plan_info;
 
 /* Output height P and width Q for a shape (formula above).  Returns

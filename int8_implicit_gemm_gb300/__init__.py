@@ -82,7 +82,8 @@ class PlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("kernel_variant", ctypes.c_int32),
                 ("halo_staging", ctypes.c_int32), ("filter_run", ctypes.c_int32),
                 ("filter_stages", ctypes.c_int32), ("tail_split", ctypes.c_int32),
-                ("work_units", ctypes.c_int32), ("tail_halves", ctypes.c_int32), ("flat_tiles", ctypes.c_int32)]
+                ("work_units", ctypes.c_int32), ("tail_halves", ctypes.c_int32), ("flat_tiles", ctypes.c_int32),
+                ("filter_resident", ctypes.c_int32)]
 
     def asdict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

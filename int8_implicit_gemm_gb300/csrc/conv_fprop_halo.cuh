@@ -46,6 +46,7 @@ struct HaloParams {
   uint32_t stg_bytes;       // one int8 staging slot: HR*CW*32 (rounded up to 128)
   int nstg;                 // int8 staging slots: 2 or 3, or 0 (producers load into registers)
   int nbs;                  // filter pipeline stages (<= kMaxBStages)
+  int resident;             // 1: the nbs stages are one unit's whole filter, loaded once and kept
   int nhs;                  // fp16 halo stages: 2 or 3
   int bgroup;               // K-slices per filter stage (one TMA box, one wait, one release)
   uint32_t off_stg, off_b, off_bar;
@@ -590,6 +591,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       }
       const int run_rowstep = GT > 0 ? (G / p.S) * row_step : 0;
       uint32_t u = 0, hst = 0, hph = 0, st = 0, bph = 0, g = 0;  // hst, hph: halo stage and its parity
+      // resident filter: the stages are loaded once, during the first
+      // first_pass K-slices, and never released
+      const bool resident = hp.resident != 0;
+      const uint32_t first_pass = static_cast<uint32_t>(nbs * G);
       bool ok = true;
 #if defined(I8C_PIPELINE_TRACE)
       const bool tracing = p.trace != nullptr && blockIdx.x == 0;
@@ -666,7 +671,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           const long long tb = tracing ? clock64() : 0;
           nr_b += ptx::mbar_test_wait<kCW>(&b_full[st], bph) ? 0 : 1;
 #endif
-          if (!wwait(&b_full[st], bph)) {
+          // a resident filter is waited for only on its first pass
+          if ((!resident || g < first_pass) && !wwait(&b_full[st], bph)) {
             ok = false;
             break;
           }
@@ -702,7 +708,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
                   ptx::mma_f16_ss(d_tmem, adv1[t], bdv[t] + 2, idesc_u, 1u);
                 }
               }
-              commit_all(&b_empty[st]);
+              if (!resident) commit_all(&b_empty[st]);
             }
             __syncwarp();
             acc_flag = 1;
@@ -747,7 +753,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             rowpos = cb_end ? 0 : rowpos;
           }
           if constexpr (!kOneBlock) {
-            if (ptx::elect_one()) commit_all(&b_empty[st]);
+            if (!resident && ptx::elect_one()) commit_all(&b_empty[st]);
             __syncwarp();
           }
 #if defined(I8C_PIPELINE_TRACE)
@@ -836,6 +842,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     bool ok = true;
     const int RS = p.R * p.S;
     for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
+      if (hp.resident && unit != ts.first) break;  // every unit reuses the first unit's stages
       const WorkUnit wu = decode_unit(unit, hp);
       const int n0 = (wu.tile % p.num_n_tiles) * BN + ts.rank * BNH;
       for (int kk = wu.cb0 * RS; kk < wu.cb1 * RS; kk += G, ++g) {

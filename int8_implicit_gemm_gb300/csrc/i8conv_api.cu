@@ -180,8 +180,11 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
     if (!(part_row || whole_rows) || G > 32) continue;
     const int min_stages = part_row ? 3 : 2;
     // a stage that holds a whole channel block leaves the producers one
-    // stage of slack with two halo stages: give them a third when it fits
-    for (int nhs = G == RS ? 3 : 2; nhs >= 2; --nhs)
+    // stage of slack with two halo stages: give them a third when it fits.
+    // With the staging ring, a single fp16 halo stage is allowed as a last
+    // resort: the ring already holds the next channel blocks' loads, and only
+    // the shared-memory conversion of each block waits for the MMAs.
+    for (int nhs = G == RS ? 3 : 2; nhs >= (loads == 1 ? 1 : 2); --nhs)
     for (int k = first; k <= last; ++k) {
       const int nstg = kSlots[k];
       const int64_t off_stg = static_cast<int64_t>(nhs) * h->halo_bytes;
@@ -723,6 +726,16 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     }
     p->halo.ksplit = ksplit;
     p->halo.nsplit = nsplit;
+    // Resident filter: with one output-channel tile and whole-tile units,
+    // every unit streams the same filter stages in the same order; when all
+    // of them fit in the stage ring, they are loaded once and kept, and the
+    // MMA warp stops waiting for and releasing filter stages after the first
+    // unit (e.g. the 64-channel 5x9 layer: five 9-slice stages per tile).
+    const int unit_stages = (s.C / 32) * s.R * s.S / p->halo.bgroup;
+    if (p->num_n_tiles == 1 && ksplit == 1 && nsplit == 1 && unit_stages <= p->halo.nbs) {
+      p->halo.nbs = unit_stages;
+      p->halo.resident = 1;
+    }
     p->halo.full_units = ksplit > 1 || nsplit > 1 ? p->num_tiles - rem : p->num_tiles;
     p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0) + (nsplit > 1 ? rem * 2 : 0);
     if (ksplit > 1)
@@ -868,6 +881,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->tail_split = pl->kernel_variant >= 2 ? pl->halo.ksplit : 1;
   info->tail_halves = pl->kernel_variant >= 2 ? pl->halo.nsplit : 1;
   info->flat_tiles = pl->kernel_variant >= 2 ? pl->halo.flat : 0;
+  info->filter_resident = pl->kernel_variant >= 2 ? pl->halo.resident : 0;
   info->work_units = pl->kernel_variant >= 2 ? pl->halo.num_units : pl->num_tiles;
   info->filter_stages = pl->kernel_variant >= 2 ? pl->halo.nbs
                         : pl->block_n >= 256 ? i8c::TileCfg<256>::kStages

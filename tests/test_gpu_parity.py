@@ -57,6 +57,8 @@ def test_small_shapes_exact(shape, alpha, kernel):
     dict(kernel_variant=1, block_n=64), dict(kernel_variant=2, block_n=256, max_chunk_slices=7),
     dict(kernel_variant=2, block_n=32, num_ctas=5), dict(kernel_variant=2, block_n=256, halo_loads=2),
     dict(kernel_variant=2, block_n=128, halo_loads=1, num_ctas=7),
+    # 256 wide with the staging ring: one fp16 halo stage beside two staging slots
+    dict(kernel_variant=2, block_n=256, halo_loads=1), dict(kernel_variant=2, block_n=256, halo_loads=1, num_ctas=5),
     dict(kernel_variant=3, num_ctas=2), dict(kernel_variant=3, num_ctas=6, max_chunk_slices=3),
     dict(kernel_variant=3, block_n=128, max_chunk_slices=1), dict(kernel_variant=3, block_n=256, num_ctas=4),
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
@@ -313,3 +315,26 @@ def test_channel_epilogue_full_size_bench_workload():
     acc_nkpq = oracle.ncxhwx32_to_nchw(acc_np, N, K, P, Q).astype(np.int64)
     y_ref = orc.requantize_channels(acc_nkpq, wl.alpha, scale, bias, relu=True)
     assert np.array_equal(y.cpu().numpy(), oracle.nchw_to_ncxhwx32(y_ref))
+
+
+@pytest.mark.parametrize("shape,opts", [
+    ((2, 32, 40, 40, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=3, block_n=64, num_ctas=4)),
+    ((2, 32, 40, 40, 32, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=2, block_n=32, num_ctas=3)),
+    ((3, 64, 20, 20, 64, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, block_n=64, num_ctas=2)),
+    ((2, 96, 17, 17, 32, 3, 3, 1, 1, 2, 2, 1, 1), dict(kernel_variant=2, num_ctas=2)),
+    ((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(num_ctas=1)),
+], ids=["dilated-pair", "dilated-single", "3x3-two-blocks", "stride2-three-blocks", "16x16"])
+def test_resident_filter_exact(shape, opts):
+    """One output-channel tile and whole-tile units: the filter stages are
+    loaded once per CTA and reused by every later tile (few CTAs, so each runs
+    many tiles); bit-exact against the oracle."""
+    import int8_implicit_gemm_gb300 as ext
+    plan = ext.Plan(shape, **opts)
+    assert plan.info["filter_resident"] == 1
+    assert plan.info["work_units"] > plan.info["num_ctas"] // (2 if plan.info["kernel_variant"] == 3 else 1)
+    plan.destroy()
+    x, f = _data(shape, 4242 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **opts)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
