@@ -3,7 +3,12 @@
 Compiles every ``csrc/*.cu`` translation unit in parallel with nvcc, then
 links them into ``_lib/libi8conv.so`` next to this file.  Run it directly or
 through ``__graft_entry__.build()``.  Rebuilds only when a source is newer
-than the library.
+than the library or the build flavour changed.
+
+``--pipeline-trace`` (or I8C_PIPELINE_TRACE=1 in the environment) builds the
+pipeline-analysis flavour: the kernels also record per-wait cycle counts and
+per-CTA timestamps in the plan's trace buffer (see pipeline_trace.py).  It is
+for analysis only; build again without it for normal use.
 """
 from __future__ import annotations
 
@@ -42,16 +47,26 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+STAMP = os.path.join(LIBDIR, "flavour")
+
+
+def _flavour(trace: bool) -> str:
+    return "pipeline-trace" if trace else "release"
+
+
+def up_to_date(trace: bool = False) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return False
+    with open(STAMP) as fh:
+        if fh.read().strip() != _flavour(trace):
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, verbose: bool) -> str:
+def _compile(src: str, verbose: bool, trace: bool = False) -> str:
     obj = os.path.join(OBJDIR, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(["-DI8C_PIPELINE_TRACE"] if trace else []), "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -62,21 +77,26 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, trace: bool | None = None) -> str:
+    if trace is None:
+        trace = os.environ.get("I8C_PIPELINE_TRACE", "") not in ("", "0")
+    if not force and up_to_date(trace):
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
+        objs = list(ex.map(lambda s: _compile(s, verbose, trace), srcs))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as fh:
+        fh.write(_flavour(trace))
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                trace=True if "--pipeline-trace" in sys.argv else None))

@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           }
 #if defined(I8C_PIPELINE_TRACE)
           const long long tb = tracing ? clock64() : 0;
-          nr_b += ptx::mbar_test_wait<kCW>(&b_full[st], bph) ? 0 : 1;
+          if (!resident || g < first_pass) nr_b += ptx::mbar_test_wait<kCW>(&b_full[st], bph) ? 0 : 1;
 #endif
           // a resident filter is waited for only on its first pass
           if ((!resident || g < first_pass) && !wwait(&b_full[st], bph)) {
