@@ -73,6 +73,10 @@ def _lib(mutation: int = 0) -> ctypes.CDLL:
             lib.oracle_requantize.argtypes = [p, i64, ctypes.c_float, p]
             lib.oracle_requantize_channels.restype = ctypes.c_int
             lib.oracle_requantize_channels.argtypes = [p, i64, i64, i64, ctypes.c_float, p, p, ctypes.c_int, p]
+            lib.oracle_conv2d_f64.restype = ctypes.c_int
+            lib.oracle_conv2d_f64.argtypes = [p, p, p, p, p, ctypes.POINTER(_Shape), ctypes.c_int]
+            lib.oracle_conv2d_f64_points.restype = ctypes.c_int
+            lib.oracle_conv2d_f64_points.argtypes = [p, p, p, ctypes.POINTER(_Shape), p, i64, p, p]
             lib.oracle_mutation_id.restype = ctypes.c_int
             _libs[mutation] = lib
         return _libs[mutation]
@@ -126,6 +130,52 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_conv2d_acc_points failed ({rc})")
         return out
+
+    # -- fp32 direct convolution (page 4), evaluated in double -------------
+    def conv_f64(self, x_nchw, w_kcrs, shape, bias=None, threads: int | None = None):
+        """(y, mag): NKPQ float64 outputs bias[k] + sum x*w of fp32 inputs, and
+        the magnitude sums |bias[k]| + sum |x*w| that bound fp32 rounding."""
+        N, C, H, W, K, R, S = shape[:7]
+        x = np.ascontiguousarray(x_nchw, dtype=np.float32)
+        w = np.ascontiguousarray(w_kcrs, dtype=np.float32)
+        assert x.shape == (N, C, H, W) and w.shape == (K, C, R, S)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(K)
+        P, Q = self.out_size(shape)
+        y = np.zeros((N, K, max(P, 0), max(Q, 0)), dtype=np.float64)
+        mag = np.zeros_like(y)
+        sh = self._shape(shape)
+        rc = self.lib.oracle_conv2d_f64(x.ctypes.data, w.ctypes.data, None if b is None else b.ctypes.data,
+                                        y.ctypes.data, mag.ctypes.data, ctypes.byref(sh),
+                                        threads or (os.cpu_count() or 1))
+        if rc != 0:
+            raise ValueError(f"oracle_conv2d_f64 failed ({rc})")
+        return y, mag
+
+    def conv_f64_points(self, x_nchw, w_kcrs, shape, pts, bias=None):
+        """(y, mag) at rows (n, k, p, q) of ``pts``."""
+        K = shape[4]
+        x = np.ascontiguousarray(x_nchw, dtype=np.float32)
+        w = np.ascontiguousarray(w_kcrs, dtype=np.float32)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(K)
+        pts = np.ascontiguousarray(pts, dtype=np.int64).reshape(-1, 4)
+        y = np.zeros(pts.shape[0], dtype=np.float64)
+        mag = np.zeros_like(y)
+        sh = self._shape(shape)
+        rc = self.lib.oracle_conv2d_f64_points(x.ctypes.data, w.ctypes.data, None if b is None else b.ctypes.data,
+                                               ctypes.byref(sh), pts.ctypes.data, pts.shape[0], y.ctypes.data,
+                                               mag.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"oracle_conv2d_f64_points failed ({rc})")
+        return y, mag
+
+    @staticmethod
+    def f32_error_bound(mag, terms: int):
+        """Largest difference between the exact sum and any fp32 recursive
+        evaluation of ``terms`` products (plus the bias) whose magnitude sum is
+        ``mag``: gamma_{terms+1} * mag with unit roundoff 2^-24."""
+        u = 2.0 ** -24
+        n = terms + 1
+        return (n * u / (1.0 - n * u)) * np.asarray(mag, dtype=np.float64)
 
     # -- epilogue (page 1: LinearCombinationClamp, alpha only) -------------
     def requantize(self, acc: np.ndarray, alpha: float) -> np.ndarray:

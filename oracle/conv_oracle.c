@@ -33,6 +33,17 @@
  *    FMA), relu(v) = max(v, 0) when asked for.  With alpha_k = alpha, no bias
  *    and no ReLU it is the clamp epilogue above.
  *
+ *  - The fp32 direct convolution of the kernel-benchmark trace (page 4):
+ *    nn.Conv2d on fp32 NCHW input and KCRS weight with an optional bias,
+ *    the same tap indexing and zero padding as above, which the trace checks
+ *    against the framework's own convolution with atol = rtol = 1e-4:
+ *        y[n][k][p][q] = bias[k] + sum_{c,r,s} x[n][c][h][w] * w[k][c][r][s]
+ *    evaluated here in double (each fp32 product is exact in double), with
+ *    the magnitude sum |bias[k]| + sum |x * w| beside it: any fp32
+ *    evaluation of the same sum, in any order, lies within
+ *    (C*R*S + 1) * 2^-24 / (1 - (C*R*S + 1) * 2^-24) times that magnitude of
+ *    the exact value (the standard bound for recursive summation).
+ *
  * Built with -ffp-contract=off and without fast-math so the epilogue is the
  * IEEE single-precision sequence described above on both x86-64 and AArch64.
  */
@@ -247,6 +258,104 @@ int oracle_requantize_channels(const int64_t *acc, int64_t N, int64_t K, int64_t
                 y[idx] = (int8_t)(int32_t)r;
             }
         }
+    return ORACLE_OK;
+}
+
+/* One fp32 direct-convolution output in double, and its magnitude sum. */
+static void f64_at(const float *x, const float *wt, const float *bias, const oracle_shape *s,
+                   int64_t n, int64_t k, int64_t p, int64_t q, double *out, double *mag)
+{
+    double sum = 0.0, abs_sum = 0.0;
+    if (bias) {
+#if ORACLE_MUTATION != 13
+        sum = (double)bias[k];                 /* (mutation 13 plants: bias ignored) */
+#endif
+        abs_sum = fabs((double)bias[k]);
+    }
+    for (int64_t c = 0; c < s->C; ++c)
+        for (int64_t r = 0; r < s->R; ++r) {
+            int64_t h = p * s->stride_h - s->pad_h + r * s->dil_h;
+            if (h < 0 || h >= s->H) continue;
+            for (int64_t t = 0; t < s->S; ++t) {
+#if ORACLE_MUTATION == 14
+                int64_t w = q * s->stride_w - s->pad_w + t;            /* planted: column dilation ignored */
+#else
+                int64_t w = q * s->stride_w - s->pad_w + t * s->dil_w;
+#endif
+                if (w < 0 || w >= s->W) continue;
+                double prod = (double)x[((n * s->C + c) * s->H + h) * s->W + w] *
+                              (double)wt[((k * s->C + c) * s->R + r) * s->S + t];
+                sum += prod;
+                abs_sum += fabs(prod);
+            }
+        }
+    *out = sum;
+    *mag = abs_sum;
+}
+
+typedef struct {
+    const float *x, *w, *bias;
+    double *y, *mag;
+    const oracle_shape *s;
+    int64_t P, Q, first, last;
+} f64_job_t;
+
+static void *run_f64_job(void *arg)
+{
+    f64_job_t *j = (f64_job_t *)arg;
+    const oracle_shape *s = j->s;
+    for (int64_t nk = j->first; nk < j->last; ++nk) {
+        int64_t n = nk / s->K, k = nk % s->K;
+        for (int64_t p = 0; p < j->P; ++p)
+            for (int64_t q = 0; q < j->Q; ++q) {
+                int64_t i = (nk * j->P + p) * j->Q + q;
+                f64_at(j->x, j->w, j->bias, s, n, k, p, q, &j->y[i], &j->mag[i]);
+            }
+    }
+    return NULL;
+}
+
+/* fp32 direct convolution in double.  x: NCHW float, w: KCRS float, bias: K
+ * floats or NULL; y and mag: NKPQ doubles (caller allocates N*K*P*Q each).
+ * Threaded over (n, k) pairs like oracle_conv2d_acc. */
+int oracle_conv2d_f64(const float *x, const float *w, const float *bias, double *y, double *mag,
+                      const oracle_shape *s, int nthreads)
+{
+    if (!x || !w || !y || !mag || !shape_ok(s)) return ORACLE_EINVAL;
+    int64_t P = oracle_out_extent(s->H, s->pad_h, s->dil_h, s->R, s->stride_h);
+    int64_t Q = oracle_out_extent(s->W, s->pad_w, s->dil_w, s->S, s->stride_w);
+    if (P <= 0 || Q <= 0) return ORACLE_OK;
+    int64_t pairs = s->N * s->K;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > pairs) nthreads = (int)pairs;
+    f64_job_t *jobs = (f64_job_t *)calloc((size_t)nthreads, sizeof(f64_job_t));
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tid) { free(jobs); free(tid); return ORACLE_ENOMEM; }
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = (f64_job_t){x, w, bias, y, mag, s, P, Q, pairs * i / nthreads, pairs * (i + 1) / nthreads};
+        if (i == 0) continue;
+        if (pthread_create(&tid[i], NULL, run_f64_job, &jobs[i]) != 0) { run_f64_job(&jobs[i]); tid[i] = 0; }
+    }
+    run_f64_job(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (tid[i]) pthread_join(tid[i], NULL);
+    free(jobs);
+    free(tid);
+    return ORACLE_OK;
+}
+
+/* fp32 direct convolution in double at rows (n, k, p, q) of pts. */
+int oracle_conv2d_f64_points(const float *x, const float *w, const float *bias, const oracle_shape *s,
+                             const int64_t *pts, int64_t npts, double *y, double *mag)
+{
+    if (!x || !w || !pts || !y || !mag || !shape_ok(s) || npts < 0) return ORACLE_EINVAL;
+    int64_t P = oracle_out_extent(s->H, s->pad_h, s->dil_h, s->R, s->stride_h);
+    int64_t Q = oracle_out_extent(s->W, s->pad_w, s->dil_w, s->S, s->stride_w);
+    for (int64_t i = 0; i < npts; ++i) {
+        int64_t n = pts[4 * i], k = pts[4 * i + 1], p = pts[4 * i + 2], q = pts[4 * i + 3];
+        if (n < 0 || n >= s->N || k < 0 || k >= s->K || p < 0 || p >= P || q < 0 || q >= Q) return ORACLE_EINVAL;
+        f64_at(x, w, bias, s, n, k, p, q, &y[i], &mag[i]);
+    }
     return ORACLE_OK;
 }
 

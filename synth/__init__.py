@@ -101,6 +101,57 @@ def normal_int8(seed: int, count: int, sigma: float) -> np.ndarray:
     return np.clip(np.rint(sigma * z), -128, 127).astype(np.int8)
 
 
+def uniform_f32(seed: int, count: int, lo: float, hi: float) -> np.ndarray:
+    """``count`` float32 values uniform on [lo, hi): lo + (hi - lo) * (u >> 40) / 2^24,
+    computed in double and rounded once to float32."""
+    u = Xoshiro256ss(seed).next_u64(count)
+    t = (u >> np.uint64(40)).astype(np.float64) * (1.0 / float(1 << 24))
+    return (lo + (hi - lo) * t).astype(np.float32)
+
+
+@dataclass(frozen=True)
+class F32Workload:
+    """The fp32 direct convolution of the kernel-benchmark trace (nn.Conv2d
+    on NCHW fp32): inputs uniform on [0, 1), weights and bias uniform on
+    [-b, b) with b = 1/sqrt(C*R*S) (nn.Conv2d's default initialisation bound)."""
+    name: str
+    N: int
+    C: int
+    H: int
+    W: int
+    K: int
+    R: int
+    S: int
+    pad: tuple
+    stride: tuple
+    dil: tuple
+    seed: int
+
+    def shape_tuple(self):
+        return (self.N, self.C, self.H, self.W, self.K, self.R, self.S, self.pad[0], self.pad[1],
+                self.stride[0], self.stride[1], self.dil[0], self.dil[1])
+
+    def bound(self) -> float:
+        return 1.0 / math.sqrt(self.C * self.R * self.S)
+
+    def inputs_nchw(self) -> np.ndarray:
+        return uniform_f32(self.seed, self.N * self.C * self.H * self.W, 0.0, 1.0).reshape(
+            self.N, self.C, self.H, self.W)
+
+    def weights_kcrs(self) -> np.ndarray:
+        b = self.bound()
+        return uniform_f32(self.seed + 1, self.K * self.C * self.R * self.S, -b, b).reshape(
+            self.K, self.C, self.R, self.S)
+
+    def bias(self) -> np.ndarray:
+        b = self.bound()
+        return uniform_f32(self.seed + 2, self.K, -b, b)
+
+
+# page 4's problem: batch 8, 32 -> 64 channels, 512 x 512, 5 x 9 kernel, pad (2, 4), dilation (2, 3)
+F32_WORKLOAD = F32Workload("f32_n8c32h512k64r5x9d2x3", 8, 32, 512, 512, 64, 5, 9, (2, 4), (1, 1), (2, 3), 20260200)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One convolution workload: shapes, value distribution, alpha and seeds.

@@ -297,4 +297,79 @@ def pin_channel_epilogue_reduces_to_alpha_only(orc):
         assert np.array_equal(orc.requantize_channels(acc, alpha), orc.requantize(acc, alpha).reshape(acc.shape))
 
 
+# --- fp32 direct convolution (page 4's nn.Conv2d), evaluated in double -------
+
+_F32_SHAPES = [(2, 3, 9, 11, 4, 3, 5, 1, 2, 1, 1, 1, 1),
+               (1, 2, 12, 30, 3, 5, 9, 2, 4, 1, 1, 2, 3),
+               (2, 4, 13, 9, 2, 3, 3, 1, 0, 2, 3, 1, 2),
+               (1, 5, 8, 8, 3, 2, 3, 0, 1, 3, 2, 3, 1)]
+
+
+def pin_f64_integer_data_matches_int_accumulators(orc):
+    """On integer-valued inputs every product and partial sum is an exact
+    integer in double, so y must equal the integer path's accumulators (which
+    are pinned to im2col, PyTorch and closed forms above) plus the bias."""
+    rng = np.random.default_rng(23)
+    for shape in _F32_SHAPES:
+        N, C, H, W, K, R, S = shape[:7]
+        x = rng.integers(-128, 128, size=(N, C, H, W)).astype(np.int8)
+        f = rng.integers(-128, 128, size=(K, C, R, S)).astype(np.int8)
+        b = rng.integers(-1000, 1000, size=K).astype(np.float32)
+        y, mag = orc.conv_f64(x.astype(np.float32), f.astype(np.float32), shape, bias=b, threads=2)
+        acc = orc.conv_acc(x, f, shape, threads=2)
+        assert np.array_equal(y, acc.astype(np.float64) + b.astype(np.float64)[None, :, None, None]), shape
+        assert np.all(mag >= np.abs(y))
+
+
+def pin_f64_matches_torch_conv2d(orc):
+    """Random fp32 data: PyTorch's CPU conv2d in float64 with bias agrees to
+    within double rounding of the magnitude sum."""
+    import torch
+    rng = np.random.default_rng(29)
+    for shape in _F32_SHAPES:
+        N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw = shape
+        x = rng.random((N, C, H, W)).astype(np.float32)
+        w = (rng.random((K, C, R, S)) * 2 - 1).astype(np.float32)
+        b = (rng.random(K) * 2 - 1).astype(np.float32)
+        want = torch.nn.functional.conv2d(torch.from_numpy(x.astype(np.float64)), torch.from_numpy(w.astype(np.float64)),
+                                          torch.from_numpy(b.astype(np.float64)), stride=(sh, sw), padding=(ph, pw),
+                                          dilation=(dh, dw)).numpy()
+        y, mag = orc.conv_f64(x, w, shape, bias=b, threads=2)
+        assert y.shape == want.shape, shape
+        assert np.all(np.abs(y - want) <= 1e-13 * mag + 1e-300), shape
+
+
+def pin_f64_bias_only_and_magnitudes(orc):
+    """Zero input: every output is its channel's bias and the magnitude is
+    |bias|.  Non-negative data: the magnitude sum equals the output."""
+    shape = (2, 3, 7, 6, 4, 3, 2, 1, 0, 1, 2, 2, 1)
+    N, C, H, W, K, R, S = shape[:7]
+    b = np.array([0.5, -1.25, 3.0, -0.0625], np.float32)
+    y, mag = orc.conv_f64(np.zeros((N, C, H, W), np.float32), np.ones((K, C, R, S), np.float32), shape, bias=b)
+    assert np.array_equal(y, np.broadcast_to(b.astype(np.float64)[None, :, None, None], y.shape))
+    assert np.array_equal(mag, np.abs(y))
+    rng = np.random.default_rng(31)
+    x = rng.random((N, C, H, W)).astype(np.float32)
+    w = rng.random((K, C, R, S)).astype(np.float32)
+    y, mag = orc.conv_f64(x, w, shape, bias=np.abs(b))
+    assert np.array_equal(y, mag)
+
+
+def pin_f64_page4_trace(orc):
+    """Page 4's hand trace of output[0,0,0,0] for its 5x9 dilated layer on
+    all-ones data: 4 in-bounds filter rows x 7 in-bounds columns x 32
+    channels, plus the bias."""
+    g = _page4()
+    d = dict(g["shape"])
+    d["N"], d["K"], d["H"], d["W"] = 1, 1, 40, 40
+    shape = _shape_of(d)
+    C, R, S = d["C"], d["R"], d["S"]
+    tr = g["trace_output_0000"]
+    rows_in = R - len(tr["rows_out_of_bounds"])
+    cols_in = S - tr["row1_columns_in_bounds_from"]
+    y, _ = orc.conv_f64_points(np.ones((1, C, 40, 40), np.float32), np.ones((1, C, R, S), np.float32), shape,
+                               np.array([[0, 0, 0, 0]]), bias=np.array([0.5], np.float32))
+    assert y[0] == C * rows_in * cols_in + 0.5
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -19,6 +19,8 @@ MUTATIONS = {
     9: "bias added before the per-channel scale",
     11: "per-channel scale indexed by the image",
     12: "fused multiply-add in the per-channel epilogue",
+    13: "bias ignored in the fp32 direct convolution",
+    14: "column dilation ignored in the fp32 direct convolution",
 }
 
 
