@@ -351,6 +351,124 @@ def run_ours(args, wl, rank, world):
     return result
 
 
+F32_METRIC = "fp32 direct conv TFLOP/s (kernel-benchmark trace layer, 1 GB300) and % of the fp32 SIMT roofline"
+
+
+def simt_fp32_peak(sms: int):
+    """fp32 FMA peak of the SIMT cores: SMs x 128 FMA lanes x 2 flops x the
+    maximum SM clock (MEASURED_PEAKS.json's sm_max_mhz, else 2070 MHz)."""
+    mhz, note = 2070.0, "nominal maximum SM clock 2070 MHz"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            mhz = float(json.load(fh)["sm_max_mhz"])
+            note = f"measured maximum SM clock {mhz:.0f} MHz"
+    except Exception:
+        pass
+    return sms * 128 * 2 * mhz * 1e6 / 1e12, f"{sms} SMs x 128 fp32 FMA lanes x 2 flops x {note}"
+
+
+def run_f32(args, rank, world):
+    """The fp32 direct convolution (i8c_conv2d_fprop_f32) on the trace's layer."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    wl = synth.F32_WORKLOAD
+    shape = wl.shape_tuple()
+    P, Q = ext.i8c_output_size(shape)
+    ops = 2 * wl.N * wl.K * P * Q * wl.C * wl.R * wl.S
+    xh = torch.from_numpy(wl.inputs_nchw())
+    wh = torch.from_numpy(wl.weights_kcrs())
+    bh = torch.from_numpy(wl.bias())
+    x, w, b = xh.cuda(), wh.cuda(), bh.cuda()
+    y = torch.empty((wl.N, wl.K, P, Q), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ext.i8c_conv2d_fprop_f32(x, w, b, y, shape, stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev) if (rank == 0 and not args.no_clocks) else None
+    if clocks:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    launches0 = ext.launch_count()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        ext.i8c_conv2d_fprop_f32(x, w, b, y, shape, stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = ext.launch_count() - launches0
+    total_ms = ev0.elapsed_time(ev1)
+    clock_rec = clocks.stop() if clocks else None
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / args.steps
+    value = world * ops / (ms * 1e-3) / 1e12
+    # end to end: pinned host inputs copied in, the call, the output copied back
+    xp, wp, bp = xh.pin_memory(), wh.pin_memory(), bh.pin_memory()
+    yp = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(xp, non_blocking=True)
+        w.copy_(wp, non_blocking=True)
+        b.copy_(bp, non_blocking=True)
+        ext.i8c_conv2d_fprop_f32(x, w, b, y, shape, stream)
+        yp.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak, peak_note = simt_fp32_peak(sms)
+    result = {
+        "metric": F32_METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded xoshiro256**: x uniform [0,1), w and "
+                                                    "bias uniform [-1/sqrt(C*R*S), 1/sqrt(C*R*S)))",
+        "config": {"workload": wl.name, "shape": dict(zip(
+            ["N", "C", "H", "W", "K", "R", "S", "pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w"], shape)),
+            "P": P, "Q": Q, "l2": "inputs 268 MB and outputs 516 MB, both larger than the 129 MiB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "alu", "achieved": round(ops / (ms * 1e-3) / 1e12, 2), "peak": round(peak, 1),
+                     "unit": "TFLOP/s", "frac": round(ops / (ms * 1e-3) / 1e12 / peak, 4),
+                     "traffic": dram_traffic(wl.name), "kernel": "conv_f32_direct_kernel",
+                     "note": f"2*N*K*P*Q*C*R*S flops per call / CUDA-event time per call (weight transpose + "
+                             f"convolution); peak {peak_note}"},
+        "e2e": {"value": round(ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 6),
+                "h2d_bytes_per_step": 4 * (xh.numel() + wh.numel() + bh.numel()),
+                "d2h_bytes_per_step": 4 * y.numel(), "path": "pinned host copies + i8c_conv2d_fprop_f32"},
+        "gpu_launches": launches,
+    }
+    if clock_rec is not None:
+        result["clocks"] = clock_rec
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        orc = oracle.Oracle()
+        xs, ws, bs = xh.numpy()[:1], wh.numpy(), bh.numpy()
+        cores = os.cpu_count() or 1
+        k = 1
+        while True:
+            sshape = (1,) + tuple(shape[1:4]) + (k,) + tuple(shape[5:])
+            t0 = time.perf_counter()
+            orc.conv_f64(xs, ws[:k], sshape, bias=bs[:k], threads=cores)
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_budget / 4 or k >= wl.K:
+                break
+            k = min(wl.K, k * 4 if dt < args.cpu_budget / 16 else k * 2)
+        s_ops = 2 * k * P * Q * wl.C * wl.R * wl.S
+        result["cpu_baseline"] = {"value": round(s_ops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                                  "kind": "oracle", "sample": f"1 of {wl.N} images, {k} of {wl.K} output channels "
+                                                              f"(double precision)", "seconds": round(dt, 2)}
+    return result
+
+
 def bench_one_quick(wl, steps=50, warmup=5):
     """Device time per step and conv-kernel roofline fraction for one workload."""
     import torch
@@ -430,7 +548,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS_BY_NAME))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(synth.WORKLOADS_BY_NAME) + [synth.F32_WORKLOAD.name])
     ap.add_argument("--all", action="store_true", help="also time every workload (quick, device time only)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps one by one")
@@ -441,6 +560,21 @@ def main():
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.workload == synth.F32_WORKLOAD.name:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the fp32 direct convolution has no reference "
+                                                                  "arm; its oracle is timed in cpu_baseline"}))
+            return
+        if world > 1:
+            import torch
+            torch.distributed.init_process_group("nccl")
+        res = run_f32(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+        return
     wl = synth.WORKLOADS_BY_NAME[args.workload]
     if args.impl == "reference":
         res = run_reference(args, wl, rank, world)

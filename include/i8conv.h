@@ -333,6 +333,27 @@ i8c_status i8c_pack_kcrs_to_cxrskx32(const int8_t* src, int8_t* dst, int32_t K, 
 i8c_status i8c_unpack_cxrskx32_to_kcrs(const int8_t* src, int8_t* dst, int32_t K, int32_t C, int32_t R, int32_t S,
                                        cudaStream_t stream);
 
+/* The fp32 direct convolution of the POPCORNBENCH kernel-benchmark trace
+ * (problem l1_p80, nn.Conv2d on fp32 tensors; the trace's checker compares
+ * with the framework's convolution at atol = rtol = 1e-4):
+ *     y[n][k][p][q] = bias[k] + sum_{c,r,s} x[n][c][h][w] * w[k][c][r][s]
+ * with h, w, P and Q as for the int8 convolution (zero padding, per-axis
+ * stride and dilation).  Computed on the SIMT cores in IEEE fp32: one fused
+ * multiply-add per product in the order (c, r, s), then the bias, so every
+ * output is within the fp32 summation bound of the exact sum.
+ *   x: NCHW fp32 [N][C][H][W]; w: KCRS fp32 [K][C][R][S]; bias: K floats or
+ *   NULL (no bias); y: NCHW fp32 [N][K][P][Q], written.  All DEVICE memory,
+ *   4-byte aligned, owned by the caller; any C and K >= 1.
+ * The first call for a filter size on a device allocates a transposed copy of
+ * the weight there (cudaMalloc; kept until exit); calls with the same filter
+ * size share that copy and must be serialised on one stream.
+ * Errors: I8C_ERR_INVALID_ARG (null pointer, bad sizes), I8C_ERR_MISALIGNED,
+ * I8C_ERR_UNSUPPORTED (empty output, N > 65535, or a filter whose input
+ * region and weights per input channel exceed the kernel's shared memory),
+ * I8C_ERR_OVERFLOW_RISK (an image over 2^31 elements), I8C_ERR_NO_DEVICE. */
+i8c_status i8c_conv2d_fprop_f32(const float* x, const float* w, const float* bias, float* y,
+                                const i8c_conv_shape* shape, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* i8c_status_string(i8c_status status);
 

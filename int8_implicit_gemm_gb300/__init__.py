@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "i8c_conv2d_fprop": [P, P, P, S, F, P],
         "i8c_conv2d_fprop_acc": [P, P, P, S, P],
         "i8c_conv2d_fprop_noalloc": [P, P, P, S, F, P],
+        "i8c_conv2d_fprop_f32": [P, P, P, P, S, P],
         "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
         "i8c_plan_run": [P, P, P, P, F, P],
         "i8c_plan_run_ex": [P, P, P, P, F, ctypes.POINTER(Epilogue), P],
@@ -220,6 +221,23 @@ def i8c_plan_autotune(x, f, y, shape, alpha: float, iters: int = 10, stream=None
         return {name: getattr(o, name) for name, _ in Options._fields_}
 
     return opts(best), best_us.value, [(opts(e.options), e.status, e.us) for e in entries[:n.value]]
+
+
+def i8c_conv2d_fprop_f32(x, w, bias, y, shape, stream=None) -> None:
+    """fp32 direct convolution (NCHW / KCRS, optional bias) on the SIMT cores."""
+    _check(lib.i8c_conv2d_fprop_f32(_ptr(x), _ptr(w), None if bias is None else _ptr(bias), _ptr(y),
+                                    ctypes.byref(ConvShape.of(shape)), _stream(stream)), "i8c_conv2d_fprop_f32")
+
+
+def conv2d_fprop_f32(x, w, shape, bias=None, out=None, stream=None):
+    """Convenience wrapper: allocate the NCHW fp32 output with torch and run."""
+    import torch
+    s = ConvShape.of(shape)
+    P, Q = i8c_output_size(s)
+    if out is None:
+        out = torch.empty((s.N, s.K, P, Q), dtype=torch.float32, device=x.device)
+    i8c_conv2d_fprop_f32(x, w, bias, out, s, stream)
+    return out
 
 
 def i8c_pack_nchw_to_ncxhwx32(src, dst, N, C, H, W, stream=None) -> None:
