@@ -469,6 +469,38 @@ def run_f32(args, rank, world):
     return result
 
 
+def run_f32_reference(args, rank, world):
+    """The double-precision oracle of the fp32 direct convolution as the
+    reference arm: each step is a bounded sample (the first 64 input rows of
+    one image, 16 of the 64 output channels), timed on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    wl = synth.F32_WORKLOAD
+    shape = wl.shape_tuple()
+    orc = oracle.Oracle()
+    k, rows = 16, 64
+    x, w, b = wl.inputs_nchw()[:1, :, :rows], wl.weights_kcrs()[:k], wl.bias()[:k]
+    sshape = (1, shape[1], rows, shape[3], k) + tuple(shape[5:])
+    P, Q = orc.out_size(sshape)
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        orc.conv_f64(x, w, sshape, bias=b, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.conv_f64(x, w, sshape, bias=b, threads=cores)
+    dt = time.perf_counter() - t0
+    v = 2 * k * P * Q * wl.C * wl.R * wl.S * args.steps / dt / 1e12
+    sample = f"first {rows} input rows of 1 of {wl.N} images, {k} of {wl.K} output channels per step (double precision)"
+    return {"impl": "reference", "metric": F32_METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def bench_one_quick(wl, steps=50, warmup=5):
     """Device time per step and conv-kernel roofline fraction for one workload."""
     import torch
@@ -562,8 +594,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.workload == synth.F32_WORKLOAD.name:
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the fp32 direct convolution has no reference "
-                                                                  "arm; its oracle is timed in cpu_baseline"}))
+            res = run_f32_reference(args, rank, world)
+            if res is not None:
+                print(json.dumps(res), flush=True)
             return
         if world > 1:
             import torch
