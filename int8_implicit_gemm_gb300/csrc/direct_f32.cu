@@ -18,7 +18,8 @@
 //   - the weights of its 64 channels, R*S rows of 64 floats per channel, from
 //     a copy of the weight transposed once per call to [C][R*S][Kpad] (read
 //     as two broadcast 16-byte loads per tap).
-// One tap is 8 input loads, 2 weight loads and 64 FMAs per thread.
+// One tap is 8 input loads, 2 weight loads and 32 paired FMAs (64 FMAs) per
+// thread.
 #include <cuda_runtime.h>
 
 #include <array>
@@ -112,11 +113,13 @@ __global__ void __launch_bounds__(kThreads, 2) conv_f32_direct_kernel(const F32P
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
 
-  float acc[8][kTileP];
+  // acc[k][j]: channel k, output rows 2j and 2j + 1 (one packed pair, so that
+  // one paired fp32 FMA instruction updates both)
+  float2 acc[8][kTileP / 2];
 #pragma unroll
   for (int k = 0; k < 8; ++k)
 #pragma unroll
-    for (int i = 0; i < kTileP; ++i) acc[k][i] = 0.0f;
+    for (int j = 0; j < kTileP / 2; ++j) acc[k][j] = make_float2(0.0f, 0.0f);
 
   const int nst = (p.C + p.CS - 1) / p.CS;
   const int row_step = p.sh * p.TW;  // between the input rows of consecutive output rows
@@ -140,13 +143,17 @@ __global__ void __launch_bounds__(kThreads, 2) conv_f32_direct_kernel(const F32P
           const float4 wb = *reinterpret_cast<const float4*>(wrow + s * kTileK + 4);
           const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
           const float* xc = irow + s * p.dw;
-          float xv[kTileP];
+          float2 xv[kTileP / 2];
 #pragma unroll
-          for (int i = 0; i < kTileP; ++i) xv[i] = xc[i * row_step];
+          for (int j = 0; j < kTileP / 2; ++j) xv[j] = make_float2(xc[2 * j * row_step], xc[(2 * j + 1) * row_step]);
+          // each lane of the paired FMA is one IEEE fp32 fused multiply-add
+          // (round to nearest), as __fmaf_rn on each row would be
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < 8; ++k) {
+            const float2 w2 = make_float2(wv[k], wv[k]);
 #pragma unroll
-            for (int i = 0; i < kTileP; ++i) acc[k][i] = __fmaf_rn(wv[k], xv[i], acc[k][i]);
+            for (int j = 0; j < kTileP / 2; ++j) acc[k][j] = __ffma2_rn(w2, xv[j], acc[k][j]);
+          }
         }
       }
     }
@@ -164,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 2) conv_f32_direct_kernel(const F32P
 #pragma unroll
     for (int i = 0; i < kTileP; ++i) {
       const int pp = p0 + i;
-      if (pp < p.P) yk[static_cast<int64_t>(pp) * p.Q + q] = __fadd_rn(acc[k][i], b);
+      const float a = (i & 1) ? acc[k][i >> 1].y : acc[k][i >> 1].x;
+      if (pp < p.P) yk[static_cast<int64_t>(pp) * p.Q + q] = __fadd_rn(a, b);
     }
   }
 }
