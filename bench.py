@@ -64,6 +64,23 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(ms: float, world: int, device: str = "cuda") -> float:
+    """The job's time: every rank times the same K steps between barriers,
+    and the slowest rank sets the pace (all-reduce MAX; gloo on CPU tensors
+    works the same way as NCCL on device tensors)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the units all replicas processed per second."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def dram_traffic(workload: str):
     """Per-launch DRAM bytes of the convolution kernel from the committed ncu
     summary, if it was taken on the current kernel sources."""
@@ -269,13 +286,9 @@ def run_ours(args, wl, rank, world):
     if st != 0:
         raise RuntimeError(f"device status {ext.status_string(st)}")
 
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
-    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    value = job_rate(ops, world, ms_per_step) / 1e12
 
     # end to end through the C-ABI on pinned host buffers: H2D of x and f,
     # the run, D2H of y, every step
@@ -404,12 +417,9 @@ def run_f32(args, rank, world):
     launches = ext.launch_count() - launches0
     total_ms = ev0.elapsed_time(ev1)
     clock_rec = clocks.stop() if clocks else None
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world)
     ms = total_ms / args.steps
-    value = world * ops / (ms * 1e-3) / 1e12
+    value = job_rate(ops, world, ms) / 1e12
     # end to end: pinned host inputs copied in, the call, the output copied back
     xp, wp, bp = xh.pin_memory(), wh.pin_memory(), bh.pin_memory()
     yp = torch.empty(y.shape, dtype=torch.float32).pin_memory()
