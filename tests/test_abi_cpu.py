@@ -98,6 +98,76 @@ def test_autotune_argument_checks(ext):
         ext.I8C_ERR_UNSUPPORTED                                                  # C not a multiple of 32
 
 
+@pytest.mark.parametrize("opts", [
+    dict(block_n=48), dict(block_n=512), dict(num_ctas=-1), dict(max_chunk_slices=33), dict(wait_timeout_us=-5),
+    dict(timing_events=70000), dict(kernel_variant=6), dict(halo_loads=3), dict(tail_split=4), dict(tile_shape=3),
+    dict(fused_filter=2), dict(tile_px=20), dict(tile_px=272), dict(tile_px=8), dict(filter_run=33),
+], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
+def test_plan_options_rejected_on_the_host(ext, opts):
+    """Out-of-range plan options are refused before any device is touched."""
+    fields = {n: 0 for n, _ in ext.Options._fields_}
+    fields.update(opts)
+    o = ext.Options(**fields)
+    h = ctypes.c_void_p()
+    shape = ctypes.byref(ext.ConvShape.of((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1)))
+    assert ext.lib.i8c_plan_create(shape, ctypes.byref(o), ctypes.byref(h)) == ext.I8C_ERR_INVALID_ARG
+    assert not h.value
+
+
+def test_f32_direct_argument_checks(ext):
+    """The fp32 entry point's host-side checks: null, misaligned, invalid and
+    unsupported shapes; a valid call without a GPU fails with a device error."""
+    buf = ctypes.create_string_buffer(64)
+    a = (ctypes.addressof(buf) + 15) & ~15
+    f = ext.lib.i8c_conv2d_fprop_f32
+    good = ctypes.byref(ext.ConvShape.of((1, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1)))
+    assert f(None, a, None, a, good, None) == ext.I8C_ERR_INVALID_ARG
+    assert f(a, a, None, a, None, None) == ext.I8C_ERR_INVALID_ARG
+    assert f(a + 2, a, None, a, good, None) == ext.I8C_ERR_MISALIGNED
+    assert f(a, a, a + 1, a, good, None) == ext.I8C_ERR_MISALIGNED            # bias misaligned
+    assert f(a, a, None, a, ctypes.byref(ext.ConvShape.of((1, 3, 2, 2, 4, 5, 5, 0, 0, 1, 1, 1, 1))),
+             None) == ext.I8C_ERR_UNSUPPORTED                                    # empty output
+    assert f(a, a, None, a, ctypes.byref(ext.ConvShape.of((1, 3, 8, 8, 4, 3, 3, 1, 1, 0, 1, 1, 1))),
+             None) == ext.I8C_ERR_INVALID_ARG                                    # zero stride
+    assert f(a, a, None, a, ctypes.byref(ext.ConvShape.of((70000, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 1, 1))),
+             None) == ext.I8C_ERR_UNSUPPORTED                                    # batch past the grid's y extent
+    import torch
+    if not torch.cuda.is_available():
+        assert f(a, a, None, a, good, None) in (ext.I8C_ERR_NO_DEVICE, ext.I8C_ERR_CUDA)
+
+
+def test_noalloc_argument_checks(ext):
+    """The no-allocation entry point refuses bad arguments on the host."""
+    buf = ctypes.create_string_buffer(64)
+    a = (ctypes.addressof(buf) + 15) & ~15
+    f = ext.lib.i8c_conv2d_fprop_noalloc
+    good = ctypes.byref(ext.ConvShape.of((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1)))
+    assert f(None, a, a, good, ctypes.c_float(1.0), None) == ext.I8C_ERR_INVALID_ARG
+    assert f(a + 1, a, a, good, ctypes.c_float(1.0), None) == ext.I8C_ERR_MISALIGNED
+    assert f(a, a, a, ctypes.byref(ext.ConvShape.of((1, 48, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1))),
+             ctypes.c_float(1.0), None) == ext.I8C_ERR_UNSUPPORTED
+
+
+def test_build_flavour_stamp(tmp_path, monkeypatch):
+    """The build script rebuilds when the requested flavour (release or
+    pipeline trace) differs from the one the library was built with."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bl", os.path.join(ROOT, "int8_implicit_gemm_gb300", "build_lib.py"))
+    bl = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bl)
+    lib = tmp_path / "libi8conv.so"
+    stamp = tmp_path / "flavour"
+    lib.write_bytes(b"x")
+    monkeypatch.setattr(bl, "LIB", str(lib))
+    monkeypatch.setattr(bl, "STAMP", str(stamp))
+    monkeypatch.setattr(bl, "_deps", lambda: [])
+    assert not bl.up_to_date(False)                   # no stamp yet
+    stamp.write_text("release")
+    assert bl.up_to_date(False) and not bl.up_to_date(True)
+    stamp.write_text("pipeline-trace")
+    assert bl.up_to_date(True) and not bl.up_to_date(False)
+
+
 @pytest.mark.parametrize("ctype,cls_name", [("i8c_conv_shape", "ConvShape"), ("i8c_options", "Options"),
                                             ("i8c_plan_info", "PlanInfo"), ("i8c_epilogue", "Epilogue"),
                                             ("i8c_tune_entry", "TuneEntry")])
