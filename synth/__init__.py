@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the INT8 NCxHWx<32> convolution workloads.
+"""Seeded synthetic inputs for the INT8 NCxHWx<32> convolution workloads and
+the fp32 direct-convolution workload.
 
 This module is shared by the CPU oracle's tests and by the GPU path's tests and
 benchmark. It holds only random-number generation and the workload table; it

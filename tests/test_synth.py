@@ -56,3 +56,22 @@ def test_workloads_table():
     assert len(synth.WORKLOADS) == 5
     for w in synth.WORKLOADS:
         assert w.C % 32 == 0 and w.K % 32 == 0
+
+
+def test_uniform_f32_mapping_and_range():
+    """uniform_f32 maps the top 24 bits of each draw onto [lo, hi) exactly as
+    its docstring states, is deterministic per seed, and never reaches hi."""
+    u = synth.Xoshiro256ss(77).next_u64(4096)
+    want = (-0.5 + 1.5 * ((u >> np.uint64(40)).astype(np.float64) / float(1 << 24))).astype(np.float32)
+    got = synth.uniform_f32(77, 4096, -0.5, 1.0)
+    assert got.dtype == np.float32 and np.array_equal(got, want)
+    assert np.array_equal(got, synth.uniform_f32(77, 4096, -0.5, 1.0))
+    assert got.min() >= -0.5 and got.max() < 1.0
+
+
+def test_f32_workload_is_the_trace_layer():
+    w = synth.F32_WORKLOAD
+    assert w.shape_tuple() == (8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3)
+    assert abs(w.bound() - 1.0 / np.sqrt(32 * 5 * 9)) < 1e-15
+    b = w.bias()
+    assert b.shape == (64,) and np.all(np.abs(b) <= w.bound())
