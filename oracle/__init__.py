@@ -1,7 +1,7 @@
 """CPU oracle for the INT8 NCxHWx<32> Conv2d forward pass -- TEST INFRASTRUCTURE.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The product library never calls it and
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline and
+reference legs of ``bench.py`` may import this package.  The product library never calls it and
 shares no code with it: the convolution, the epilogue and the layout
 transforms here are written from their definitions, independently of the
 CUDA kernels they check.

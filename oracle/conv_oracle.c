@@ -4,7 +4,8 @@
  * This file is the plain, slow, obviously correct definition that the GPU
  * implicit-GEMM kernels are checked against.  It shares no code with the
  * GPU path.  Only the tests, the package's smoke check and the benchmark's
- * CPU-baseline leg may load it; the product path never calls it.
+ * CPU-baseline and reference legs may load it; the product path never
+ * calls it.
  *
  * What it computes (written out from the pages, not from any listing):
  *  - Output extent per axis (kernel-benchmark trace, page 4, first analysis
