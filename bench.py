@@ -578,7 +578,9 @@ def run_reference(args, wl, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8 (int64 accumulation)",
-            "data": "synthetic", "config": {"workload": wl.name},
+            "data": "synthetic", "config": {"workload": wl.name, "shape": dict(zip(
+                ["N", "C", "H", "W", "K", "R", "S", "pad_h", "pad_w", "stride_h", "stride_w", "dil_h", "dil_w"],
+                wl.shape_tuple())), "P": P, "Q": Q, "alpha": wl.alpha},
             "cpu_baseline": {"value": round(v, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(v, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
