@@ -54,13 +54,21 @@ def tensor_peak():
         return FALLBACK_TENSOR_TFLOPS, "of fallback (1.9 PFLOP/s bf16; fp16 at the same nominal rate)"
 
 
-def kernel_source_digest() -> str:
+F32_SOURCES = ("direct_f32.cu",)  # the fp32 direct convolution's kernel source
+
+
+def kernel_source_digest(workload: str | None = None) -> str:
+    """Digest of the kernel sources a workload's traffic figure depends on:
+    the fp32 direct convolution's own file for the fp32 workload, every other
+    source for the int8 workloads."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int8_implicit_gemm_gb300", "csrc")
+    f32 = workload == synth.F32_WORKLOAD.name
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(fh.read())
+        if not name.endswith((".cu", ".cuh", ".h")) or (name in F32_SOURCES) != f32:
+            continue
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -82,7 +90,7 @@ def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
 
 
 def dram_traffic(workload: str):
-    """Per-launch DRAM bytes of the convolution kernel from the committed ncu
+    """Per-launch DRAM bytes of the workload's kernel from the committed ncu
     summary, if it was taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "conv_fprop_dram_traffic.json")
     try:
@@ -90,10 +98,10 @@ def dram_traffic(workload: str):
             d = json.load(fh)
     except Exception:
         return None
-    if d.get("kernel_source_digest") != kernel_source_digest():
-        return None
     entry = d.get("workloads", {}).get(workload)
-    return None if entry is None else entry.get("bytes_per_launch")
+    if entry is None or entry.get("source_digest") != kernel_source_digest(workload):
+        return None
+    return entry.get("bytes_per_launch")
 
 
 class ClockSampler:
