@@ -34,11 +34,20 @@ def _data(shape, seed):
     return x, w, bias
 
 
+def _page4_tolerance():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "page4_dilated_conv.json")) as fh:
+        t = json.load(fh)["checker_tolerance"]
+    return t["atol"], t["rtol"]
+
+
 def _check(y, ref, mag, terms):
     orc = oracle.Oracle
     diff = np.abs(y.astype(np.float64) - ref)
     assert np.all(diff <= orc.f32_error_bound(mag, terms)), float(np.max(diff))
-    assert np.all(diff <= 1e-4 + 1e-4 * np.abs(ref))
+    atol, rtol = _page4_tolerance()
+    assert np.all(diff <= atol + rtol * np.abs(ref))
 
 
 @pytest.mark.parametrize("with_bias", [True, False], ids=["bias", "no-bias"])
