@@ -1,8 +1,9 @@
 """GPU parity of the fp32 direct convolution (the kernel-benchmark trace's
 nn.Conv2d) against the double-precision oracle.
 
-Two bars, both written here: the trace's own checker tolerance, |y - ref| <=
-1e-4 + 1e-4 * |ref|, and the rigorous fp32 summation bound, |y - ref| <=
+Two bars: the trace's own checker tolerance, |y - ref| <= 1e-4 + 1e-4 * |ref|
+(read from the page-4 golden fixture, with its citation), and the rigorous
+fp32 summation bound, |y - ref| <=
 gamma_{C*R*S+1} * (|bias| + sum |x * w|) with unit roundoff 2^-24, which holds
 for any order of fp32 additions and fused multiply-adds and is far tighter on
 small sums.
