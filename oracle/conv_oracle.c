@@ -268,14 +268,23 @@ static void f64_at(const float *x, const float *wt, const float *bias, const ora
 {
     double sum = 0.0, abs_sum = 0.0;
     if (bias) {
-#if ORACLE_MUTATION != 13
-        sum = (double)bias[k];                 /* (mutation 13 plants: bias ignored) */
+#if ORACLE_MUTATION == 16
+        const int64_t kb = n % s->K;           /* planted: bias indexed by the image */
+#else
+        const int64_t kb = k;
 #endif
-        abs_sum = fabs((double)bias[k]);
+#if ORACLE_MUTATION != 13
+        sum = (double)bias[kb];                /* (mutation 13 plants: bias ignored) */
+#endif
+        abs_sum = fabs((double)bias[kb]);
     }
     for (int64_t c = 0; c < s->C; ++c)
         for (int64_t r = 0; r < s->R; ++r) {
+#if ORACLE_MUTATION == 15
+            int64_t h = p - s->pad_h + r * s->dil_h;                   /* planted: row stride ignored */
+#else
             int64_t h = p * s->stride_h - s->pad_h + r * s->dil_h;
+#endif
             if (h < 0 || h >= s->H) continue;
             for (int64_t t = 0; t < s->S; ++t) {
 #if ORACLE_MUTATION == 14

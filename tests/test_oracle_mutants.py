@@ -21,6 +21,8 @@ MUTATIONS = {
     12: "fused multiply-add in the per-channel epilogue",
     13: "bias ignored in the fp32 direct convolution",
     14: "column dilation ignored in the fp32 direct convolution",
+    15: "row stride ignored in the fp32 direct convolution",
+    16: "bias indexed by the image in the fp32 direct convolution",
 }
 
 
