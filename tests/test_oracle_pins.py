@@ -27,3 +27,19 @@ def test_points_match_full(orc):
     N, K, P, Q = acc.shape
     pts = np.array([(n, k, p, q) for n in range(N) for k in range(K) for p in range(P) for q in range(Q)])
     assert np.array_equal(orc.conv_acc_points(x, f, shape, pts), acc.reshape(-1))
+
+
+def test_f64_points_match_full(orc):
+    """The point-wise fp32-path entry computes the same values (and magnitude
+    sums) as the full convolution."""
+    import numpy as np
+    rng = np.random.default_rng(6)
+    shape = (2, 3, 11, 9, 4, 3, 2, 1, 1, 2, 1, 1, 2)
+    x = rng.random((2, 3, 11, 9)).astype(np.float32)
+    w = (rng.random((4, 3, 3, 2)) - 0.5).astype(np.float32)
+    b = (rng.random(4) - 0.5).astype(np.float32)
+    y, mag = orc.conv_f64(x, w, shape, bias=b)
+    N, K, P, Q = y.shape
+    pts = np.array([(n, k, p, q) for n in range(N) for k in range(K) for p in range(P) for q in range(Q)])
+    yp, mp = orc.conv_f64_points(x, w, shape, pts, bias=b)
+    assert np.array_equal(yp, y.reshape(-1)) and np.array_equal(mp, mag.reshape(-1))
