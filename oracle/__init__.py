@@ -168,13 +168,16 @@ class Oracle:
             raise ValueError(f"oracle_conv2d_f64_points failed ({rc})")
         return y, mag
 
-    @staticmethod
-    def f32_error_bound(mag, terms: int):
-        """Largest difference between the exact sum and any fp32 recursive
-        evaluation of ``terms`` products (plus the bias) whose magnitude sum is
-        ``mag``: gamma_{terms+1} * mag with unit roundoff 2^-24."""
-        u = 2.0 ** -24
-        n = terms + 1
+    def f32_error_bound(self, mag, terms: int):
+        """Largest difference between the exact sum and any fp32 evaluation of
+        a dot product of ``terms`` products plus the bias, in any order, whose
+        magnitude sum is ``mag``: gamma_{terms+1} * mag, gamma_n = n*u/(1-n*u)
+        with the single-precision unit roundoff u = 2^-24 (the standard bound
+        for a dot product whose products and sums are each rounded once; a
+        fused multiply-add only rounds less).  Mutations 17 and 18 (planted
+        mistakes for the pin test) use u = 2^-23 and gamma_terms."""
+        u = 2.0 ** -23 if self.mutation == 17 else 2.0 ** -24
+        n = terms if self.mutation == 18 else terms + 1
         return (n * u / (1.0 - n * u)) * np.asarray(mag, dtype=np.float64)
 
     # -- epilogue (page 1: LinearCombinationClamp, alpha only) -------------

@@ -372,4 +372,32 @@ def pin_f64_page4_trace(orc):
     assert y[0] == C * rows_in * cols_in + 0.5
 
 
+def pin_f32_error_bound_worked_values(orc):
+    """gamma_n = n*u/(1 - n*u) with u = 2^-24, worked by hand: one product plus
+    the bias (n = 2) gives 2^-23/(1 - 2^-23) = 1/(2^23 - 1) = 1/8388607; two
+    products plus the bias (n = 3) give 3*2^-24/(1 - 3*2^-24) = 3/16777213."""
+    assert orc.f32_error_bound(1.0, 1) == 1.0 / 8388607.0
+    assert orc.f32_error_bound(1.0, 2) == 3.0 / 16777213.0
+    assert orc.f32_error_bound(0.0, 1440) == 0.0
+
+
+def pin_f32_error_bound_attained(orc):
+    """The bound is nearly attained, so it cannot be loose by a constant
+    factor: summing 1 and then m addends of 2^-24 in single precision loses
+    every addend (1 + 2^-24 lies halfway between 1 and its successor 1 + 2^-23
+    and ties to the even 1), an error of m*2^-24 on m + 1 summands of
+    magnitude 1 + m*2^-24, while gamma_{m+1} times that magnitude is only
+    (m+1)/m times as large, to first order in u."""
+    for m in (1, 7, 100):
+        s = np.float32(0.0)
+        for v in [np.float32(1.0)] + [np.float32(2.0 ** -24)] * m:
+            s = np.float32(s + v)
+        assert s == np.float32(1.0)
+        exact = 1.0 + m * 2.0 ** -24
+        err = exact - float(s)
+        bound = float(orc.f32_error_bound(exact, m))   # m products plus the bias: m + 1 summands
+        assert err <= bound, (m, err, bound)
+        assert err >= bound * m / (m + 1) * (1.0 - 1e-4), (m, err, bound)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

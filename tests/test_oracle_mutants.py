@@ -23,6 +23,8 @@ MUTATIONS = {
     14: "column dilation ignored in the fp32 direct convolution",
     15: "row stride ignored in the fp32 direct convolution",
     16: "bias indexed by the image in the fp32 direct convolution",
+    17: "fp32 error bound with the unit roundoff 2^-23",
+    18: "fp32 error bound gamma_n with n the product count (bias not counted)",
 }
 
 
