@@ -30,8 +30,9 @@
  *     immediately; results are valid once the stream reaches that point.
  *   - No entry point throws; each returns an i8c_status.  Argument errors are
  *     detected on the host before anything is enqueued.  Errors raised while a
- *     kernel runs (a bounded wait that ran out) are recorded in a per-plan
- *     device status word read by i8c_plan_status().
+ *     kernel runs (a bounded wait that ran out) are recorded in a device
+ *     status word: read per plan by i8c_plan_status(), and for the checked
+ *     one-shot calls by i8c_last_device_status().
  *   - There is no CPU fallback: without a usable CUDA device the calls fail
  *     with I8C_ERR_CUDA / I8C_ERR_NO_DEVICE.
  */
@@ -71,7 +72,9 @@ typedef struct {
   int32_t num_ctas;          /* persistent CTAs: 0 = one per SM                                */
   int32_t max_chunk_slices;  /* K-slices (32 channels each) per exact fp32 chunk: 0 = 32      */
   int32_t wait_timeout_us;   /* device-side bounded waits: 0 = 2,000,000 us                     */
-  int32_t host_staging;      /* 1 = allocate device staging buffers for i8c_plan_run_host     */
+  int32_t host_staging;      /* 1 = allocate device staging buffers for i8c_plan_run_host,
+                                2 = two staging sets and copy streams, for
+                                i8c_plan_run_host_pipelined as well                        */
   int32_t debug_flags;       /* test hooks, see I8C_DEBUG_*; 0 in production                  */
   int32_t timing_events;     /* > 0: bracket each convolution kernel with CUDA events (keeps
                                 the last timing_events launches) for i8c_plan_kernel_time;
@@ -176,6 +179,52 @@ typedef struct {
                                 whole-tile units, every stage fits)           */
 } i8c_plan_info;
 
+/* Shared- and tensor-memory layout of a plan's kernel, as the kernel will
+ * use it: the numbers a host-side bounds check needs to show that every
+ * matrix descriptor, TMA box and producer store stays inside its region.
+ * Byte offsets are relative to the CTA's 1024-byte-aligned shared-memory
+ * base (smem_bytes includes the 1024 bytes of slack for that alignment). */
+typedef struct {
+  int32_t kernel_variant;      /* as in i8c_plan_info                                  */
+  int32_t cta_group;           /* CTAs per MMA tile (2: a CTA pair)                    */
+  int32_t block_n;             /* output channels per tile (variants 4, 5: 128 per CTA) */
+  int32_t smem_bytes;          /* dynamic shared memory requested per CTA              */
+  int32_t tmem_cols;           /* tensor-memory columns allocated per CTA              */
+  int32_t chunk_slices;        /* K-slices per exact fp32 chunk                        */
+  int32_t num_chunks;
+  /* halo and transposed-tile kernels (variants 2-5; 0 for the gather kernel) */
+  int32_t flat_tiles;          /* 1: tiles of consecutive padded-row pixels            */
+  int32_t tile_px;             /* flat tiles: output pixels per CTA and tile            */
+  int32_t halo_rows, halo_cw;  /* halo rows; positions per halo row (flat: padded W)   */
+  int32_t positions;           /* halo positions per channel block                     */
+  int32_t plane_bytes;         /* one 8-channel fp16 plane of the halo                 */
+  int32_t halo_bytes;          /* one halo stage: 4 planes                             */
+  int32_t halo_stages;
+  int32_t off_staging, staging_slots, staging_bytes;  /* int8 staging ring (may be empty) */
+  int32_t off_filter;          /* first filter stage                                   */
+  int32_t filter_stages;
+  int32_t filter_run;          /* K-slices per filter stage                            */
+  int32_t filter_stage_bytes;  /* filter_run x filter rows per CTA x 64 bytes          */
+  int32_t off_out;             /* transposed tiles: the epilogue's output staging rows */
+  int32_t off_bar, bar_bytes;  /* mbarriers and the CTA's control words                */
+  int32_t phase_off[9];        /* halo: first position of column phase f, f <= stride_w */
+  /* per-tap gather kernel (variant 1; 0 otherwise) */
+  int32_t gather_stages, gather_off_a, gather_stage_a, gather_off_b, gather_stage_b;
+  int32_t gather_off_staging, gather_staging_slots, gather_staging_bytes, gather_off_bar;
+} i8c_layout;
+
+/* The layout i8c_plan_create would give `shape` with `opts` (may be NULL) on
+ * a GPU of `num_sms` SMs, computed on the host alone: no CUDA call is made,
+ * so it works without a GPU (CTA pairs are assumed to fit one per two SMs,
+ * which changes only the grid size, not the layout).  Errors as for
+ * i8c_plan_create's argument and shape checks, and I8C_ERR_UNSUPPORTED when
+ * a forced kernel form does not fit. */
+i8c_status i8c_plan_layout(const i8c_conv_shape* shape, const i8c_options* opts, int32_t num_sms,
+                           i8c_layout* out);
+
+/* The same layout for an existing plan. */
+i8c_status i8c_plan_get_layout(const i8c_plan* plan, i8c_layout* out);
+
 /* Output height P and width Q for a shape (formula above).  Returns
  * I8C_ERR_INVALID_ARG for non-positive sizes or negative padding and
  * I8C_ERR_UNSUPPORTED when the dilated filter does not fit (P or Q < 1). */
@@ -227,10 +276,37 @@ i8c_status i8c_conv2d_fprop_ex(const int8_t* x, const int8_t* f, int8_t* y, cons
  * first call before any stream capture.  All calls share the one array and
  * each call overwrites it, so calls that may overlap on the GPU (different
  * streams, or different host threads) race and must be serialised by the
- * caller.  A device-side wait that runs out is recorded only in the shared
- * status word and is not reported back; the output is then undefined. */
+ * caller.  A device-side wait that runs out is recorded in the array's
+ * status word (zeroed at the start of every call); i8c_last_device_status
+ * reads it back, without allocating, and the output is then undefined. */
 i8c_status i8c_conv2d_fprop_noalloc(const int8_t* x, const int8_t* f, int8_t* y, const i8c_conv_shape* shape,
                                     float alpha, cudaStream_t stream);
+
+/* Device status of the checked one-shot calls (the checked-call side of the
+ * host-latency tutorial's split, "Bypassing argument checks": the checked
+ * calls report what their kernels met).  Synchronises `stream`, then returns
+ * and clears the device status words of the plans that i8c_conv2d_fprop,
+ * i8c_conv2d_fprop_acc and i8c_conv2d_fprop_ex cached for (current device,
+ * `stream`), and of i8c_conv2d_fprop_noalloc on the current device (one word
+ * per device, shared by all streams: reliable when its last call was made on
+ * `stream`).  I8C_OK, or I8C_ERR_TIMEOUT if a bounded wait in one of their
+ * kernels ran out since the last read (the outputs of that call are then
+ * undefined; the next call runs normally).  Allocates nothing.
+ *
+ * The one-shot calls keep at most 64 cached plans (one per device, stream
+ * and shape); creating a 65th destroys the least recently used one, which
+ * synchronises the device, and a status word not yet read goes with it. */
+i8c_status i8c_last_device_status(cudaStream_t stream);
+
+/* Number of plans the one-shot calls currently keep (at most 64). */
+int64_t i8c_oneshot_cached_plans(void);
+
+/* Test hook: destroys the one-shot calls' cached plans (synchronising the
+ * device) and makes the plans they create from now on, and the
+ * no-allocation entry point, run with these i8c_options debug_flags and
+ * wait_timeout_us (0, 0: the defaults).  I8C_ERR_INVALID_ARG for negative
+ * values.  Not for production use. */
+i8c_status i8c_debug_set_oneshot(int32_t debug_flags, int32_t wait_timeout_us);
 
 /* Compile-once / run-many (host-latency tutorial, "Compiling once"): a plan
  * holds the validated shape, the tile schedule, the filter staging buffer
@@ -265,6 +341,23 @@ i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t*
  * before reading y. */
 i8c_status i8c_plan_run_host(const i8c_plan* plan, const int8_t* x_host, const int8_t* f_host, int8_t* y_host,
                              float alpha, cudaStream_t stream);
+
+/* `steps` end-to-end runs on HOST buffers, pipelined: run i copies x_host[i]
+ * and f_host[i] in, runs with alpha[i] and copies y out to y_host[i] (each
+ * array holds `steps` host pointers; pinned memory makes the copies
+ * asynchronous).  The plan must have been created with host_staging = 2: two
+ * device staging sets and two copy streams owned by the plan, so that the
+ * input copies of run i + 1 and the output copy of run i - 1 overlap run i
+ * (the runs stay on `stream`, in order, sharing the plan's filter buffer).
+ * Enqueues everything and returns; `stream` reaches the end of the call once
+ * the last output copy has completed, so the caller synchronises `stream`
+ * before reading any y_host[i].  Host buffers must stay untouched until
+ * then.  I8C_ERR_INVALID_ARG for null pointers, steps < 0, or a plan
+ * without the second staging set.  Not capturable (it records events on
+ * the plan's own streams). */
+i8c_status i8c_plan_run_host_pipelined(const i8c_plan* plan, const int8_t* const* x_host,
+                                       const int8_t* const* f_host, int8_t* const* y_host, const float* alpha,
+                                       int32_t steps, cudaStream_t stream);
 
 /* Synchronises `stream`, then returns (and clears) the plan's device status
  * word: I8C_OK, or I8C_ERR_TIMEOUT if a bounded wait in a kernel ran out. */

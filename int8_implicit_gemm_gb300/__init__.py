@@ -66,6 +66,23 @@ class Options(ctypes.Structure):
                 ("fused_filter", ctypes.c_int32), ("tile_px", ctypes.c_int32), ("filter_run", ctypes.c_int32)]
 
 
+class Layout(ctypes.Structure):
+    """i8c_layout: the shared- and tensor-memory layout of a plan's kernel."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "kernel_variant", "cta_group", "block_n", "smem_bytes", "tmem_cols", "chunk_slices", "num_chunks",
+        "flat_tiles", "tile_px", "halo_rows", "halo_cw", "positions", "plane_bytes", "halo_bytes", "halo_stages",
+        "off_staging", "staging_slots", "staging_bytes", "off_filter", "filter_stages", "filter_run",
+        "filter_stage_bytes", "off_out", "off_bar", "bar_bytes")] + [("phase_off", ctypes.c_int32 * 9)] + [
+        (n, ctypes.c_int32) for n in (
+            "gather_stages", "gather_off_a", "gather_stage_a", "gather_off_b", "gather_stage_b",
+            "gather_off_staging", "gather_staging_slots", "gather_staging_bytes", "gather_off_bar")]
+
+    def asdict(self):
+        d = {n: getattr(self, n) for n, _ in self._fields_}
+        d["phase_off"] = list(self.phase_off)
+        return d
+
+
 class TuneEntry(ctypes.Structure):
     """i8c_tune_entry: one candidate of i8c_plan_autotune."""
     _fields_ = [("options", Options), ("status", ctypes.c_int32), ("us", ctypes.c_float)]
@@ -103,14 +120,19 @@ def _load() -> ctypes.CDLL:
         "i8c_conv2d_fprop_acc": [P, P, P, S, P],
         "i8c_conv2d_fprop_noalloc": [P, P, P, S, F, P],
         "i8c_conv2d_fprop_f32": [P, P, P, P, S, P],
+        "i8c_last_device_status": [P],
+        "i8c_debug_set_oneshot": [I32, I32],
         "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
         "i8c_plan_run": [P, P, P, P, F, P],
         "i8c_plan_run_ex": [P, P, P, P, F, ctypes.POINTER(Epilogue), P],
         "i8c_conv2d_fprop_ex": [P, P, P, S, F, ctypes.POINTER(Epilogue), P],
         "i8c_plan_run_acc": [P, P, P, P, P],
         "i8c_plan_run_host": [P, P, P, P, F, P],
+        "i8c_plan_run_host_pipelined": [P, P, P, P, P, I32, P],
         "i8c_plan_status": [P, P],
         "i8c_plan_get_info": [P, ctypes.POINTER(PlanInfo)],
+        "i8c_plan_layout": [S, ctypes.POINTER(Options), I32, ctypes.POINTER(Layout)],
+        "i8c_plan_get_layout": [P, ctypes.POINTER(Layout)],
         "i8c_plan_kernel_time": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)],
         "i8c_plan_trace": [P, P, I64],
         "i8c_plan_destroy": [P],
@@ -131,6 +153,8 @@ def _load() -> ctypes.CDLL:
     lib.i8c_status_string.restype = ctypes.c_char_p
     lib.i8c_launch_count.argtypes = []
     lib.i8c_launch_count.restype = I64
+    lib.i8c_oneshot_cached_plans.argtypes = []
+    lib.i8c_oneshot_cached_plans.restype = I64
     return lib
 
 
@@ -204,6 +228,39 @@ def i8c_conv2d_fprop_noalloc(x, f, y, shape, alpha: float, stream=None) -> None:
                                         ctypes.c_float(alpha), _stream(stream)), "i8c_conv2d_fprop_noalloc")
 
 
+def i8c_last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status of the
+    one-shot calls made on it (and of the no-allocation entry point)."""
+    return lib.i8c_last_device_status(_stream(stream))
+
+
+def i8c_oneshot_cached_plans() -> int:
+    return lib.i8c_oneshot_cached_plans()
+
+
+def i8c_debug_set_oneshot(debug_flags: int = 0, wait_timeout_us: int = 0) -> None:
+    _check(lib.i8c_debug_set_oneshot(debug_flags, wait_timeout_us), "i8c_debug_set_oneshot")
+
+
+def make_options(**kw) -> "Options":
+    """i8c_options from keyword arguments (the Plan constructor's names)."""
+    o = Options()
+    for k, v in kw.items():
+        if k not in dict(Options._fields_):
+            raise TypeError(f"unknown plan option {k}")
+        setattr(o, k, int(v))
+    return o
+
+
+def i8c_plan_layout(shape, num_sms: int = 152, **options) -> dict:
+    """The layout a plan of `shape` with these options would get on a GPU of
+    num_sms SMs, computed on the host alone (no GPU needed)."""
+    out = Layout()
+    _check(lib.i8c_plan_layout(ctypes.byref(ConvShape.of(shape)), ctypes.byref(make_options(**options)), num_sms,
+                               ctypes.byref(out)), "i8c_plan_layout")
+    return out.asdict()
+
+
 def i8c_plan_autotune(x, f, y, shape, alpha: float, iters: int = 10, stream=None):
     """Time the candidate plans of `shape` on these tensors (i8c_plan_autotune).
     Returns (options, us, entries): the fastest candidate's plan options as a
@@ -274,7 +331,7 @@ class Plan:
                  host_staging=False, debug_flags=0, timing_events=0, kernel_variant=0, halo_loads=0, tail_split=0,
                  tile_shape=0, fused_filter=0, tile_px=0, filter_run=0):
         self.shape = ConvShape.of(shape)
-        opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(bool(host_staging)), debug_flags,
+        opts = Options(block_n, num_ctas, max_chunk_slices, wait_timeout_us, int(host_staging), debug_flags,
                        timing_events, kernel_variant, halo_loads, tail_split, tile_shape, fused_filter, tile_px,
                        filter_run)
         h = ctypes.c_void_p()
@@ -303,11 +360,29 @@ class Plan:
         _check(lib.i8c_plan_run_host(self.handle, _ptr(x_host), _ptr(f_host), _ptr(y_host), ctypes.c_float(alpha),
                                      _stream(stream)), "i8c_plan_run_host")
 
+    def run_host_pipelined(self, x_hosts, f_hosts, y_hosts, alphas, stream=None) -> None:
+        """len(x_hosts) end-to-end runs on pinned host tensors, the copies of
+        neighbouring runs overlapped (plan created with host_staging=2)."""
+        n = len(x_hosts)
+        if not (len(f_hosts) == len(y_hosts) == len(alphas) == n):
+            raise ValueError("one x, f, y and alpha per run")
+        arr = ctypes.c_void_p * max(1, n)
+        xa, fa, ya = arr(*[_ptr(t) for t in x_hosts]), arr(*[_ptr(t) for t in f_hosts]), arr(*[_ptr(t) for t in y_hosts])
+        al = (ctypes.c_float * max(1, n))(*[float(a) for a in alphas])
+        _check(lib.i8c_plan_run_host_pipelined(self.handle, xa, fa, ya, al, n, _stream(stream)),
+               "i8c_plan_run_host_pipelined")
+
     def kernel_time(self):
         """(summed ms, launches) of the convolution kernels timed since the last call."""
         ms, n = ctypes.c_double(), ctypes.c_int64()
         _check(lib.i8c_plan_kernel_time(self.handle, ctypes.byref(ms), ctypes.byref(n)), "i8c_plan_kernel_time")
         return ms.value, n.value
+
+    def layout(self) -> dict:
+        """The shared- and tensor-memory layout of this plan's kernel."""
+        out = Layout()
+        _check(lib.i8c_plan_get_layout(self.handle, ctypes.byref(out)), "i8c_plan_get_layout")
+        return out.asdict()
 
     def trace(self):
         """The trace of a plan created with I8C_DEBUG_TRACE, shape (8, 4, 512):

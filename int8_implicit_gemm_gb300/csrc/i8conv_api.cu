@@ -35,6 +35,11 @@ struct i8c_plan {
   long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), kTraceRows * kTraceSlots entries
   CUtensorMap tmap;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
+  // host_staging = 2: a second staging set and the pipelined host-buffer
+  // runs' copy streams and ordering events (set b: in_done, run_done, out_done)
+  int8_t *stage_x2, *stage_f2, *stage_y2;
+  cudaStream_t s_in, s_out;
+  cudaEvent_t ev_begin, ev_in[2], ev_run[2], ev_out[2];
   uint32_t* gbar;        // halo kernel converting the filter itself: grid barrier {arrivals, generation}
   int* split_count;      // halo kernel, split tail tiles: arrivals per tile and CTA rank
   int32_t* split_part;   // halo kernel, split tail tiles: int32 partial sums
@@ -286,6 +291,13 @@ void free_plan_memory(i8c_plan* p) {
   if (p->split_count) cudaFree(p->split_count);
   if (p->gbar) cudaFree(p->gbar);
   if (p->split_part) cudaFree(p->split_part);
+  if (p->stage_x2) cudaFree(p->stage_x2);
+  if (p->stage_f2) cudaFree(p->stage_f2);
+  if (p->stage_y2) cudaFree(p->stage_y2);
+  for (cudaEvent_t e : {p->ev_begin, p->ev_in[0], p->ev_in[1], p->ev_run[0], p->ev_run[1], p->ev_out[0], p->ev_out[1]})
+    if (e) cudaEventDestroy(e);
+  if (p->s_in) cudaStreamDestroy(p->s_in);
+  if (p->s_out) cudaStreamDestroy(p->s_out);
 }
 
 ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
@@ -373,103 +385,78 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
   return from_cuda(e);
 }
 
-// Plans behind the one-shot entry points, one per (device, stream, shape).
+// Plans behind the one-shot entry points, one per (device, stream, shape),
+// at most kMaxCachedPlans of them: the least recently used plan is destroyed
+// when a new one would exceed the bound (a caller that creates streams call
+// after call cannot grow the cache without limit).
+constexpr size_t kMaxCachedPlans = 64;
+using CacheKey = std::array<int64_t, 15>;
+struct CacheEntry {
+  i8c_plan* plan;
+  uint64_t last_use;
+};
 std::mutex g_cache_mu;
-std::map<std::array<int64_t, 15>, i8c_plan*> g_cache;
+std::map<CacheKey, CacheEntry> g_cache;
+uint64_t g_cache_clock = 0;
+// Test hooks for the one-shot and no-allocation entry points
+// (i8c_debug_set_oneshot): debug flags and the bounded-wait limit.
+int32_t g_oneshot_debug_flags = 0;
+int32_t g_oneshot_timeout_us = 0;
 
 i8c_status cached_plan(const i8c_conv_shape* s, cudaStream_t stream, i8c_plan** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return from_cuda(e);
-  std::array<int64_t, 15> key{dev, static_cast<int64_t>(reinterpret_cast<uintptr_t>(stream)),
-                              s->N, s->C, s->H, s->W, s->K, s->R, s->S, s->pad_h, s->pad_w,
-                              s->stride_h, s->stride_w, s->dil_h * 65536LL + s->dil_w, 0};
+  CacheKey key{dev, static_cast<int64_t>(reinterpret_cast<uintptr_t>(stream)),
+               s->N, s->C, s->H, s->W, s->K, s->R, s->S, s->pad_h, s->pad_w,
+               s->stride_h, s->stride_w, s->dil_h * 65536LL + s->dil_w, 0};
   std::lock_guard<std::mutex> lock(g_cache_mu);
   auto it = g_cache.find(key);
   if (it != g_cache.end()) {
-    *out = it->second;
+    it->second.last_use = ++g_cache_clock;
+    *out = it->second.plan;
     return I8C_OK;
   }
+  i8c_options o{};
+  o.debug_flags = g_oneshot_debug_flags;
+  o.wait_timeout_us = g_oneshot_timeout_us;
   i8c_plan* p = nullptr;
-  i8c_status st = i8c_plan_create(s, nullptr, &p);
+  i8c_status st = i8c_plan_create(s, &o, &p);
   if (st != I8C_OK) return st;
-  g_cache[key] = p;
+  if (g_cache.size() >= kMaxCachedPlans) {
+    auto lru = g_cache.begin();
+    for (auto jt = g_cache.begin(); jt != g_cache.end(); ++jt)
+      if (jt->second.last_use < lru->second.last_use) lru = jt;
+    i8c_plan_destroy(lru->second.plan);  // synchronises the device first
+    g_cache.erase(lru);
+  }
+  g_cache[key] = CacheEntry{p, ++g_cache_clock};
   *out = p;
   return I8C_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* i8c_status_string(i8c_status status) {
-  switch (status) {
-    case I8C_OK: return "ok";
-    case I8C_ERR_INVALID_ARG: return "invalid argument";
-    case I8C_ERR_UNSUPPORTED: return "unsupported shape";
-    case I8C_ERR_MISALIGNED: return "pointer not 16-byte aligned";
-    case I8C_ERR_OVERFLOW_RISK: return "int32 accumulator or index overflow possible";
-    case I8C_ERR_CUDA: return "CUDA error";
-    case I8C_ERR_TIMEOUT: return "device-side wait timed out";
-    case I8C_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
-  }
-  return "unknown status";
+bool options_valid(const i8c_options& o) {
+  if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256) return false;
+  return !(o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
+           o.timing_events < 0 || o.timing_events > 65536 || o.host_staging < 0 || o.host_staging > 2 ||
+           o.kernel_variant < 0 || o.kernel_variant > 5 || o.halo_loads < 0 || o.halo_loads > 2 ||
+           o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
+           o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
+           (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)));
 }
 
-int64_t i8c_launch_count(void) { return i8c::g_launches.load(std::memory_order_relaxed); }
-
-i8c_status i8c_output_size(const i8c_conv_shape* shape, int32_t* P, int32_t* Q) {
-  if (P == nullptr || Q == nullptr) return I8C_ERR_INVALID_ARG;
-  int64_t p = 0, q = 0;
-  i8c_status st = check_shape(shape, &p, &q);
-  if (st != I8C_OK) return st;
-  if (p > kMaxI32 || q > kMaxI32) return I8C_ERR_OVERFLOW_RISK;
-  *P = static_cast<int32_t>(p);
-  *Q = static_cast<int32_t>(q);
-  return I8C_OK;
-}
-
-i8c_status i8c_supported(const i8c_conv_shape* shape) {
-  int64_t p = 0, q = 0;
-  return check_supported(shape, &p, &q);
-}
-
-i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts, i8c_plan** out) {
-  if (out == nullptr) return I8C_ERR_INVALID_ARG;
-  *out = nullptr;
-  int64_t P = 0, Q = 0;
-  i8c_status st = check_supported(shape, &P, &Q);
-  if (st != I8C_OK) return st;
-  i8c_options o{};
-  if (opts) o = *opts;
-  if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256)
-    return I8C_ERR_INVALID_ARG;
-  if (o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
-      o.timing_events < 0 || o.timing_events > 65536 || o.kernel_variant < 0 || o.kernel_variant > 5 ||
-      o.halo_loads < 0 || o.halo_loads > 2 || o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 ||
-      o.tile_shape > 2 || o.fused_filter < 0 || o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
-      (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)))
-    return I8C_ERR_INVALID_ARG;
-
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return from_cuda(e);
-  cudaDeviceProp prop;
-  e = cudaGetDeviceProperties(&prop, dev);
-  if (e != cudaSuccess) return from_cuda(e);
-  if (prop.major != 10 || prop.minor != 3) return I8C_ERR_NO_DEVICE;
-  EncodeTiled encode = get_encode_tiled();
-  if (encode == nullptr) return I8C_ERR_CUDA;
-
-  i8c_plan* p = new (std::nothrow) i8c_plan();
-  if (p == nullptr) return I8C_ERR_CUDA;
-  const i8c_conv_shape& s = *shape;
+// The planner: kernel form, tile shape, persistent schedule, exact-fp32
+// chunking and shared-memory layout of shape `s` (P, Q already checked) on
+// `ctas` SMs, into `p`.  host_only: no device call at all -- CTA pairs are
+// assumed to fit one per two SMs -- so that the layout can be inspected
+// without a GPU (i8c_plan_layout).  *split_bytes_out: the int32 partial-sum
+// workspace the schedule needs.
+i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t P, int64_t Q, int ctas,
+                         bool host_only, i8c_plan* p, int64_t* split_bytes_out) {
   p->shape = s;
   p->P = static_cast<int>(P);
   p->Q = static_cast<int>(Q);
   p->M = static_cast<int64_t>(s.N) * P * Q;
-  p->device = dev;
-  const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
   // Kernel and tile width.  The halo kernel (16x8 output patches) is preferred
   // whenever its halo fits in shared memory; its tile width is the one with
   // the best wave efficiency (ties go to the wider tile).  Variant 3 runs it
@@ -506,8 +493,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (cg == 2 && o.kernel_variant != 5 && h.positions > 1.6 * (n / 2)) continue;
       int g = ctas / cg;
       if (cg == 2) {
-        if (i8c::tr_prepare_pair() != cudaSuccess) continue;
-        const int fit = i8c::tr_pair_max_clusters(h.bgroup, s.S, n, sm);
+        if (!host_only && i8c::tr_prepare_pair() != cudaSuccess) continue;
+        const int fit = host_only ? g : i8c::tr_pair_max_clusters(h.bgroup, s.S, n, sm);
         if (fit < 1) continue;
         if (g > fit) g = fit;
       }
@@ -528,7 +515,6 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     double cost = 0.0;
     const int n = pick_tr(cg, &cost, &groups);
     if (n == 0) {
-      delete p;
       return I8C_ERR_UNSUPPORTED;
     }
     tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &p->halo, &halo_smem);
@@ -560,8 +546,8 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
         int g = ctas / cg;
         if (cg == 2) {
           // pairs that fit on the GPU at once (clusters need both SMs free)
-          if (i8c::halo_prepare_pair(cand) != cudaSuccess) continue;
-          const int fit = i8c::halo_pair_max_clusters(cand, h.bgroup, s.S, sm);
+          if (!host_only && i8c::halo_prepare_pair(cand) != cudaSuccess) continue;
+          const int fit = host_only ? g : i8c::halo_pair_max_clusters(cand, h.bgroup, s.S, sm);
           if (fit < 1) continue;
           if (g > fit) g = fit;
           if (g < 1) g = 1;
@@ -663,7 +649,6 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       p->cta_group = cg;
       halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, best.flat, &p->halo, &halo_smem);
     } else if (o.kernel_variant >= 2) {
-      delete p;
       return I8C_ERR_UNSUPPORTED;
     }
   }
@@ -678,12 +663,12 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
                               : (p->M + 127) / 128;
   const int64_t tiles = m_tiles * p->num_n_tiles;
   if (tiles > kMaxI32) {
-    delete p;
     return I8C_ERR_OVERFLOW_RISK;
   }
   p->num_m_tiles = static_cast<int>(m_tiles);
   p->num_tiles = static_cast<int>(tiles);
-  int64_t split_bytes = 0;
+  int64_t& split_bytes = *split_bytes_out;
+  split_bytes = 0;
   if (p->kernel_variant >= 4) {
     // one unit per tile, no split tail
     p->halo.ksplit = 1;
@@ -770,6 +755,78 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
   }
   p->smem_bytes = p->kernel_variant >= 2 ? halo_smem : i8c::conv_smem_bytes(bn);
+  return I8C_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* i8c_status_string(i8c_status status) {
+  switch (status) {
+    case I8C_OK: return "ok";
+    case I8C_ERR_INVALID_ARG: return "invalid argument";
+    case I8C_ERR_UNSUPPORTED: return "unsupported shape";
+    case I8C_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case I8C_ERR_OVERFLOW_RISK: return "int32 accumulator or index overflow possible";
+    case I8C_ERR_CUDA: return "CUDA error";
+    case I8C_ERR_TIMEOUT: return "device-side wait timed out";
+    case I8C_ERR_NO_DEVICE: return "no usable sm_103 CUDA device";
+  }
+  return "unknown status";
+}
+
+int64_t i8c_launch_count(void) { return i8c::g_launches.load(std::memory_order_relaxed); }
+
+i8c_status i8c_output_size(const i8c_conv_shape* shape, int32_t* P, int32_t* Q) {
+  if (P == nullptr || Q == nullptr) return I8C_ERR_INVALID_ARG;
+  int64_t p = 0, q = 0;
+  i8c_status st = check_shape(shape, &p, &q);
+  if (st != I8C_OK) return st;
+  if (p > kMaxI32 || q > kMaxI32) return I8C_ERR_OVERFLOW_RISK;
+  *P = static_cast<int32_t>(p);
+  *Q = static_cast<int32_t>(q);
+  return I8C_OK;
+}
+
+i8c_status i8c_supported(const i8c_conv_shape* shape) {
+  int64_t p = 0, q = 0;
+  return check_supported(shape, &p, &q);
+}
+
+i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts, i8c_plan** out) {
+  if (out == nullptr) return I8C_ERR_INVALID_ARG;
+  *out = nullptr;
+  int64_t P = 0, Q = 0;
+  i8c_status st = check_supported(shape, &P, &Q);
+  if (st != I8C_OK) return st;
+  i8c_options o{};
+  if (opts) o = *opts;
+  if (!options_valid(o)) return I8C_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaDeviceProp prop;
+  e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (prop.major != 10 || prop.minor != 3) return I8C_ERR_NO_DEVICE;
+  EncodeTiled encode = get_encode_tiled();
+  if (encode == nullptr) return I8C_ERR_CUDA;
+
+  i8c_plan* p = new (std::nothrow) i8c_plan();
+  if (p == nullptr) return I8C_ERR_CUDA;
+  const i8c_conv_shape& s = *shape;
+  p->device = dev;
+  const int ctas = o.num_ctas > 0 ? o.num_ctas : prop.multiProcessorCount;
+  int64_t split_bytes = 0;
+  st = plan_geometry(s, o, P, Q, ctas, false, p, &split_bytes);
+  if (st != I8C_OK) {
+    delete p;
+    return st;
+  }
+  const int bn = p->block_n;
+  const int halo_smem = p->smem_bytes;
   p->timeout_ns = static_cast<uint64_t>(o.wait_timeout_us > 0 ? o.wait_timeout_us : 2000000) * 1000ull;
   p->debug_flags = o.debug_flags;
   p->x_bytes = static_cast<size_t>(s.N) * s.C * s.H * s.W;
@@ -817,6 +874,17 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     if (e == cudaSuccess) e = cudaMalloc(&p->stage_y, p->y_bytes);
     p->workspace_bytes += static_cast<int64_t>(p->x_bytes + p->f_bytes + p->y_bytes);
   }
+  if (e == cudaSuccess && o.host_staging == 2) {
+    e = cudaMalloc(&p->stage_x2, p->x_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->stage_f2, p->f_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&p->stage_y2, p->y_bytes);
+    p->workspace_bytes += static_cast<int64_t>(p->x_bytes + p->f_bytes + p->y_bytes);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&p->ev_begin, &p->ev_in[0], &p->ev_in[1], &p->ev_run[0], &p->ev_run[1], &p->ev_out[0],
+                            &p->ev_out[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  }
   for (int i = 0; e == cudaSuccess && i < o.timing_events; ++i) {
     cudaEvent_t a = nullptr, b = nullptr;
     e = cudaEventCreate(&a);
@@ -847,6 +915,83 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
     return I8C_ERR_CUDA;
   }
   *out = p;
+  return I8C_OK;
+}
+
+namespace {
+
+void fill_layout(const i8c_plan* pl, i8c_layout* L) {
+  *L = i8c_layout{};
+  L->kernel_variant = pl->kernel_variant;
+  L->cta_group = pl->cta_group;
+  L->block_n = pl->block_n;
+  L->smem_bytes = pl->smem_bytes;
+  L->tmem_cols = static_cast<int32_t>(pl->tmem_cols);
+  L->chunk_slices = pl->chunk_slices;
+  L->num_chunks = pl->num_chunks;
+  if (pl->kernel_variant >= 2) {
+    const i8c::HaloParams& h = pl->halo;
+    L->flat_tiles = h.flat;
+    L->tile_px = h.flat ? h.tile_px : 0;
+    L->halo_rows = h.HR;
+    L->halo_cw = h.CW;
+    L->positions = h.positions;
+    L->plane_bytes = static_cast<int32_t>(h.plane_bytes);
+    L->halo_bytes = static_cast<int32_t>(h.halo_bytes);
+    L->halo_stages = h.nhs;
+    L->off_staging = static_cast<int32_t>(h.off_stg);
+    L->staging_slots = h.nstg;
+    L->staging_bytes = static_cast<int32_t>(h.stg_bytes);
+    L->off_filter = static_cast<int32_t>(h.off_b);
+    L->filter_stages = h.nbs;
+    L->filter_run = h.bgroup;
+    const int rows = pl->kernel_variant >= 4 ? 128 : pl->block_n / pl->cta_group;  // transposed: 128 channels per CTA
+    L->filter_stage_bytes = h.bgroup * rows * 64;
+    L->off_out = static_cast<int32_t>(h.off_out);
+    L->off_bar = static_cast<int32_t>(h.off_bar);
+    L->bar_bytes = i8c::kHaloBarBytes;
+    for (int f = 0; f < 9; ++f) L->phase_off[f] = h.phase_off[f];
+  } else {
+    auto gather = [&](auto cfg) {
+      using Cfg = decltype(cfg);
+      L->gather_stages = Cfg::kStages;
+      L->gather_off_a = Cfg::kOffA;
+      L->gather_stage_a = Cfg::kAStage;
+      L->gather_off_b = Cfg::kOffB;
+      L->gather_stage_b = Cfg::kBStage;
+      L->gather_off_staging = Cfg::kOffStg;
+      L->gather_staging_slots = Cfg::kStg;
+      L->gather_staging_bytes = Cfg::kStgBytes;
+      L->gather_off_bar = Cfg::kOffBar;
+    };
+    if (pl->block_n >= 256) gather(i8c::TileCfg<256>{});
+    else if (pl->block_n >= 128) gather(i8c::TileCfg<128>{});
+    else if (pl->block_n >= 64) gather(i8c::TileCfg<64>{});
+    else gather(i8c::TileCfg<32>{});
+  }
+}
+
+}  // namespace
+
+i8c_status i8c_plan_layout(const i8c_conv_shape* shape, const i8c_options* opts, int32_t num_sms, i8c_layout* out) {
+  if (out == nullptr || num_sms < 1) return I8C_ERR_INVALID_ARG;
+  int64_t P = 0, Q = 0;
+  i8c_status st = check_supported(shape, &P, &Q);
+  if (st != I8C_OK) return st;
+  i8c_options o{};
+  if (opts) o = *opts;
+  if (!options_valid(o)) return I8C_ERR_INVALID_ARG;
+  i8c_plan pl{};
+  int64_t split_bytes = 0;
+  st = plan_geometry(*shape, o, P, Q, o.num_ctas > 0 ? o.num_ctas : num_sms, true, &pl, &split_bytes);
+  if (st != I8C_OK) return st;
+  fill_layout(&pl, out);
+  return I8C_OK;
+}
+
+i8c_status i8c_plan_get_layout(const i8c_plan* plan, i8c_layout* out) {
+  if (plan == nullptr || out == nullptr) return I8C_ERR_INVALID_ARG;
+  fill_layout(plan, out);
   return I8C_OK;
 }
 
@@ -956,6 +1101,46 @@ i8c_status i8c_plan_run_host(const i8c_plan* pl, const int8_t* x_host, const int
   return from_cuda(cudaMemcpyAsync(y_host, pl->stage_y, pl->y_bytes, cudaMemcpyDeviceToHost, stream));
 }
 
+i8c_status i8c_plan_run_host_pipelined(const i8c_plan* pl, const int8_t* const* x_host, const int8_t* const* f_host,
+                                       int8_t* const* y_host, const float* alpha, int32_t steps,
+                                       cudaStream_t stream) {
+  if (pl == nullptr || x_host == nullptr || f_host == nullptr || y_host == nullptr || alpha == nullptr || steps < 0)
+    return I8C_ERR_INVALID_ARG;
+  if (pl->stage_x2 == nullptr) return I8C_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < steps; ++i)
+    if (x_host[i] == nullptr || f_host[i] == nullptr || y_host[i] == nullptr) return I8C_ERR_INVALID_ARG;
+  int8_t* const sx[2] = {pl->stage_x, pl->stage_x2};
+  int8_t* const sf[2] = {pl->stage_f, pl->stage_f2};
+  int8_t* const sy[2] = {pl->stage_y, pl->stage_y2};
+  // the copy streams start after the work already on `stream`
+  cudaError_t e = cudaEventRecord(pl->ev_begin, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(pl->s_in, pl->ev_begin, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(pl->s_out, pl->ev_begin, 0);
+  for (int32_t i = 0; e == cudaSuccess && i < steps; ++i) {
+    const int b = i & 1;
+    // inputs of step i into set b once run i - 2 has read that set
+    if (i >= 2) e = cudaStreamWaitEvent(pl->s_in, pl->ev_run[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sx[b], x_host[i], pl->x_bytes, cudaMemcpyHostToDevice, pl->s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sf[b], f_host[i], pl->f_bytes, cudaMemcpyHostToDevice, pl->s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(pl->ev_in[b], pl->s_in);
+    // run i on `stream` once its inputs are in and step i - 2's output has left set b
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, pl->ev_in[b], 0);
+    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(stream, pl->ev_out[b], 0);
+    if (e != cudaSuccess) break;
+    const i8c_status st = run_plan(pl, sx[b], sf[b], sy[b], nullptr, alpha[i], stream);
+    if (st != I8C_OK) return st;
+    e = cudaEventRecord(pl->ev_run[b], stream);
+    // output of step i back to the host
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(pl->s_out, pl->ev_run[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(y_host[i], sy[b], pl->y_bytes, cudaMemcpyDeviceToHost, pl->s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(pl->ev_out[b], pl->s_out);
+  }
+  // `stream` reaches the end of the call once the last output copy is done
+  if (e == cudaSuccess) e = cudaEventRecord(pl->ev_begin, pl->s_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, pl->ev_begin, 0);
+  return from_cuda(e);
+}
+
 i8c_status i8c_plan_status(const i8c_plan* pl, cudaStream_t stream) {
   if (pl == nullptr) return I8C_ERR_INVALID_ARG;
   cudaError_t e = cudaStreamSynchronize(stream);
@@ -1005,6 +1190,42 @@ i8c_status i8c_conv2d_fprop_acc(const int8_t* x, const int8_t* f, int32_t* acc, 
   i8c_status st = cached_plan(shape, stream, &p);
   if (st != I8C_OK) return st;
   return run_plan(p, x, f, nullptr, acc, 1.0f, stream);
+}
+
+i8c_status i8c_last_device_status(cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  i8c_status first = I8C_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    const int64_t sk = static_cast<int64_t>(reinterpret_cast<uintptr_t>(stream));
+    for (auto& kv : g_cache) {
+      if (kv.first[0] != dev || kv.first[1] != sk) continue;
+      const i8c_status st = i8c_plan_status(kv.second.plan, stream);
+      if (st != I8C_OK && first == I8C_OK) first = st;
+    }
+  }
+  const i8c_status na = static_cast<i8c_status>(i8c::noalloc_take_status(dev));
+  return first != I8C_OK ? first : na;
+}
+
+i8c_status i8c_debug_set_oneshot(int32_t debug_flags, int32_t wait_timeout_us) {
+  if (debug_flags < 0 || wait_timeout_us < 0) return I8C_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (auto& kv : g_cache) i8c_plan_destroy(kv.second.plan);
+  g_cache.clear();
+  g_oneshot_debug_flags = debug_flags;
+  g_oneshot_timeout_us = wait_timeout_us;
+  i8c::noalloc_set_debug(debug_flags, wait_timeout_us);
+  return I8C_OK;
+}
+
+int64_t i8c_oneshot_cached_plans(void) {
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  return static_cast<int64_t>(g_cache.size());
 }
 
 i8c_status i8c_pack_nchw_to_ncxhwx32(const int8_t* src, int8_t* dst, int32_t N, int32_t C, int32_t H, int32_t W,

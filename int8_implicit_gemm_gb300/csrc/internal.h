@@ -45,6 +45,12 @@ cudaError_t tr_launch_pair(const CUtensorMap& tmap, const HaloParams& p, int sme
 int tr_pair_max_clusters(int bgroup, int S, int mma_n, int smem_bytes);
 constexpr int kMaxDynamicSmem = 232448;
 
+// noalloc.cu: the no-allocation entry point's status word on device `dev`
+// (synchronous; I8C_OK if that entry point has not run there), cleared once
+// read; and the one-shot test hooks (debug flags, bounded-wait limit in us).
+int noalloc_take_status(int dev);
+void noalloc_set_debug(int debug_flags, int timeout_us);
+
 // layout_kernels.cu
 cudaError_t launch_filter_to_f16(const int8_t* f, uint16_t* f16, int64_t count, cudaStream_t stream);
 cudaError_t launch_pack_act(const int8_t* src, int8_t* dst, int N, int C, int H, int W, bool to_interleaved,

@@ -34,14 +34,21 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Per device: whether it was checked to be an sm_103 device, its SM count,
+// and whether this entry point has run there (so its status word means
+// something).  The scratch array's device address and the kernels' shared
+// memory limit are looked up again on every call, since a device reset
+// (cudaDeviceReset, or a torn-down primary context) invalidates both.
 struct DeviceSetup {
-  bool ready = false;
-  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  bool checked = false;
+  bool used = false;
   int num_sms = 0;
 };
 
 std::mutex g_setup_mu;
 DeviceSetup g_setup[kMaxDevices];
+int g_debug_flags = 0;       // test hooks (i8c_debug_set_oneshot)
+int g_timeout_us = 0;        // 0: 2 s
 
 using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
 
@@ -65,32 +72,34 @@ i8c_status status_of(cudaError_t e) {
   return I8C_ERR_CUDA;
 }
 
-// Once per device, with that device current: look up the device address of
-// the scratch array (the host-side name is only a stand-in) and prepare the
-// kernels.  Nothing here allocates.
-i8c_status setup_device(int dev, DeviceSetup* out) {
+// With device `dev` current: check it once, then (every call) look up the
+// device address of the scratch array -- the host-side name is only a
+// stand-in -- and raise the kernels' shared-memory limit.  Nothing here
+// allocates.
+i8c_status setup_device(int dev, unsigned char** scratch, int* num_sms) {
   if (dev < 0 || dev >= kMaxDevices) return I8C_ERR_NO_DEVICE;
   std::lock_guard<std::mutex> lock(g_setup_mu);
   DeviceSetup& s = g_setup[dev];
-  if (!s.ready) {
+  if (!s.checked) {
     int major = 0, minor = 0, sms = 0;
     cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return status_of(e);
     if (major != 10 || minor != 3) return I8C_ERR_NO_DEVICE;
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) return e != cudaSuccess ? status_of(e) : I8C_ERR_CUDA;
-    for (int bn : {32, 64, 128, 256}) {
-      e = i8c::conv_prepare(bn);
-      if (e != cudaSuccess) return status_of(e);
-    }
-    s.scratch = static_cast<unsigned char*>(p);
     s.num_sms = sms;
-    s.ready = true;
+    s.checked = true;
   }
-  *out = s;
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) return e != cudaSuccess ? status_of(e) : I8C_ERR_CUDA;
+  for (int bn : {32, 64, 128, 256}) {
+    e = i8c::conv_prepare(bn);
+    if (e != cudaSuccess) return status_of(e);
+  }
+  s.used = true;
+  *scratch = static_cast<unsigned char*>(p);
+  *num_sms = s.num_sms;
   return I8C_OK;
 }
 
@@ -114,8 +123,9 @@ extern "C" i8c_status i8c_conv2d_fprop_noalloc(const int8_t* x, const int8_t* f,
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return status_of(e);
-  DeviceSetup ds;
-  st = setup_device(dev, &ds);
+  unsigned char* scratch = nullptr;
+  int num_sms = 0;
+  st = setup_device(dev, &scratch, &num_sms);
   if (st != I8C_OK) return st;
   EncodeTiled encode = encode_fn();
   if (encode == nullptr) return I8C_ERR_CUDA;
@@ -134,8 +144,8 @@ extern "C" i8c_status i8c_conv2d_fprop_noalloc(const int8_t* x, const int8_t* f,
   int tmem_cols = 32;
   while (tmem_cols < acc_buffers * bn + run_cols) tmem_cols <<= 1;
 
-  int* status = reinterpret_cast<int*>(ds.scratch);
-  uint16_t* f16 = reinterpret_cast<uint16_t*>(ds.scratch + kStatusBytes);
+  int* status = reinterpret_cast<int*>(scratch);
+  uint16_t* f16 = reinterpret_cast<uint16_t*>(scratch + kStatusBytes);
 
   cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(s.K), static_cast<cuuint64_t>(num_slices)};
   cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(s.K) * 64};
@@ -184,9 +194,42 @@ extern "C" i8c_status i8c_conv2d_fprop_noalloc(const int8_t* x, const int8_t* f,
   p.acc_buffers = acc_buffers;
   p.tmem_cols = static_cast<uint32_t>(tmem_cols);
   p.img_stride = static_cast<int64_t>(s.C) * s.H * s.W;
-  p.timeout_ns = 2000000000ull;
+  int debug_flags = 0, timeout_us = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    debug_flags = g_debug_flags;
+    timeout_us = g_timeout_us;
+  }
+  p.timeout_ns = static_cast<uint64_t>(timeout_us > 0 ? timeout_us : 2000000) * 1000ull;
   p.out_mode = 0;
-  p.debug_flags = 0;
-  const int ctas = ds.num_sms < p.num_tiles ? ds.num_sms : p.num_tiles;
+  p.debug_flags = debug_flags;
+  const int ctas = num_sms < p.num_tiles ? num_sms : p.num_tiles;
   return status_of(i8c::launch_conv(bn, tmap, p, ctas, stream));
 }
+
+namespace i8c {
+
+int noalloc_take_status(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return I8C_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_setup[dev].used) return I8C_OK;
+  }
+  int h = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&h, g_noalloc_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return status_of(e);
+  if (h != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof(int), 0, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return status_of(e);
+  }
+  return h;
+}
+
+void noalloc_set_debug(int debug_flags, int timeout_us) {
+  std::lock_guard<std::mutex> lock(g_setup_mu);
+  g_debug_flags = debug_flags;
+  g_timeout_us = timeout_us;
+}
+
+}  // namespace i8c

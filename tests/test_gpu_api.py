@@ -81,6 +81,43 @@ def test_host_buffer_run(torch_cuda):
     assert np.array_equal(yh.numpy(), y_ref.reshape(-1))
 
 
+def test_host_buffer_pipelined_runs(torch_cuda):
+    """i8c_plan_run_host_pipelined: five end-to-end runs on pinned host
+    buffers with different inputs, alphas and outputs, the copies of
+    neighbouring runs overlapped on the plan's copy streams: every output
+    exact against the oracle once the caller's stream is synchronised."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 18, 18, 128, 3, 3, 1, 1, 1, 1, 1, 1)
+    N, C, H, W, K = shape[:5]
+    plan = ext.Plan(shape, host_staging=2)
+    xs, fs, ys, alphas, refs = [], [], [], [], []
+    for i in range(5):
+        x = synth.uniform_int8(40 + i, N * C * H * W, -128, 127).reshape(N, C, H, W)
+        f = synth.uniform_int8(50 + i, K * C * 9, -128, 127).reshape(K, C, 3, 3)
+        alpha = 2.0 ** -(9 + i)
+        y_ref, _ = gpu_util.oracle_packed(shape, x, f, alpha)
+        xp, fp = gpu_util.packed_inputs(x, f)
+        xs.append(torch.from_numpy(xp).pin_memory())
+        fs.append(torch.from_numpy(fp).pin_memory())
+        ys.append(torch.full((y_ref.size,), 77, dtype=torch.int8).pin_memory())
+        alphas.append(alpha)
+        refs.append(y_ref.reshape(-1))
+    stream = torch.cuda.Stream()
+    plan.run_host_pipelined(xs, fs, ys, alphas, stream)
+    stream.synchronize()
+    assert plan.status(stream) == 0
+    for i in range(5):
+        assert np.array_equal(ys[i].numpy(), refs[i]), i
+    plan.destroy()
+    with pytest.raises(ext.I8ConvError):      # a plan without the second staging set
+        p1 = ext.Plan(shape, host_staging=1)
+        try:
+            p1.run_host_pipelined(xs[:1], fs[:1], ys[:1], alphas[:1], stream)
+        finally:
+            p1.destroy()
+
+
 def test_misaligned_pointer_rejected(torch_cuda):
     import ctypes
     import int8_implicit_gemm_gb300 as ext
@@ -118,6 +155,84 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
     y2, _ = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, want_acc=False)
     assert np.array_equal(y2, y_ref)
+
+
+def test_one_shot_timeout_reported_by_last_device_status(torch_cuda):
+    """A bounded wait that runs out inside a checked one-shot call (a producer
+    skips one arrival on purpose, through the one-shot test hook) surfaces as
+    I8C_ERR_TIMEOUT from i8c_last_device_status on that call's stream, once;
+    after the hook is removed the next one-shot call is bit-exact."""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    shape = (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x = synth.uniform_int8(16, 2 * 64 * 256, -128, 127).reshape(2, 64, 16, 16)
+    f = synth.uniform_int8(17, 64 * 64 * 9, -128, 127).reshape(64, 64, 3, 3)
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
+    acc = torch.zeros(2 * 64 * 256, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    try:
+        ext.i8c_debug_set_oneshot(ext.I8C_DEBUG_SKIP_FIRST_ARRIVE, 20000)
+        ext.i8c_conv2d_fprop(xd, fd, y, shape, 1.0, stream)
+        assert ext.i8c_last_device_status(stream) == ext.I8C_ERR_TIMEOUT
+        assert ext.i8c_last_device_status(stream) == ext.I8C_OK      # read once, then cleared
+        ext.i8c_conv2d_fprop_acc(xd, fd, acc, shape, stream)
+        assert ext.i8c_last_device_status(stream) == ext.I8C_ERR_TIMEOUT
+    finally:
+        ext.i8c_debug_set_oneshot(0, 0)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    ext.i8c_conv2d_fprop(xd, fd, y, shape, 2.0 ** -10, stream)
+    ext.i8c_conv2d_fprop_acc(xd, fd, acc, shape, stream)
+    assert ext.i8c_last_device_status(stream) == ext.I8C_OK
+    assert np.array_equal(y.cpu().numpy(), y_ref.reshape(-1))
+    assert np.array_equal(acc.cpu().numpy(), acc_ref.astype(np.int32).reshape(-1))
+
+
+def test_one_shot_plan_cache_is_bounded(torch_cuda):
+    """A caller that keeps presenting new cache keys (a new shape or a new
+    stream for every call) cannot grow the one-shot plan cache beyond its
+    bound: the least recently used plan makes room, and every call stays
+    exact.  (Shapes stand in for streams here: torch hands out its streams
+    from a small pool, so new torch streams would repeat keys.)"""
+    import int8_implicit_gemm_gb300 as ext
+    torch = torch_cuda
+    stream = torch.cuda.current_stream()
+    ext.i8c_debug_set_oneshot(0, 0)          # starts from an empty cache
+    for i in range(70):
+        shape = (1, 32, 6 + i % 10, 6 + i // 10, 32, 3, 3, 1, 1, 1, 1, 1, 1)
+        N, C, H, W, K = shape[:5]
+        x = synth.uniform_int8(18 + i, C * H * W, -128, 127).reshape(1, C, H, W)
+        f = synth.uniform_int8(19, K * C * 9, -128, 127).reshape(K, C, 3, 3)
+        y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -9)
+        xp, fp = gpu_util.packed_inputs(x, f)
+        xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+        y = torch.zeros(y_ref.size, dtype=torch.int8, device="cuda")
+        ext.i8c_conv2d_fprop(xd, fd, y, shape, 2.0 ** -9, stream)
+        assert ext.i8c_last_device_status(stream) == ext.I8C_OK
+        assert np.array_equal(y.cpu().numpy(), y_ref.reshape(-1)), i
+        assert ext.i8c_oneshot_cached_plans() == min(i + 1, 64)
+    ext.i8c_debug_set_oneshot(0, 0)
+    assert ext.i8c_oneshot_cached_plans() == 0
+
+
+@pytest.mark.parametrize("opts", [{}, dict(kernel_variant=1), dict(kernel_variant=2), dict(kernel_variant=3),
+                                  dict(kernel_variant=4), dict(kernel_variant=5)],
+                         ids=["auto", "gather", "halo", "halo-pair", "transposed", "transposed-pair"])
+def test_host_layout_matches_real_plans(torch_cuda, opts):
+    """The layout the host-only planner reports (the one the CPU bounds check
+    inspects) is the layout real plans give their kernels on this GPU."""
+    import int8_implicit_gemm_gb300 as ext
+    sms = torch_cuda.cuda.get_device_properties(0).multi_processor_count
+    for wl in synth.WORKLOADS:
+        shape = wl.shape_tuple()
+        try:
+            plan = ext.Plan(shape, **opts)
+        except ext.I8ConvError as e:
+            assert e.status == ext.I8C_ERR_UNSUPPORTED
+            continue
+        assert plan.layout() == ext.i8c_plan_layout(shape, sms, **opts), wl.name
+        plan.destroy()
 
 
 def test_plan_runs_captured_in_a_cuda_graph(torch_cuda):

@@ -44,7 +44,7 @@ def _page4_tolerance():
 
 
 def _check(y, ref, mag, terms):
-    orc = oracle.Oracle
+    orc = oracle.Oracle()
     diff = np.abs(y.astype(np.float64) - ref)
     assert np.all(diff <= orc.f32_error_bound(mag, terms)), float(np.max(diff))
     atol, rtol = _page4_tolerance()
