@@ -3,7 +3,9 @@
 
 One step = one i8c_plan_run (fp16 filter staging kernel + the tcgen05
 implicit-GEMM kernel) over one batch of the synthetic workload, inputs
-resident in HBM.  Prints one JSON line (rank 0).
+resident in HBM.  The default workload is the largest of the five, the
+dilated 5x9 layer of the kernel-benchmark trace (N=8 C=32 512x512 K=64).
+Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--all]
   python bench.py --impl reference ...   # the CPU oracle, timed on the host
@@ -31,7 +33,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "INT8 conv fprop TOPS (1 GB300) and % of dense INT8 tensor-core roofline"
-DEFAULT_WORKLOAD = "n8c256h56k256r3s1"
+DEFAULT_WORKLOAD = "n8c32h512k64r5x9d2x3"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_TENSOR_TFLOPS = 1900.0
 
@@ -89,9 +91,10 @@ def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
     return world * units_per_rank / (ms_per_step * 1e-3)
 
 
-def dram_traffic(workload: str):
-    """Per-launch DRAM bytes of the workload's kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+def ncu_counters(workload: str):
+    """The workload's kernel counters from the committed ncu summary (DRAM
+    bytes per launch, tensor-pipe and DRAM throughput percentages), if they
+    were taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "conv_fprop_dram_traffic.json")
     try:
         with open(path) as fh:
@@ -101,7 +104,34 @@ def dram_traffic(workload: str):
     entry = d.get("workloads", {}).get(workload)
     if entry is None or entry.get("source_digest") != kernel_source_digest(workload):
         return None
-    return entry.get("bytes_per_launch")
+    return entry
+
+
+def dram_traffic(workload: str):
+    """Per-launch DRAM bytes of the workload's kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    entry = ncu_counters(workload)
+    return None if entry is None else entry.get("bytes_per_launch")
+
+
+# The tensor-core engine the int8 path runs on (tcgen05 kind::f16): the engine
+# probe measured 128 SM cycles per M = 128, N = 256, K = 16 MMA, that is
+# 128*256*16 / 128 = 4096 multiply-adds, or 8192 ops, per SM cycle.
+ENGINE_OPS_PER_SM_CLOCK = 2 * 128 * 256 * 16 / 128
+
+
+def engine_peak(sms: int):
+    """Peak of the engine actually used: ops per SM clock x SMs x the maximum
+    SM clock (MEASURED_PEAKS.json's sm_max_mhz, else 2070 MHz)."""
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            mhz = float(json.load(fh)["sm_max_mhz"])
+    except Exception:
+        pass
+    return ENGINE_OPS_PER_SM_CLOCK * sms * mhz * 1e6 / 1e12, (
+        f"tcgen05 kind::f16 at 8192 ops per SM cycle (engine probe: 128 cycles per 128x256x16 MMA) x {sms} SMs "
+        f"x {mhz:.0f} MHz")
 
 
 class ClockSampler:
@@ -181,53 +211,6 @@ def cpu_oracle_rate(wl, budget_s: float, max_images: int | None = None):
         n_img = min(limit, n_img * 4 if dt < budget_s / 16 else n_img * 2)
     sample = f"{n_img} of {wl.N} images, all {wl.K} output channels ({done_ops / 2:.3g} multiply-adds)"
     return done_ops / elapsed / 1e12, cores, sample, elapsed
-
-
-def e2e_pipelined(ext, plan, xh, fh, yh, alpha, steps):
-    """ms per step of `steps` end-to-end steps from pinned host buffers:
-    every step copies x and f in, runs the plan and copies y out.  Copies in,
-    runs and copies out each have a stream; two device staging sets alternate,
-    and events order the reuse of each set (its input copy waits for the run
-    two steps back to have read it, its run waits for that run's output copy
-    to have read y).  Runs share the plan and stay on one stream."""
-    import torch
-    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    bufs = [(torch.empty_like(xh, device="cuda"), torch.empty_like(fh, device="cuda"),
-             torch.empty_like(yh, device="cuda")) for _ in range(2)]
-    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
-    in_done, run_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-
-    def step(i):
-        b = i & 1
-        xd, fd, yd = bufs[b]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(run_done[b])
-            xd.copy_(xh, non_blocking=True)
-            fd.copy_(fh, non_blocking=True)
-            in_done[b].record(s_in)
-        s_run.wait_event(in_done[b])
-        if i >= 2:
-            s_run.wait_event(out_done[b])
-        plan.run(xd, fd, yd, alpha, s_run)
-        run_done[b].record(s_run)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(run_done[b])
-            yh.copy_(yd, non_blocking=True)
-            out_done[b].record(s_out)
-
-    for i in range(4):  # warm-up
-        step(i)
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(s_in)
-    for i in range(steps):
-        step(i)
-    t1.record(s_out)
-    torch.cuda.synchronize()
-    if plan.status(s_run) != 0:
-        raise RuntimeError("device status not ok after the end-to-end steps")
-    return t0.elapsed_time(t1) / steps
 
 
 def run_ours(args, wl, rank, world):
@@ -345,9 +328,13 @@ def run_ours(args, wl, rank, world):
     ms_per_step = total_ms / args.steps
     value = job_rate(ops, world, ms_per_step) / 1e12
 
-    # end to end through the C-ABI on pinned host buffers: H2D of x and f,
-    # the run, D2H of y, every step
-    plan_h = ext.Plan(shape, host_staging=True)
+    # End to end through the C-ABI on pinned host buffers: every step copies
+    # x and f in, runs and copies y out.  i8c_plan_run_host_pipelined
+    # overlaps step i's run with step i+1's input copy and step i-1's output
+    # copy (the plan's two staging sets and copy streams); the serial form
+    # (i8c_plan_run_host: copy in, run, copy out on one stream) is reported
+    # beside it.
+    plan_h = ext.Plan(shape, host_staging=2)
     xh = x0.cpu().pin_memory()
     fh = f0.cpu().pin_memory()
     yh = torch.empty(y_bytes, dtype=torch.int8).pin_memory()
@@ -363,19 +350,25 @@ def run_ours(args, wl, rank, world):
     torch.cuda.synchronize()
     assert plan_h.status(stream) == 0
     e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
+    plan_h.run_host_pipelined([xh] * 4, [fh] * 4, [yh] * 4, [wl.alpha] * 4, stream)  # warm-up
+    torch.cuda.synchronize()
+    e0.record(stream)
+    plan_h.run_host_pipelined([xh] * e2e_steps, [fh] * e2e_steps, [yh] * e2e_steps, [wl.alpha] * e2e_steps, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert plan_h.status(stream) == 0
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
     plan_h.destroy()
-    # The same steps pipelined: each step's H2D copy, run and D2H copy on
-    # three streams with double-buffered device staging, so that step i's run
-    # overlaps step i+1's input copy and step i-1's output copy.
-    e2e_ms = e2e_pipelined(ext, plan, xh, fh, yh, wl.alpha, e2e_steps)
 
     peak, peak_note = tensor_peak()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    epeak, epeak_note = engine_peak(sms)
     kernel_name = {1: "conv_fprop_tc_kernel", 4: "conv_fprop_tr_kernel", 5: "conv_fprop_tr_kernel"}.get(
-        plan.info["kernel_variant"],
-                                                                           "conv_fprop_halo_kernel")
+        plan.info["kernel_variant"], "conv_fprop_halo_kernel")
     kern_avg_ms = kern_ms / max(1, kern_n)
     achieved = ops / (kern_avg_ms * 1e-3) / 1e12
-    traffic = dram_traffic(wl.name)
+    counters = ncu_counters(wl.name)
+    traffic = None if counters is None else counters.get("bytes_per_launch")
     result = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -400,11 +393,17 @@ def run_ours(args, wl, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_name, "kernel_ms": round(kern_avg_ms, 6),
-                     "note": f"int8 ops (2*N*K*P*Q*C*R*S) per launch / CUDA-event duration; peak {peak_note}"},
+                     "algorithmic_bytes": x_bytes + f_bytes + y_bytes,
+                     "engine_peak": round(epeak, 1), "frac_engine": round(achieved / epeak, 4),
+                     "ncu": None if counters is None else {
+                         k: counters.get(k) for k in ("tensor_pipe_active_pct", "dram_gbs", "duration_us", "source")},
+                     "note": f"int8 ops (2*N*K*P*Q*C*R*S) per launch / CUDA-event duration of the convolution kernel "
+                             f"(events on the launch stream around each launch); peak {peak_note}; engine_peak "
+                             f"{epeak_note}"},
         "e2e": {"value": round(ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS", "ms_per_step": round(e2e_ms, 6),
                 "h2d_bytes_per_step": x_bytes + f_bytes, "d2h_bytes_per_step": y_bytes,
-                "path": "i8c_plan_run on double-buffered device staging; H2D of x and f from pinned host memory and "
-                        "D2H of y on their own streams, overlapped across steps",
+                "path": "i8c_plan_run_host_pipelined (C-ABI): H2D of x and f from pinned host memory and D2H of y "
+                        "on the plan's copy streams with two device staging sets, overlapped across steps",
                 "serial_ms_per_step": round(e2e_serial_ms, 6),
                 "serial_path": "i8c_plan_run_host (copy in, run, copy out on one stream)"},
         "gpu_launches": launches,
