@@ -70,6 +70,11 @@ struct HaloParams {
   uint16_t* f16;
   int64_t f_vecs;           // 16-element vectors of the filter
   uint32_t* gbar;           // {arrivals, generation}, arrivals zero between launches
+  // Stacked-tap kernel (64 output channels): tiles of 128 consecutive output
+  // columns of one row, vq of them valid, tq per output row; the halo is one
+  // segment of seg_len input columns per filter row; slots = MMAs (tap pairs
+  // and an odd last tap) per filter row and 16-channel half.
+  int seg_len, vq, tq, slots;
 };
 
 

@@ -44,6 +44,7 @@ struct i8c_plan {
   int* split_count;      // halo kernel, split tail tiles: arrivals per tile and CTA rank
   int32_t* split_part;   // halo kernel, split tail tiles: int32 partial sums
   size_t x_bytes, f_bytes, y_bytes;
+  size_t f16_bytes;  // the fp16 filter copy
   int64_t workspace_bytes;
   // optional per-launch timing of the convolution kernel
   std::vector<cudaEvent_t> ev_start, ev_end;
@@ -53,6 +54,9 @@ struct i8c_plan {
 namespace {
 
 constexpr int64_t kMaxI32 = 2147483647LL;
+// Whether the automatic plan takes the stacked-tap kernel for the 64-channel
+// layers it suits (with a resident filter).
+constexpr bool kStackAuto = false;
 
 i8c_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return I8C_OK;
@@ -277,6 +281,59 @@ bool tr_layout(const i8c_conv_shape& s, int P, int np, int cg, int want_g, int n
   return false;
 }
 
+// Layout of the stacked-tap kernel (64 output channels, stride 1, CTA
+// pairs): per 32-channel block a halo of R segments of L = 128 + (S-1)*dw
+// input positions (one per filter row), two or three halo stages, the
+// epilogue's shift buffers, and filter stages of one filter row's U = ceil(S/2)
+// slots of 64 fp16 rows per CTA.  The filter is kept resident when all
+// (C/32)*R stages fit: three halo stages when that still holds, else two.
+// Returns false when the shape does not suit the kernel or nothing fits.
+bool stack_layout(const i8c_conv_shape& s, int P, int Q, i8c::HaloParams* h, int* smem_bytes) {
+  if (s.K != 64 || s.stride_h != 1 || s.stride_w != 1 || s.S < 2 || s.S > 16 || s.dil_w > 8) return false;
+  *h = i8c::HaloParams{};
+  const int U = (s.S + 1) / 2;
+  const int64_t L = 128 + static_cast<int64_t>(s.S - 1) * s.dil_w;
+  const int64_t npos = static_cast<int64_t>(s.R) * L;
+  const int vq = 128 - s.dil_w;
+  const int64_t tq = (static_cast<int64_t>(Q) + vq - 1) / vq;
+  const int64_t tiles = static_cast<int64_t>(s.N) * P * tq;
+  if (npos > 65536 || tiles > kMaxI32 - 1) return false;
+  h->seg_len = static_cast<int>(L);
+  h->vq = vq;
+  h->tq = static_cast<int>(tq);
+  h->slots = U;
+  h->num_patches = static_cast<int>(tiles);
+  h->HR = s.R;
+  h->CW = static_cast<int>(L);
+  h->positions = static_cast<int>(npos);
+  h->plane_bytes = (static_cast<uint32_t>(npos) * 16 + 127) / 128 * 128;
+  h->halo_bytes = 4 * h->plane_bytes;
+  h->phase_off[0] = 0;
+  h->phase_off[1] = static_cast<int>(L);
+  h->bgroup = U;
+  const int budget = i8c::kMaxDynamicSmem - 1024 - i8c::kHaloBarBytes;
+  const int64_t stage = static_cast<int64_t>(U) * 64 * 64;
+  const int stages = (s.C / 32) * s.R;
+  int64_t nbs_for[4] = {0, 0, 0, 0}, off_b_for[4] = {0, 0, 0, 0};
+  for (int nhs = 2; nhs <= 3; ++nhs) {
+    off_b_for[nhs] = (static_cast<int64_t>(nhs) * h->halo_bytes + i8c::kStackXbufBytes + 1023) / 1024 * 1024;
+    const int64_t n = (budget - off_b_for[nhs]) / stage;
+    nbs_for[nhs] = n > i8c::kMaxBStages ? i8c::kMaxBStages : n;
+  }
+  int nhs = nbs_for[3] >= stages ? 3 : 2;
+  if (nbs_for[nhs] < (stages < 2 ? stages : 2)) return false;
+  h->nhs = nhs;
+  h->nstg = 0;
+  h->resident = nbs_for[nhs] >= stages ? 1 : 0;
+  h->nbs = static_cast<int>(h->resident ? stages : nbs_for[nhs]);
+  h->off_stg = static_cast<uint32_t>(nhs * h->halo_bytes);
+  h->off_out = h->off_stg;
+  h->off_b = static_cast<uint32_t>(off_b_for[nhs]);
+  h->off_bar = static_cast<uint32_t>(off_b_for[nhs] + static_cast<int64_t>(h->nbs) * stage);
+  *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
+  return true;
+}
+
 void free_plan_memory(i8c_plan* p) {
   for (cudaEvent_t e : p->ev_start) cudaEventDestroy(e);
   for (cudaEvent_t e : p->ev_end) cudaEventDestroy(e);
@@ -341,7 +398,10 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
                     cudaStream_t stream, const i8c_epilogue* ep = nullptr) {
   const i8c_conv_shape& s = pl->shape;
   cudaError_t e = cudaSuccess;
-  if (pl->gbar == nullptr) {  // else the halo kernel converts the filter itself
+  if (pl->kernel_variant == 6) {
+    e = i8c::launch_filter_to_f16_stacked(f, pl->f16, s.C / 32, s.R, s.S, stream);
+    if (e != cudaSuccess) return from_cuda(e);
+  } else if (pl->gbar == nullptr) {  // else the halo kernel converts the filter itself
     e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
     if (e != cudaSuccess) return from_cuda(e);
   }
@@ -368,7 +428,8 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
       hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
       hp.gbar = pl->gbar;
     }
-    e = pl->kernel_variant == 5   ? i8c::tr_launch_pair(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+    e = pl->kernel_variant == 6   ? i8c::stack_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 5 ? i8c::tr_launch_pair(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
         : pl->kernel_variant == 4 ? i8c::tr_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
         : pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
                                                           stream)
@@ -439,7 +500,7 @@ bool options_valid(const i8c_options& o) {
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256) return false;
   return !(o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
            o.timing_events < 0 || o.timing_events > 65536 || o.host_staging < 0 || o.host_staging > 2 ||
-           o.kernel_variant < 0 || o.kernel_variant > 5 || o.halo_loads < 0 || o.halo_loads > 2 ||
+           o.kernel_variant < 0 || o.kernel_variant > 6 || o.halo_loads < 0 || o.halo_loads > 2 ||
            o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
            o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
            (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)));
@@ -457,6 +518,51 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
   p->P = static_cast<int>(P);
   p->Q = static_cast<int>(Q);
   p->M = static_cast<int64_t>(s.N) * P * Q;
+  if (o.kernel_variant == 6 || (kStackAuto && o.kernel_variant == 0 && o.block_n == 0 && o.halo_loads == 0 &&
+                                 o.tile_shape == 0 && o.tail_split == 0 && o.fused_filter == 0 && o.tile_px == 0 &&
+                                 o.filter_run == 0)) {
+    // The stacked-tap kernel: two taps per N = 128 MMA on CTA pairs.
+    int smem = 0;
+    if (!stack_layout(s, p->P, p->Q, &p->halo, &smem) || (o.kernel_variant == 0 && !p->halo.resident)) {
+      if (o.kernel_variant == 6) return I8C_ERR_UNSUPPORTED;
+      p->halo = i8c::HaloParams{};
+    } else {
+      p->kernel_variant = 6;
+      p->cta_group = 2;
+      p->block_n = 64;
+      p->num_n_tiles = 1;
+      const int64_t units = (static_cast<int64_t>(p->halo.num_patches) + 1) / 2;
+      p->num_m_tiles = static_cast<int>(units);
+      p->num_tiles = static_cast<int>(units);
+      p->halo.ksplit = 1;
+      p->halo.nsplit = 1;
+      p->halo.full_units = p->num_tiles;
+      p->halo.num_units = p->num_tiles;
+      p->split_tiles = 0;
+      int g = ctas / 2;
+      if (!host_only) {
+        if (i8c::stack_prepare() != cudaSuccess) return I8C_ERR_CUDA;
+        const int fit = i8c::stack_max_clusters(p->halo.slots, smem);
+        if (fit < 1) return I8C_ERR_UNSUPPORTED;
+        if (g > fit) g = fit;
+      }
+      if (g < 1) g = 1;
+      p->num_ctas = 2 * (g < p->num_tiles ? g : p->num_tiles);
+      // chunks of whole filter rows: a column gathers at most U taps x 32
+      // channels per row, so 32 / U rows stay within 1024 products
+      const int U = p->halo.slots;
+      int rows = 32 / U;
+      if (o.max_chunk_slices > 0) rows = o.max_chunk_slices / U < rows ? o.max_chunk_slices / U : rows;
+      if (rows < 1) rows = 1;
+      p->num_slices = (s.C / 32) * s.R * s.S;
+      p->chunk_slices = rows;  // filter rows per chunk for this kernel
+      p->num_chunks = ((s.C / 32) * s.R + rows - 1) / rows;
+      p->acc_buffers = 2;
+      p->tmem_cols = 256;
+      p->smem_bytes = smem;
+      return I8C_OK;
+    }
+  }
   // Kernel and tile width.  The halo kernel (16x8 output patches) is preferred
   // whenever its halo fits in shared memory; its tile width is the one with
   // the best wave efficiency (ties go to the wider tile).  Variant 3 runs it
@@ -833,12 +939,19 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   p->f_bytes = static_cast<size_t>(s.K) * s.C * s.R * s.S;
   p->y_bytes = static_cast<size_t>(s.N) * s.K * P * Q;
 
-  e = p->kernel_variant == 5   ? i8c::tr_prepare_pair()
+  e = p->kernel_variant == 6   ? i8c::stack_prepare()
+      : p->kernel_variant == 5 ? i8c::tr_prepare_pair()
       : p->kernel_variant == 4 ? i8c::tr_prepare()
       : p->kernel_variant == 3 ? i8c::halo_prepare_pair(bn)
       : p->kernel_variant == 2 ? i8c::halo_prepare_single(bn)
                                : i8c::conv_prepare(bn);
-  if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f_bytes * 2);
+  // the fp16 filter copy: the int8 filter's order, or the stacked-tap
+  // kernel's [C/32][R][2][ceil(S/2)][64][32] (one slot more per row and rank
+  // pair when S is odd)
+  p->f16_bytes = p->kernel_variant == 6
+                     ? static_cast<size_t>(s.C / 32) * s.R * 2 * ((s.S + 1) / 2) * 64 * 32 * 2
+                     : p->f_bytes * 2;
+  if (e == cudaSuccess) e = cudaMalloc(&p->f16, p->f16_bytes);
   if (e == cudaSuccess) e = cudaMalloc(&p->status, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(p->status, 0, sizeof(int));
   if (e == cudaSuccess && p->kernel_variant == 2 && o.fused_filter == 1) {
@@ -853,7 +966,7 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
       if (e == cudaSuccess) e = cudaMemset(p->gbar, 0, 2 * sizeof(uint32_t));
     }
   }
-  p->workspace_bytes = static_cast<int64_t>(p->f_bytes * 2 + sizeof(int));
+  p->workspace_bytes = static_cast<int64_t>(p->f16_bytes + sizeof(int));
   if (e == cudaSuccess && split_bytes > 0) {
     const size_t counts = sizeof(int) * static_cast<size_t>(p->split_tiles) * p->cta_group;
     e = cudaMalloc(&p->split_part, static_cast<size_t>(split_bytes));
@@ -905,6 +1018,15 @@ i8c_status i8c_plan_create(const i8c_conv_shape* shape, const i8c_options* opts,
   cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(s.K) * 64};
   cuuint32_t box[3] = {32, static_cast<cuuint32_t>(bn / p->cta_group),
                        static_cast<cuuint32_t>(p->kernel_variant >= 2 ? p->halo.bgroup : 1)};
+  if (p->kernel_variant == 6) {
+    // the stacked copy: slots of 64 rows; a box is one filter row's U slots of one rank
+    const int U = p->halo.slots;
+    dims[1] = 64;
+    dims[2] = static_cast<cuuint64_t>(s.C / 32) * s.R * 2 * U;
+    strides[1] = 64 * 64;
+    box[1] = 64;
+    box[2] = static_cast<cuuint32_t>(U);
+  }
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p->f16, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -932,7 +1054,7 @@ void fill_layout(const i8c_plan* pl, i8c_layout* L) {
   if (pl->kernel_variant >= 2) {
     const i8c::HaloParams& h = pl->halo;
     L->flat_tiles = h.flat;
-    L->tile_px = h.flat ? h.tile_px : 0;
+    L->tile_px = h.flat ? h.tile_px : pl->kernel_variant == 6 ? h.vq : 0;
     L->halo_rows = h.HR;
     L->halo_cw = h.CW;
     L->positions = h.positions;
@@ -945,7 +1067,9 @@ void fill_layout(const i8c_plan* pl, i8c_layout* L) {
     L->off_filter = static_cast<int32_t>(h.off_b);
     L->filter_stages = h.nbs;
     L->filter_run = h.bgroup;
-    const int rows = pl->kernel_variant >= 4 ? 128 : pl->block_n / pl->cta_group;  // transposed: 128 channels per CTA
+    // rows per K-slice of a stage: transposed tiles 128 channels, the stacked
+    // kernel a slot of 64 rows, the halo kernel the CTA's share of the tile
+    const int rows = pl->kernel_variant == 6 ? 64 : pl->kernel_variant >= 4 ? 128 : pl->block_n / pl->cta_group;
     L->filter_stage_bytes = h.bgroup * rows * 64;
     L->off_out = static_cast<int32_t>(h.off_out);
     L->off_bar = static_cast<int32_t>(h.off_bar);
@@ -1011,7 +1135,9 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->M = pl->M;
   info->gemm_n = s.K;
   info->gemm_k = s.C * s.R * s.S;
-  info->block_m = pl->kernel_variant >= 4 ? pl->cta_group * pl->halo.tile_px : 128 * pl->cta_group;
+  info->block_m = pl->kernel_variant == 4 || pl->kernel_variant == 5 ? pl->cta_group * pl->halo.tile_px
+                  : pl->kernel_variant == 6                          ? 2 * pl->halo.vq
+                                                                     : 128 * pl->cta_group;
   info->block_n = pl->block_n;
   info->num_tiles = pl->num_tiles;
   info->num_ctas = pl->num_ctas;

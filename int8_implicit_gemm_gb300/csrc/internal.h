@@ -45,6 +45,16 @@ cudaError_t tr_launch_pair(const CUtensorMap& tmap, const HaloParams& p, int sme
 int tr_pair_max_clusters(int bgroup, int S, int mma_n, int smem_bytes);
 constexpr int kMaxDynamicSmem = 232448;
 
+// stack_kernels.cu: the stacked-tap kernel for 64-output-channel layers (two
+// filter taps per N = 128 MMA, CTA pairs) and its filter conversion into the
+// stacked fp16 order
+cudaError_t stack_prepare();
+cudaError_t stack_launch(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+                         cudaStream_t stream);
+int stack_max_clusters(int slots, int smem_bytes);
+cudaError_t launch_filter_to_f16_stacked(const int8_t* f, uint16_t* f16, int CB, int R, int S, cudaStream_t stream);
+constexpr int kStackXbufBytes = 2 * 8 * 8 * 32 * 4;  // the epilogue's shift buffers (two tiles)
+
 // noalloc.cu: the no-allocation entry point's status word on device `dev`
 // (synchronous; I8C_OK if that entry point has not run there), cleared once
 // read; and the one-shot test hooks (debug flags, bounded-wait limit in us).

@@ -136,7 +136,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     """A producer skips one arrival on purpose: the MMA warp's wait runs out
     after 20 ms, every role stops, the kernel returns and the plan reports
     I8C_ERR_TIMEOUT (gather kernel, halo kernel, halo kernel on CTA pairs,
-    transposed tiles, on single CTAs and on pairs).
+    transposed tiles, on single CTAs and on pairs, stacked taps).
     The same context then runs a correct convolution."""
     import int8_implicit_gemm_gb300 as ext
     torch = torch_cuda
@@ -146,7 +146,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     xp, fp = gpu_util.packed_inputs(x, f)
     xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
     y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
-    for kernel in (1, 2, 3, 4, 5):
+    for kernel in (1, 2, 3, 4, 5, 6):
         bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE,
                        kernel_variant=kernel)
         bad.run(xd, fd, y, 1.0)
@@ -217,8 +217,8 @@ def test_one_shot_plan_cache_is_bounded(torch_cuda):
 
 
 @pytest.mark.parametrize("opts", [{}, dict(kernel_variant=1), dict(kernel_variant=2), dict(kernel_variant=3),
-                                  dict(kernel_variant=4), dict(kernel_variant=5)],
-                         ids=["auto", "gather", "halo", "halo-pair", "transposed", "transposed-pair"])
+                                  dict(kernel_variant=4), dict(kernel_variant=5), dict(kernel_variant=6)],
+                         ids=["auto", "gather", "halo", "halo-pair", "transposed", "transposed-pair", "stacked"])
 def test_host_layout_matches_real_plans(torch_cuda, opts):
     """The layout the host-only planner reports (the one the CPU bounds check
     inspects) is the layout real plans give their kernels on this GPU."""

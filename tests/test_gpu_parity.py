@@ -88,6 +88,22 @@ def _extreme_data(shape):
     return x, f
 
 
+@pytest.mark.parametrize("kw", [dict(kernel_variant=6), dict(kernel_variant=6, max_chunk_slices=6)],
+                         ids=["stacked", "stacked-short-chunks"])
+def test_extreme_magnitudes_exact_stacked(kw):
+    """The stacked-tap kernel (64 output channels, two taps per MMA): chunks
+    of 16 filter rows of a 3x3 filter put 16 x 2 taps x 32 channels = 1024
+    products near 2^14 into a column, sums at 2^24, and the int32 running
+    sums of both column blocks must add up exactly."""
+    shape = (1, 1024, 8, 8, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x, f = _extreme_data(shape)
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -20)
+    assert np.abs(acc_ref).max() > 2 ** 27
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -20, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
 @pytest.mark.parametrize("kw", [dict(kernel_variant=1), dict(kernel_variant=2), dict(kernel_variant=2, block_n=64),
                                 dict(kernel_variant=3), dict(kernel_variant=3, block_n=256),
                                 dict(kernel_variant=4), dict(kernel_variant=4, tile_px=256),
@@ -159,8 +175,9 @@ def _full_oracle(wl):
 
 
 @pytest.mark.parametrize("kw", [{}, dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
-                                dict(kernel_variant=3), dict(kernel_variant=4), dict(kernel_variant=5)],
-                         ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair"])
+                                dict(kernel_variant=3), dict(kernel_variant=4), dict(kernel_variant=5),
+                                dict(kernel_variant=6)],
+                         ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair", "stacked"])
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
 def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
@@ -372,3 +389,70 @@ def test_resident_filter_exact(shape, opts):
     y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **opts)
     assert np.array_equal(acc, acc_ref.astype(np.int32))
     assert np.array_equal(y, y_ref)
+
+
+STACKED_SHAPES = [
+    # N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw        (K = 64, stride 1)
+    (2, 32, 40, 300, 64, 5, 9, 2, 4, 1, 1, 2, 3),       # the dilated 5x9 layer's geometry, ragged row tiles
+    (2, 32, 17, 130, 64, 3, 3, 1, 1, 1, 1, 1, 1),       # odd S, shift 1, two tiles per row
+    (1, 64, 9, 250, 64, 2, 2, 0, 1, 1, 1, 1, 2),        # even S (no single tap), two channel blocks
+    (3, 96, 6, 40, 64, 3, 5, 1, 2, 1, 1, 1, 1),         # three channel blocks, one tile per row
+    (1, 32, 12, 128, 64, 1, 7, 0, 3, 1, 1, 1, 8),       # R = 1, the largest shift (8)
+    (2, 32, 5, 5, 64, 3, 3, 1, 1, 1, 1, 1, 1),          # tiny image: most of the tile outside the row
+    (1, 32, 6, 200, 64, 4, 16, 1, 7, 1, 1, 1, 1),       # S = 16: eight tap pairs per row
+    (1, 160, 7, 64, 64, 3, 3, 1, 1, 1, 1, 2, 2),        # five channel blocks: several chunks of rows
+]
+
+
+@pytest.mark.parametrize("shape", STACKED_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kw", [dict(), dict(num_ctas=2), dict(num_ctas=6, max_chunk_slices=4)],
+                         ids=["default", "one-pair", "three-pairs-short-chunks"])
+def test_stacked_taps_exact(shape, kw):
+    """The stacked-tap kernel (two filter taps per N = 128 MMA, the second
+    tap's column block shifted by dw pixels in the epilogue, row tiles of
+    128 - dw valid outputs, CTA pairs): every int32 accumulator and int8 output
+    exact, for odd and even filter widths, shifts 1 to 8, several channel
+    blocks and chunks, and few CTAs running many tiles on a resident filter."""
+    x, f = _data(shape, 3131 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, kernel_variant=6, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)
+
+
+@pytest.mark.parametrize("ep", [dict(scale=True, bias=True, relu=True), dict(bias=True)], ids=["scale-bias-relu", "bias"])
+def test_stacked_taps_channel_epilogue(ep):
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 32, 20, 150, 64, 5, 9, 2, 4, 1, 1, 2, 3)
+    N, C, H, W, K = shape[:5]
+    x, f = _data(shape, 4343)
+    orc = oracle.Oracle()
+    acc = orc.conv_acc(x, f, shape)
+    scale, bias = _channel_params(K, 98)
+    alpha = 2.0 ** -10
+    y_ref = orc.requantize_channels(acc, alpha, scale if ep.get("scale") else None,
+                                    bias if ep.get("bias") else None, ep.get("relu", False))
+    xp, fp = gpu_util.packed_inputs(x, f)
+    xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
+    plan = ext.Plan(shape, kernel_variant=6)
+    P, Q = plan.info["P"], plan.info["Q"]
+    y = torch.full((N, K // 32, P, Q, 32), 77, dtype=torch.int8, device="cuda")
+    sd = torch.from_numpy(scale).cuda() if ep.get("scale") else None
+    bd = torch.from_numpy(bias).cuda() if ep.get("bias") else None
+    plan.run(xd, fd, y, alpha, alpha_k=sd, bias=bd, relu=ep.get("relu", False))
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    plan.destroy()
+    assert np.array_equal(y.cpu().numpy(), oracle.nchw_to_ncxhwx32(y_ref))
+
+
+def test_stacked_taps_rejects_unsuited_shapes():
+    import int8_implicit_gemm_gb300 as ext
+    for shape in [(1, 32, 16, 16, 128, 3, 3, 1, 1, 1, 1, 1, 1),     # K != 64
+                  (1, 32, 16, 16, 64, 3, 3, 1, 1, 2, 2, 1, 1),      # stride 2
+                  (1, 32, 16, 16, 64, 3, 1, 1, 0, 1, 1, 1, 1),      # S = 1: no tap pairs
+                  (1, 32, 40, 40, 64, 3, 3, 1, 9, 1, 1, 1, 9)]:     # shift 9 > 8
+        with pytest.raises(ext.I8ConvError) as ei:
+            ext.Plan(shape, kernel_variant=6)
+        assert ei.value.status == ext.I8C_ERR_UNSUPPORTED, shape

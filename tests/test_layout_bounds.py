@@ -22,7 +22,7 @@ off-by-one in a layout must fail the check.
 import pytest
 
 import synth
-from tests.test_gpu_parity import SMALL, TRANSPOSED_EXTRA
+from tests.test_gpu_parity import SMALL, STACKED_SHAPES, TRANSPOSED_EXTRA
 
 KMAX_SMEM = 232448          # opt-in dynamic shared memory per block on sm_103
 KMAX_FILTER_STAGES = 16     # filter stages the kernels have barriers for
@@ -41,6 +41,8 @@ def check_layout(shape, L):
     assert L["smem_bytes"] <= KMAX_SMEM, "shared memory over the per-block limit"
     tc = L["tmem_cols"]
     assert 32 <= tc <= 512 and tc & (tc - 1) == 0, "tensor-memory allocation must be a power of two in [32, 512]"
+    if v == 6:
+        return check_stacked_layout(shape, L)
     assert 1 <= L["chunk_slices"] <= 32, "an exact fp32 chunk holds at most 32 K-slices (1024 products)"
     assert L["num_chunks"] * L["chunk_slices"] >= (C // 32) * R * S
     if v == 1:
@@ -123,6 +125,40 @@ def check_layout(shape, L):
     assert P >= 1 and Q >= 1
 
 
+XBUF_BYTES = 2 * 8 * 8 * 32 * 4   # the stacked kernel's epilogue shift buffers: 2 tiles x 8 warps x 8 lanes x 32 words
+
+
+def check_stacked_layout(shape, L):
+    """The stacked-tap kernel: halo segments of L = 128 + (S-1)*dw positions
+    per filter row, A views of tap pairs 2*dw apart, filter stages of U slots
+    of 64 fp16 rows, the epilogue's shift buffers, 2 x 128 accumulator columns."""
+    N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw = shape
+    assert K == 64 and sh == 1 and sw == 1 and 2 <= S <= 16 and dw <= 8
+    U = (S + 1) // 2
+    seg = 128 + (S - 1) * dw
+    assert L["halo_cw"] == seg and L["halo_rows"] == R and L["positions"] == R * seg
+    assert L["tile_px"] == 128 - dw, "valid outputs per tile"
+    rows = L["chunk_slices"]
+    assert rows >= 1 and rows * U * 32 <= 1024, "a column sums at most 1024 products per chunk"
+    assert L["num_chunks"] * rows >= (C // 32) * R
+    pos, plane = L["positions"], L["plane_bytes"]
+    assert L["halo_bytes"] == 4 * plane and plane % 128 == 0 and plane >= 16 * pos
+    # the furthest A row: segment R-1, the last slot's view ((S-1)*dw), row 127
+    reach = (R - 1) * seg + (S - 1) * dw + 127
+    assert reach < pos, f"an operand view reaches halo position {reach} of {pos}"
+    assert 3 * plane + 16 * reach + 15 < L["halo_bytes"]
+    assert 2 <= L["halo_stages"] <= 3
+    assert L["off_out"] >= L["halo_stages"] * L["halo_bytes"], "shift buffers overlap the halo"
+    assert L["off_out"] + XBUF_BYTES <= L["off_filter"], "shift buffers overlap the filter"
+    assert L["off_filter"] % 1024 == 0
+    assert L["filter_run"] == U and L["filter_stage_bytes"] == U * 64 * 64
+    assert 1 <= L["filter_stages"] <= KMAX_FILTER_STAGES
+    assert L["off_filter"] + L["filter_stages"] * L["filter_stage_bytes"] <= L["off_bar"]
+    assert KHALO_BARRIER_WORDS * 8 <= L["bar_bytes"]
+    assert L["off_bar"] + L["bar_bytes"] + 1024 <= L["smem_bytes"] <= KMAX_SMEM
+    assert L["tmem_cols"] >= 2 * 128
+
+
 PLAN_FORMS = [
     {}, dict(kernel_variant=1), dict(kernel_variant=2), dict(kernel_variant=2, halo_loads=1),
     dict(kernel_variant=2, halo_loads=2), dict(kernel_variant=3), dict(kernel_variant=3, block_n=64),
@@ -132,9 +168,10 @@ PLAN_FORMS = [
     dict(kernel_variant=4, tile_px=256), dict(kernel_variant=4, tile_px=64, filter_run=3),
     dict(kernel_variant=4, halo_loads=1), dict(kernel_variant=5), dict(kernel_variant=5, tile_px=128),
     dict(kernel_variant=5, tile_px=240, halo_loads=1), dict(max_chunk_slices=5), dict(kernel_variant=2, max_chunk_slices=7),
+    dict(kernel_variant=6), dict(kernel_variant=6, max_chunk_slices=4),
 ]
 
-SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + [
+SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + STACKED_SHAPES + [
     (1, 1024, 8, 8, 256, 3, 3, 1, 1, 1, 1, 1, 1), (2, 512, 7, 6, 64, 3, 3, 1, 1, 1, 1, 1, 1),
     (1, 1120, 6, 6, 416, 3, 3, 1, 1, 1, 1, 1, 1), (2, 32, 40, 40, 64, 5, 9, 2, 4, 1, 1, 2, 3)]
 
@@ -168,7 +205,8 @@ def test_every_plan_form_stays_in_bounds(ext, shape):
     assert checked >= 2
 
 
-@pytest.mark.parametrize("plant", ["positions", "plane_bytes", "off_bar", "off_staging", "tmem_cols", "off_out"])
+@pytest.mark.parametrize("plant", ["positions", "plane_bytes", "off_bar", "off_staging", "tmem_cols", "off_out",
+                                   "stacked_positions", "stacked_xbuf"])
 def test_planted_off_by_one_is_caught(ext, plant):
     """Each planted mistake shrinks one region by the smallest step the
     layout allows; the check must notice."""
@@ -179,6 +217,8 @@ def test_planted_off_by_one_is_caught(ext, plant):
         "off_staging": ((2, 64, 13, 11, 64, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, halo_loads=1), None),
         "tmem_cols": ((64, 512, 28, 28, 512, 3, 3, 1, 1, 1, 1, 1, 1), {}, None),
         "off_out": ((8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=4), None),
+        "stacked_positions": ((8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=6), None),
+        "stacked_xbuf": ((8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=6), None),
     }
     shape, opts, _ = cases[plant]
     L = _layout(ext, shape, opts)
@@ -197,5 +237,9 @@ def test_planted_off_by_one_is_caught(ext, plant):
         bad["tmem_cols"] //= 2
     elif plant == "off_out":
         bad["off_out"] -= 1024
+    elif plant == "stacked_positions":   # one halo position short
+        bad["positions"] -= 1
+    elif plant == "stacked_xbuf":        # shift buffers one row into the filter stages
+        bad["off_out"] = L["off_filter"] - XBUF_BYTES + 128
     with pytest.raises(AssertionError):
         check_layout(shape, bad)
