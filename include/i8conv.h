@@ -87,7 +87,10 @@ typedef struct {
                                 MMA's M on the channels; stride 1 only, else
                                 I8C_ERR_UNSUPPORTED), 5 = transposed tiles on CTA pairs (256
                                 output channels, 128 per CTA, x tile_px pixels, each CTA
-                                building the halo of half of them; stride 1 only)            */
+                                building the halo of half of them; stride 1 only), 6 = stacked
+                                taps (64 output channels only, stride 1, 2 <= S <= 16,
+                                dil_w <= 8: two filter taps of a row per N = 128 MMA on CTA
+                                pairs; row tiles of 128 - dil_w output columns)               */
   int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
                                 (currently the same as 2), 1 = int8 staging ring filled by
                                 cp.async ahead of use, 2 = straight into registers (no
@@ -164,7 +167,10 @@ typedef struct {
                                 3 = halo kernel on CTA pairs, 4 = transposed
                                 tiles (block_m = tile_px pixels, block_n = 128
                                 output channels), 5 = transposed tiles on CTA
-                                pairs (block_n = 256)                          */
+                                pairs (block_n = 256), 6 = stacked taps
+                                (block_m = a pair's two row tiles of valid
+                                outputs, block_n = 64; chunk_slices counts
+                                filter rows)                                   */
   int32_t halo_staging;      /* halo kernel: int8 staging slots (0 = loads
                                 straight into registers); 0 for the gather kernel */
   int32_t filter_run;        /* halo kernel: K-slices per filter stage (taps of
