@@ -48,6 +48,27 @@ extern "C" {
 i8c_status i8c_probe_mma_f16(int32_t n, int32_t a_swizzled, int32_t loop_mode, int32_t num_ctas, int32_t iters,
                              long long* cycles, float* elapsed_ms, cudaStream_t stream);
 
+/* The warp-level integer MMA the Ampere configurations use
+ * (mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32: 16 x 8 x 32 int8
+ * multiply-adds per warp instruction, 8192 int8 ops): num_ctas CTAs of
+ * warps_per_cta warps (1-16), each warp issuing iters x 8 MMAs on register
+ * operands into 8 independent accumulators.
+ *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles of the loop
+ *           (twice), 1;  sink: DEVICE int (written only if the accumulators
+ *           come out at an impossible value: keeps them live)
+ *   elapsed_ms: host float, kernel duration from CUDA events on `stream`.
+ * Synchronises `stream`. */
+i8c_status i8c_probe_imma_s8(int32_t num_ctas, int32_t warps_per_cta, int32_t iters, long long* cycles, int* sink,
+                             float* elapsed_ms, cudaStream_t stream);
+
+/* tcgen05.mma.cta_group::1.kind::f8f6f4 with e4m3 A and B and fp32
+ * accumulation (M = 128, N = n in {64, 128, 256}, K = 32: the engine an
+ * exact e4m3 nibble split of int8 operands would use), issued back to back
+ * by one thread per CTA on zero operands in shared memory; cycles and
+ * elapsed_ms as for i8c_probe_mma_f16.  Synchronises `stream`. */
+i8c_status i8c_probe_mma_f8(int32_t n, int32_t num_ctas, int32_t iters, long long* cycles, float* elapsed_ms,
+                            cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
