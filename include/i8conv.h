@@ -91,11 +91,12 @@ typedef struct {
                                 taps (64 output channels only, stride 1, 2 <= S <= 16,
                                 dil_w <= 8: two filter taps of a row per N = 128 MMA on CTA
                                 pairs; row tiles of 128 - dil_w output columns)               */
-  int32_t halo_loads;        /* halo kernel, how activations reach shared memory: 0 = auto
-                                (currently the same as 2), 1 = int8 staging ring filled by
+  int32_t halo_loads;        /* halo and transposed-tile kernels, how activations reach
+                                shared memory: 0 = auto, 1 = int8 staging ring filled by
                                 cp.async ahead of use, 2 = straight into registers (no
-                                staging memory); I8C_ERR_UNSUPPORTED if the forced form
-                                does not fit                                               */
+                                staging memory), 3 = one TMA box per tile and channel block
+                                into int8 slots, converted to fp16 in shared memory;
+                                I8C_ERR_UNSUPPORTED if the forced form does not fit        */
   int32_t tail_split;        /* halo kernel, the tiles of a partial last wave: 0 = auto (split
                                 along the channel blocks when the estimated saving clearly
                                 exceeds the partial-sum traffic), 1 = never split, 2 = split
@@ -214,6 +215,8 @@ typedef struct {
   int32_t off_out;             /* transposed tiles: the epilogue's output staging rows */
   int32_t off_bar, bar_bytes;  /* mbarriers and the CTA's control words                */
   int32_t phase_off[9];        /* halo: first position of column phase f, f <= stride_w */
+  /* TMA-fed halos (halo_loads = 3): int8 slots of one TMA box each */
+  int32_t tma_halo, x8_slots, off_x8, x8_bytes, box_w, box_h;
   /* per-tap gather kernel (variant 1; 0 otherwise) */
   int32_t gather_stages, gather_off_a, gather_stage_a, gather_off_b, gather_stage_b;
   int32_t gather_off_staging, gather_staging_slots, gather_staging_bytes, gather_off_bar;

@@ -73,7 +73,7 @@ class Layout(ctypes.Structure):
         "flat_tiles", "tile_px", "halo_rows", "halo_cw", "positions", "plane_bytes", "halo_bytes", "halo_stages",
         "off_staging", "staging_slots", "staging_bytes", "off_filter", "filter_stages", "filter_run",
         "filter_stage_bytes", "off_out", "off_bar", "bar_bytes")] + [("phase_off", ctypes.c_int32 * 9)] + [
-        (n, ctypes.c_int32) for n in (
+        (n, ctypes.c_int32) for n in ("tma_halo", "x8_slots", "off_x8", "x8_bytes", "box_w", "box_h",
             "gather_stages", "gather_off_a", "gather_stage_a", "gather_off_b", "gather_stage_b",
             "gather_off_staging", "gather_staging_slots", "gather_staging_bytes", "gather_off_bar")]
 
@@ -149,6 +149,10 @@ def _load() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.i8c_probe_mma_f16.argtypes = [I32, I32, I32, I32, I32, P, ctypes.POINTER(F), P]
     lib.i8c_probe_mma_f16.restype = ctypes.c_int
+    lib.i8c_probe_imma_s8.argtypes = [I32, I32, I32, P, P, ctypes.POINTER(F), P]
+    lib.i8c_probe_imma_s8.restype = ctypes.c_int
+    lib.i8c_probe_mma_f8.argtypes = [I32, I32, I32, P, ctypes.POINTER(F), P]
+    lib.i8c_probe_mma_f8.restype = ctypes.c_int
     lib.i8c_status_string.argtypes = [ctypes.c_int]
     lib.i8c_status_string.restype = ctypes.c_char_p
     lib.i8c_launch_count.argtypes = []
@@ -321,6 +325,27 @@ def i8c_probe_mma_f16(n: int, a_swizzled: int, num_ctas: int, iters: int, loop_m
     ms = ctypes.c_float()
     _check(lib.i8c_probe_mma_f16(n, int(a_swizzled), loop_mode, num_ctas, iters, buf.data_ptr(), ctypes.byref(ms),
                                  _stream(stream)), "i8c_probe_mma_f16")
+    return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
+
+
+def i8c_probe_imma_s8(num_ctas: int, warps_per_cta: int, iters: int, stream=None):
+    """Warp-level s8 IMMA probe: (per-CTA cycles [num_ctas, 3], elapsed ms)."""
+    import torch
+    buf = torch.zeros(3 * num_ctas, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ms = ctypes.c_float()
+    _check(lib.i8c_probe_imma_s8(num_ctas, warps_per_cta, iters, buf.data_ptr(), sink.data_ptr(), ctypes.byref(ms),
+                                 _stream(stream)), "i8c_probe_imma_s8")
+    return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
+
+
+def i8c_probe_mma_f8(n: int, num_ctas: int, iters: int, stream=None):
+    """tcgen05 kind::f8f6f4 (e4m3) probe: (per-CTA cycles [num_ctas, 3], elapsed ms)."""
+    import torch
+    buf = torch.zeros(3 * num_ctas, dtype=torch.int64, device="cuda")
+    ms = ctypes.c_float()
+    _check(lib.i8c_probe_mma_f8(n, num_ctas, iters, buf.data_ptr(), ctypes.byref(ms), _stream(stream)),
+           "i8c_probe_mma_f8")
     return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
 
 

@@ -75,6 +75,16 @@ struct HaloParams {
   // segment of seg_len input columns per filter row; slots = MMAs (tap pairs
   // and an odd last tap) per filter row and 16-channel half.
   int seg_len, vq, tq, slots;
+  // Halo loads by TMA (tma_halo = 1): for every channel block, one box of
+  // the input -- the tile's halo region in natural order (2-D patches:
+  // box_h rows x box_w columns), or the whole zero-padded input rows the
+  // flat run spans (flat tiles: box_w = W + 2*pad_w) -- lands in one of nxs
+  // int8 slots of x8_bytes at off_x8 (x8_box bytes each), and the producer
+  // threads convert it to the fp16 halo.  The kernels take the activations'
+  // tensor map (a 4-D tensor {32 channels, W, H, N*C/32} of bytes, encoded
+  // for every run) as a parameter of its own.
+  int tma_halo, nxs, box_w, box_h;
+  uint32_t off_x8, x8_bytes, x8_box;
 };
 
 
@@ -145,6 +155,15 @@ __device__ __forceinline__ void arrive_on_leader(uint64_t* bar, const TileSched&
   }
 }
 
+// Producer thread t of a group of whole warps stores the 16-byte half
+// halo_lane_half(t) of halo position halo_lane_pos(t), then of the positions
+// (group threads / 2) apart from it: each quarter-warp (the eight lanes whose
+// 16-byte stores share one shared-memory wavefront) writes eight consecutive
+// positions of one 8-channel plane, 128 contiguous bytes without a bank
+// conflict, and each warp still reads 16 whole 32-byte input vectors.
+__device__ __forceinline__ int halo_lane_half(int t) { return (t >> 3) & 1; }
+__device__ __forceinline__ int halo_lane_pos(int t) { return ((t >> 5) << 4) + (((t >> 4) & 1) << 3) + (t & 7); }
+
 // First halo position of thread pt and the walk between its positions.
 struct HaloWalk {
   int e_first, b_first, pos_first, b_step, pos_step;
@@ -153,7 +172,7 @@ constexpr int kHaloStep = kProducers / 2;
 
 __device__ __forceinline__ HaloWalk halo_walk(const HaloParams& hp, int pt) {
   HaloWalk w;
-  w.e_first = pt >> 1;
+  w.e_first = halo_lane_pos(pt);
   w.b_first = w.e_first / hp.CW;
   w.pos_first = w.e_first - w.b_first * hp.CW;
   w.b_step = kHaloStep / hp.CW;
@@ -236,7 +255,7 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
                                                    uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                    int pt) {
   const ConvParams& p = hp.c;
-  const int h = pt & 1;
+  const int h = halo_lane_half(pt);
   const int positions = hp.positions;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
@@ -302,7 +321,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
                                                    int pt) {
   const ConvParams& p = hp.c;
   constexpr int kBatch = 6;  // stride-2 halos: one load round trip per stage instead of two
-  const int h = pt & 1;
+  const int h = halo_lane_half(pt);
   const int positions = hp.positions;
   const HaloWalk w = halo_walk(hp, pt);
   const int HW32 = p.H * p.W * 32;
@@ -382,7 +401,7 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
 // timed out.
 template <int kB>
 __device__ __forceinline__ int halo_groups(const HaloParams& hp) {
-  if (hp.nstg != 0) return 0;
+  if (hp.nstg != 0 || hp.tma_halo) return 0;
   if (hp.nhs >= 3 && hp.positions <= (kProducers / 6) * kB) return 3;
   if (hp.positions <= (kProducers / 4) * kB) return 2;
   return 0;
@@ -403,8 +422,8 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
   const uint32_t grp = static_cast<uint32_t>(pt / gsize);
   const int lt = pt - static_cast<int>(grp) * gsize;
   const int step = gsize / 2;  // positions between a thread's loads, two threads per position
-  const int h = lt & 1;
-  const int e_first = lt >> 1;
+  const int h = halo_lane_half(lt);
+  const int e_first = halo_lane_pos(lt);
   const int b_first = e_first / hp.CW, pos_first = e_first - b_first * hp.CW;
   const int b_step = step / hp.CW, pos_step = step - b_step * hp.CW;
   const int positions = hp.positions;
@@ -459,6 +478,7 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
 // when a channel block is one batch of kB loads per thread, else all
 // producers on every channel block.
 constexpr int kHaloSplitBatch = 4;  // the halo kernel's producers: the most that fits 72 registers
+
 template <int kB>
 __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                       uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
@@ -466,6 +486,100 @@ __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, con
   const int ng = halo_groups<kB>(hp);
   if (ng > 0) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt, ng);
   return halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+}
+
+// Producer fed by TMA: thread 0 issues, nxs channel blocks ahead, one box
+// per channel block into an int8 slot (x_full[slot] counts its bytes); every
+// producer thread converts its positions of the slot into the fp16 halo
+// stage, arrives on h_full as the register producers do and on
+// x_done[slot]; once all have (warp 1 waits for that), thread 0 reuses the
+// slot for the next box.  No registers hold loads in flight and the box's
+// zero fill takes the place of the bounds checks.  Returns false when a wait
+// timed out; boxes still in flight then land before the function returns.
+__device__ __forceinline__ bool halo_produce_tma(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
+                                                 uint64_t* h_full, uint64_t* h_empty, uint64_t* x_full,
+                                                 uint64_t* x_done, const CUtensorMap* tmap_x,
+                                                 volatile int* abort_flag, int pt) {
+  const ConvParams& p = hp.c;
+  const int h = halo_lane_half(pt);
+  const int positions = hp.positions;
+  const HaloWalk w = halo_walk(hp, pt);
+  const uint32_t nxs = static_cast<uint32_t>(hp.nxs);
+  // Warp 1 (producer threads 0-31) tracks the next channel block to load --
+  // every one of its lanes, so that its warp-wide waits below stay uniform --
+  // and its lane 0 issues the boxes.
+  StageIter lit(hp, ts);
+  uint32_t issued = 0;
+  auto issue = [&](uint32_t slot) {  // all lanes of warp 1: the box of channel block `lit` into `slot`
+    if (pt == 0) {
+      const PatchTile t = decode_patch(lit.tile, hp, ts);
+      int c1, c2;
+      if (hp.flat) {
+        c1 = -p.pad_w;
+        c2 = t.m0 / hp.CW - p.pad_h;
+      } else {
+        c1 = t.q0 * p.stride_w - p.pad_w;
+        c2 = t.p0 * p.stride_h - p.pad_h;
+      }
+      if (!t.valid) c2 = p.H + 256;  // a pair's missing patch: a box wholly outside the image, all zeros
+      ptx::mbar_arrive_expect_tx(&x_full[slot], hp.x8_box);
+      ptx::tma_load_4d(smem + hp.off_x8 + slot * hp.x8_bytes, tmap_x, &x_full[slot], 0, c1, c2,
+                       t.n * p.CB + lit.cb);
+    }
+    lit.next(hp, ts);
+    ++issued;
+  };
+  if (pt < 32)
+    for (uint32_t j = 0; j < nxs && lit.valid(hp); ++j) issue(j);
+  bool skip = (p.debug_flags & 1) && pt == 0;  // test hook: this thread skips its first arrival
+  uint32_t hs = 0, hph = 0, i = 0;
+  bool ok = true;
+  for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts), ++i) {
+    const uint32_t slot = i % nxs, xph = (i / nxs) & 1u;
+    // warp-uniform outcomes: the arrives below are warp-wide
+    if (!__all_sync(0xffffffffu, ptx::mbar_wait(&x_full[slot], xph, p.timeout_ns, abort_flag)) ||
+        !__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) {
+      ok = false;
+      break;
+    }
+    const PatchTile t = decode_patch(it.tile, hp, ts);
+    const uint8_t* x8 = smem + hp.off_x8 + slot * hp.x8_bytes;
+    uint8_t* halo = smem + hs * hp.halo_bytes;
+    // halo position e in the box: flat tiles f0 + e (the run starts f0
+    // positions into the box's first padded row); 2-D patches row b, natural
+    // column halo_column(pos) of the phase-ordered position pos
+    const int f0 = hp.flat ? t.m0 - (t.m0 / hp.CW) * hp.CW : 0;
+    int b = w.b_first, pos = w.pos_first;
+    for (int e = w.e_first; e < positions; e += kHaloStep) {
+      const int src = hp.flat ? f0 + e : b * hp.CW + halo_column(hp, pos);
+      halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(x8 + src * 32 + h * 16));
+      b += w.b_step;
+      pos += w.pos_step;
+      if (pos >= hp.CW) {
+        pos -= hp.CW;
+        ++b;
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    arrive_on_leader(&h_full[hs], ts, !skip);
+    skip = false;
+    ptx::mbar_arrive(&x_done[slot]);
+    hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
+    hph ^= hs == 0 ? 1u : 0u;
+    if (pt < 32 && lit.valid(hp)) {  // warp 1: the slot is free once every producer has read it
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&x_done[slot], xph, p.timeout_ns, abort_flag))) {
+        ok = false;
+        break;
+      }
+      issue(slot);
+      __syncwarp();
+    }
+  }
+  // boxes issued but not consumed (after a timeout) land before the CTA moves on
+  if (pt == 0)
+    for (uint32_t k = i; k < issued; ++k)
+      if (!ptx::mbar_wait(&x_full[k % nxs], (k / nxs) & 1u, p.timeout_ns, nullptr)) break;
+  return ok;
 }
 
 // GT > 0 fixes the run length (K-slices per filter stage) at compile time so
@@ -476,7 +590,8 @@ __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, con
 // CTAs produce their own halo and drain their own 128 accumulator rows.
 template <int BN, int GT, int CG>
 __global__ void __launch_bounds__(kHaloThreads, 1)
-    conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+    conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const __grid_constant__ CUtensorMap tmap_x,
+                           const HaloParams hp) {
   static_assert(CG == 1 || CG == 2, "CTA group");
   static_assert(CG == 1 || BN >= 64, "a CTA pair splits B into halves of at least 32 rows");
   const ConvParams& p = hp.c;
@@ -496,6 +611,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 13);  // this CTA combines a split tile
   uint64_t* fconv_done = h_full + 14;  // this CTA's share of the filter is converted and announced
   volatile uint32_t* fconv_gen = reinterpret_cast<volatile uint32_t*>(h_full + 15);  // grid barrier generation seen
+  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded
+  uint64_t* x_done = h_full + 18;  // TMA-fed halo: int8 slot converted
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -525,6 +642,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(epi_sync, kEpilogue);
     ptx::mbar_init(fconv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&x_full[i], 1);
+      ptx::mbar_init(&x_done[i], kProducers);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -894,8 +1015,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ halo producers
-    // Thread pt owns the 16-byte half (pt & 1) of halo positions
-    // e = pt/2 + k*(kProducers/2), k = 0, 1, ...  Two ways to bring a channel
+    // Thread pt owns the 16-byte half halo_lane_half(pt) of halo positions
+    // e = halo_lane_pos(pt) + k*(kProducers/2), k = 0, 1, ...  Two ways to bring a channel
     // block in, chosen by the plan: through an int8 staging ring that
     // cp.async fills nstg-1 channel blocks ahead (deep prefetch, costs
     // shared memory), or straight into registers in batches whose first one
@@ -905,9 +1026,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<kWorkerRegs>();
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
-    const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_registers<kHaloSplitBatch>(hp, ts, smem, h_full, h_empty,
-                                                                           abort_flag, pt);
+    const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,
+                                                   abort_flag, pt)
+                    : hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
+                                  : halo_produce_registers<kHaloSplitBatch>(hp, ts, smem, h_full, h_empty,
+                                                                             abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue

@@ -65,14 +65,14 @@ __device__ __forceinline__ RowTile decode_row_tile(int t, const HaloParams& hp) 
 
 // Halo producer: segment r of a tile is input row p + r*dh - pad_h, columns
 // q0 - pad_w .. q0 - pad_w + L - 1 (zeros outside the image); thread pt owns
-// the 16-byte half (pt & 1) of positions pt/2 + k*96.  Loads go straight
+// the 16-byte half halo_lane_half(pt) of positions halo_lane_pos(pt) + k*96.  Loads go straight
 // into registers, kB at a time; the first batch is in flight while the thread
 // waits for the halo stage to be free.  Returns false when a wait timed out.
 template <int kB>
 __device__ __forceinline__ bool stack_produce(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                               uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag, int pt) {
   const ConvParams& p = hp.c;
-  const int h = pt & 1;
+  const int h = halo_lane_half(pt);
   const int positions = hp.positions;
   const int L = hp.seg_len;
   const int HW32 = p.H * p.W * 32;
@@ -84,7 +84,7 @@ __device__ __forceinline__ bool stack_produce(const HaloParams& hp, const TileSc
     for (int cb = 0; cb < p.CB; ++cb) {
       const int8_t* img = p.x + static_cast<int64_t>(t.n) * p.img_stride + cb * HW32;
       uint8_t* halo = smem + hs * hp.halo_bytes;
-      int e = pt >> 1, r = 0, o = pt >> 1;  // position, its segment and offset (96 < L)
+      int e = halo_lane_pos(pt), r = 0, o = e;  // position, its segment and offset (96 < L)
       bool stage_free = false;
       do {
         uint4 v[kB];
@@ -134,7 +134,8 @@ __device__ __forceinline__ bool stack_produce(const HaloParams& hp, const TileSc
 // uniform registers before one elected lane issues them back to back.
 template <int SLOTS>
 __global__ void __launch_bounds__(kHaloThreads, 1)
-    conv_fprop_stack_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+    conv_fprop_stack_kernel(const __grid_constant__ CUtensorMap tmap_f, const __grid_constant__ CUtensorMap tmap_x,
+                            const HaloParams hp) {
   static_assert(SLOTS >= 1 && SLOTS <= kStackMaxSlots, "tap pairs per filter row");
   constexpr int CG = 2;
   const ConvParams& p = hp.c;

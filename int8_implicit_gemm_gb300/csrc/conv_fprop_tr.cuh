@@ -59,7 +59,8 @@ struct TrRegs {
 // serves.  CG: CTAs per MMA tile (1, or 2 for pairs).
 template <int GT, int MAXPX, int CG>
 __global__ void __launch_bounds__(kHaloThreads, 1)
-    conv_fprop_tr_kernel(const __grid_constant__ CUtensorMap tmap_f, const HaloParams hp) {
+    conv_fprop_tr_kernel(const __grid_constant__ CUtensorMap tmap_f, const __grid_constant__ CUtensorMap tmap_x,
+                         const HaloParams hp) {
   static_assert(CG == 1 || CG == 2, "CTA group");
   using Regs = TrRegs<MAXPX>;
   constexpr int kMaxGroupsPerWarp = MAXPX / 16;  // 8-column groups of one epilogue warp
@@ -76,6 +77,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   uint64_t* drain = h_full + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 11) + 1;
+  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded
+  uint64_t* x_done = h_full + 18;  // TMA-fed halo: int8 slot converted
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -103,6 +106,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
     ptx::mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&x_full[i], 1);
+      ptx::mbar_init(&x_done[i], kProducers);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -383,9 +390,11 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<Regs::kWorker>();
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
-    const bool ok = hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                : halo_produce_registers<Regs::kBatch>(hp, ts, smem, h_full, h_empty, abort_flag,
-                                                                       pt);
+    const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,
+                                                   abort_flag, pt)
+                    : hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
+                                  : halo_produce_registers<Regs::kBatch>(hp, ts, smem, h_full, h_empty,
+                                                                         abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue

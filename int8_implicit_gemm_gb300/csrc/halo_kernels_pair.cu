@@ -12,12 +12,12 @@ cudaError_t halo_prepare_pair(int block_n) {
   }
 }
 
-cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
+cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem, int num_ctas,
                              cudaStream_t stream) {
   switch (block_n) {
-    case 64: return halo_launch_bn<64, 2>(tmap, p, smem, num_ctas, stream);
-    case 128: return halo_launch_bn<128, 2>(tmap, p, smem, num_ctas, stream);
-    case 256: return halo_launch_bn<256, 2>(tmap, p, smem, num_ctas, stream);
+    case 64: return halo_launch_bn<64, 2>(tmap, tmap_x, p, smem, num_ctas, stream);
+    case 128: return halo_launch_bn<128, 2>(tmap, tmap_x, p, smem, num_ctas, stream);
+    case 256: return halo_launch_bn<256, 2>(tmap, tmap_x, p, smem, num_ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }

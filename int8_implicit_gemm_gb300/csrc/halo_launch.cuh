@@ -7,7 +7,7 @@
 
 namespace i8c {
 
-using HaloKernel = void (*)(const CUtensorMap, const HaloParams);
+using HaloKernel = void (*)(const CUtensorMap, const CUtensorMap, const HaloParams);
 
 // Run lengths with an unrolled tap loop and precomputed tap offsets, for runs
 // of whole filter rows (S divides the run length): 3 (a row of a 3x3
@@ -66,11 +66,11 @@ cudaLaunchConfig_t halo_launch_config(int smem, int num_ctas, cudaStream_t strea
 }
 
 template <int BN, int CG>
-cudaError_t halo_launch_bn(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
-                           cudaStream_t stream) {
+cudaError_t halo_launch_bn(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem,
+                           int num_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr, p.f_int8 != nullptr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, tmap_x, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -34,6 +34,10 @@ struct i8c_plan {
   int* status;     // device status word
   long long* trace;  // clock64 trace of CTA 0 (debug flag I8C_DEBUG_TRACE), kTraceRows * kTraceSlots entries
   CUtensorMap tmap;
+  // TMA-fed halos: the activations' tensor map, encoded for the x pointer of
+  // the last run (a run with another x encodes it again)
+  mutable CUtensorMap tmap_x;
+  mutable const int8_t* tmap_x_ptr;
   int8_t *stage_x, *stage_f, *stage_y;  // device staging for host-buffer runs (optional)
   // host_staging = 2: a second staging set and the pipelined host-buffer
   // runs' copy streams and ordering events (set b: in_done, run_done, out_done)
@@ -124,6 +128,25 @@ double wave_efficiency(int64_t tiles, int ctas) {
   return static_cast<double>(tiles) / static_cast<double>(waves * ctas);
 }
 
+// The TMA box that carries one channel block of a tile's halo into shared
+// memory (int8, 32 bytes per position): for 2-D patches the halo region
+// itself (CW columns x HR rows, natural column order); for flat tiles the
+// whole zero-padded input rows (W + 2*pad_w wide) that the run of
+// `positions` padded positions can span, from any starting column.  TMA
+// boxes are at most 256 elements per dimension.  Returns false when the box
+// does not fit that limit.
+bool tma_halo_box(const i8c_conv_shape& s, const i8c::HaloParams& h, i8c::HaloParams* out) {
+  const int64_t bw = h.CW;
+  const int64_t bh = h.flat ? (h.CW - 1 + static_cast<int64_t>(h.positions) + h.CW - 1) / h.CW : h.HR;
+  if (bw > 256 || bh > 256 || bw < 1 || bh < 1) return false;
+  if (h.flat && h.CW != s.W + 2 * s.pad_w) return false;
+  out->box_w = static_cast<int>(bw);
+  out->box_h = static_cast<int>(bh);
+  out->x8_box = static_cast<uint32_t>(32 * bw * bh);
+  out->x8_bytes = (out->x8_box + 1023) / 1024 * 1024;
+  return true;
+}
+
 // Halo geometry and shared-memory layout of the halo kernel for tile width bn
 // on cg CTAs (each CTA of a pair stages bn/2 filter rows): two fp16 halo
 // stages, the int8 staging ring (if any), the filter stages, the barriers.
@@ -183,6 +206,12 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
   static const int kSlots[3] = {3, 2, 0};
   const int first = loads == 1 ? 0 : 2, last = loads == 1 ? 1 : 2;
   const int RS = s.R * s.S;
+  // TMA-fed halos (loads == 3): one or two int8 slots of one box each; two
+  // unless the second would cost the filter its residency (one output-channel
+  // tile whose every stage fits)
+  const bool tma = loads == 3;
+  if (tma && !tma_halo_box(s, *h, h)) return false;
+  const int n_tiles = (s.K + bn - 1) / bn;
   for (int G = RS; G >= 1; --G) {
     const bool part_row = s.S % G == 0;
     const bool whole_rows = G % s.S == 0 && RS % G == 0;
@@ -195,19 +224,42 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
     // the shared-memory conversion of each block waits for the MMAs.
     for (int nhs = G == RS ? 3 : 2; nhs >= (loads == 1 ? 1 : 2); --nhs)
     for (int k = first; k <= last; ++k) {
-      const int nstg = kSlots[k];
-      const int64_t off_stg = static_cast<int64_t>(nhs) * h->halo_bytes;
-      const int64_t off_b = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
-      const int64_t room = budget - off_b;
+      const int nstg = tma ? 0 : kSlots[k];
       const int64_t stage = static_cast<int64_t>(G) * (bn / cg) * 64;
-      if (room < min_stages * stage) continue;
-      int64_t nbs = room / stage;
-      if (nbs > i8c::kMaxBStages) nbs = i8c::kMaxBStages;
+      const int64_t need_resident = (s.C / 32) * RS / G;
+      int64_t off_x8 = 0, off_b = 0, nbs = 0;
+      int nxs = 0;
+      for (int nx = tma ? 2 : 0; nx >= 0; --nx) {  // TMA: two slots, else one; no TMA: none
+        const int64_t off_stg = static_cast<int64_t>(nhs) * h->halo_bytes;
+        const int64_t ox = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
+        const int64_t ob = (ox + static_cast<int64_t>(nx) * h->x8_bytes + 1023) / 1024 * 1024;
+        int64_t n = (budget - ob) / stage;
+        if (n > i8c::kMaxBStages) n = i8c::kMaxBStages;
+        if (n < min_stages) {
+          if (tma && nx > 1) continue;
+          break;
+        }
+        if (tma && nx == 2 && n_tiles == 1 && n < need_resident) {
+          // would one slot keep the filter resident?
+          const int64_t ob1 = (ox + h->x8_bytes + 1023) / 1024 * 1024;
+          const int64_t n1 = (budget - ob1) / stage;
+          if (n1 >= need_resident && need_resident <= i8c::kMaxBStages) continue;
+        }
+        off_x8 = ox;
+        off_b = ob;
+        nbs = n;
+        nxs = nx;
+        break;
+      }
+      if (nbs < min_stages || (tma && nxs < 1)) continue;
       h->bgroup = G;
       h->nhs = nhs;
       h->nstg = nstg;
       h->nbs = static_cast<int>(nbs);
-      h->off_stg = static_cast<uint32_t>(off_stg);
+      h->tma_halo = tma ? 1 : 0;
+      h->nxs = nxs;
+      h->off_x8 = static_cast<uint32_t>(off_x8);
+      h->off_stg = static_cast<uint32_t>(static_cast<int64_t>(nhs) * h->halo_bytes);
       h->off_b = static_cast<uint32_t>(off_b);
       h->off_bar = static_cast<uint32_t>(off_b + nbs * stage);
       *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
@@ -227,7 +279,7 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
 // of nstg slots that cp.async fills nstg - 1 channel blocks ahead.  Returns
 // false when nothing fits.
 bool tr_layout(const i8c_conv_shape& s, int P, int np, int cg, int want_g, int nstg, i8c::HaloParams* h,
-               int* smem_bytes) {
+               int* smem_bytes, bool tma = false) {
   if (s.stride_h != 1 || s.stride_w != 1) return false;
   const int mma_n = cg * np;
   if (mma_n < 16 || mma_n > 256 || mma_n % 16 != 0 || np % 8 != 0) return false;
@@ -253,27 +305,45 @@ bool tr_layout(const i8c_conv_shape& s, int P, int np, int cg, int want_g, int n
   const int RS = s.R * s.S;
   const int64_t stage_unit = 128 * 64;  // one K-slice of 128 output channels, fp16
   const int64_t out_bytes = static_cast<int64_t>(mma_n) * 128;
+  if (tma) {
+    if (!tma_halo_box(s, *h, h)) return false;
+    nstg = 0;
+  }
   for (int G = RS < 32 ? RS : 32; G >= 1; --G) {
     if (RS % G != 0 || (want_g != 0 && G != want_g)) continue;
     const int64_t stage = G * stage_unit;
-    int64_t nbs_for[4] = {0, 0, 0, 0};
+    // halo stages (2 or 3) and TMA slots (2 or 1; none without TMA): the
+    // first combination in this order that leaves two filter stages; a third
+    // halo stage only when it costs no filter stage
+    int nhs = 0, nxs = 0;
+    int64_t nbs = 0, off_x8 = 0, off_b = 0;
     const int64_t stg = static_cast<int64_t>(nstg) * h->stg_bytes;
-    for (int nhs = 2; nhs <= 3; ++nhs) {
-      const int64_t off_b = (static_cast<int64_t>(nhs) * h->halo_bytes + stg + 1023) / 1024 * 1024;
-      const int64_t n = (budget - off_b - out_bytes) / stage;
-      nbs_for[nhs] = n > i8c::kMaxBStages ? i8c::kMaxBStages : n;
+    auto fit = [&](int nh, int nx, int64_t* ox, int64_t* ob) {
+      *ox = (static_cast<int64_t>(nh) * h->halo_bytes + stg + 1023) / 1024 * 1024;
+      *ob = (*ox + static_cast<int64_t>(nx) * h->x8_bytes + 1023) / 1024 * 1024;
+      const int64_t n = (budget - *ob - out_bytes) / stage;
+      return n > i8c::kMaxBStages ? static_cast<int64_t>(i8c::kMaxBStages) : n;
+    };
+    for (int nx = tma ? 2 : 0; nx >= (tma ? 1 : 0) && nbs < 2; --nx) {
+      int64_t ox3, ob3, ox2, ob2;
+      const int64_t n3 = fit(3, nx, &ox3, &ob3), n2 = fit(2, nx, &ox2, &ob2);
+      if (n3 >= 2 && n3 >= n2) {
+        nhs = 3, nxs = nx, nbs = n3, off_x8 = ox3, off_b = ob3;
+      } else if (n2 >= 2) {
+        nhs = 2, nxs = nx, nbs = n2, off_x8 = ox2, off_b = ob2;
+      }
     }
-    // a third halo stage gives the producers slack unless it costs a filter stage
-    const int nhs = nbs_for[3] >= 2 && nbs_for[3] >= nbs_for[2] ? 3 : 2;
-    if (nbs_for[nhs] < 2) continue;
-    const int64_t off_b = (static_cast<int64_t>(nhs) * h->halo_bytes + stg + 1023) / 1024 * 1024;
+    if (nbs < 2) continue;
     h->bgroup = G;
     h->nhs = nhs;
     h->nstg = nstg;
-    h->nbs = static_cast<int>(nbs_for[nhs]);
+    h->nbs = static_cast<int>(nbs);
+    h->tma_halo = tma ? 1 : 0;
+    h->nxs = nxs;
+    h->off_x8 = static_cast<uint32_t>(off_x8);
     h->off_stg = static_cast<uint32_t>(nhs * h->halo_bytes);
     h->off_b = static_cast<uint32_t>(off_b);
-    h->off_out = static_cast<uint32_t>(off_b + nbs_for[nhs] * stage);
+    h->off_out = static_cast<uint32_t>(off_b + nbs * stage);
     h->off_bar = static_cast<uint32_t>(h->off_out + out_bytes);
     *smem_bytes = static_cast<int>(h->off_bar) + i8c::kHaloBarBytes + 1024;
     return true;
@@ -422,19 +492,36 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
   if (pl->kernel_variant >= 2) {
     i8c::HaloParams hp = pl->halo;
     hp.c = p;
+    if (hp.tma_halo && pl->tmap_x_ptr != x) {
+      // the activations as {32 channel bytes, W, H, N*C/32}; one box is one
+      // channel block of a tile's halo (zeros outside the image)
+      EncodeTiled encode = get_encode_tiled();
+      if (encode == nullptr) return I8C_ERR_CUDA;
+      cuuint64_t dims[4] = {32, static_cast<cuuint64_t>(s.W), static_cast<cuuint64_t>(s.H),
+                            static_cast<cuuint64_t>(s.N) * (s.C / 32)};
+      cuuint64_t strides[3] = {32, static_cast<cuuint64_t>(s.W) * 32, static_cast<cuuint64_t>(s.W) * s.H * 32};
+      cuuint32_t box[4] = {32, static_cast<cuuint32_t>(hp.box_w), static_cast<cuuint32_t>(hp.box_h), 1};
+      cuuint32_t estr[4] = {1, 1, 1, 1};
+      if (encode(&pl->tmap_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<int8_t*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return I8C_ERR_CUDA;
+      pl->tmap_x_ptr = x;
+    }
     if (pl->gbar != nullptr) {
       hp.f_int8 = f;
       hp.f16 = pl->f16;
       hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
       hp.gbar = pl->gbar;
     }
-    e = pl->kernel_variant == 6   ? i8c::stack_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
-        : pl->kernel_variant == 5 ? i8c::tr_launch_pair(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
-        : pl->kernel_variant == 4 ? i8c::tr_launch(pl->tmap, hp, pl->smem_bytes, pl->num_ctas, stream)
-        : pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
-                                                          stream)
-                                  : i8c::halo_launch_single(pl->block_n, pl->tmap, hp, pl->smem_bytes, pl->num_ctas,
-                                                            stream);
+    const CUtensorMap& tx = pl->tmap_x;  // read only by TMA-fed halos
+    e = pl->kernel_variant == 6   ? i8c::stack_launch(pl->tmap, tx, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 5 ? i8c::tr_launch_pair(pl->tmap, tx, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 4 ? i8c::tr_launch(pl->tmap, tx, hp, pl->smem_bytes, pl->num_ctas, stream)
+        : pl->kernel_variant == 3 ? i8c::halo_launch_pair(pl->block_n, pl->tmap, tx, hp, pl->smem_bytes,
+                                                          pl->num_ctas, stream)
+                                  : i8c::halo_launch_single(pl->block_n, pl->tmap, tx, hp, pl->smem_bytes,
+                                                            pl->num_ctas, stream);
   } else {
     e = i8c::launch_conv(pl->block_n, pl->tmap, p, pl->num_ctas, stream);
   }
@@ -500,7 +587,7 @@ bool options_valid(const i8c_options& o) {
   if (o.block_n != 0 && o.block_n != 32 && o.block_n != 64 && o.block_n != 128 && o.block_n != 256) return false;
   return !(o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
            o.timing_events < 0 || o.timing_events > 65536 || o.host_staging < 0 || o.host_staging > 2 ||
-           o.kernel_variant < 0 || o.kernel_variant > 6 || o.halo_loads < 0 || o.halo_loads > 2 ||
+           o.kernel_variant < 0 || o.kernel_variant > 6 || o.halo_loads < 0 || o.halo_loads > 3 ||
            o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
            o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
            (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)));
@@ -591,7 +678,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
       if (o.tile_px != 0 && n != o.tile_px) continue;
       i8c::HaloParams h;
       int sm = 0;
-      if (!tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &h, &sm)) continue;
+      if (!tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &h, &sm, o.halo_loads == 3)) continue;
       // A pair's CTA builds the halo of n / 2 pixels plus the filter's overhang
       // for every channel block; when the overhang outweighs the pixels the
       // producers, not the tensor core, set the pace (8x256x56x56 layer: 88
@@ -623,7 +710,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     if (n == 0) {
       return I8C_ERR_UNSUPPORTED;
     }
-    tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &p->halo, &halo_smem);
+    tr_layout(s, p->P, n / cg, cg, o.filter_run, tr_stg, &p->halo, &halo_smem, o.halo_loads == 3);
     p->kernel_variant = o.kernel_variant;
     p->cta_group = cg;
     bn = 128 * cg;
@@ -737,7 +824,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
         if ((n1 != 0 || n2 != 0) && cost < 0.97 * halo_cost) {
           const int cgt = pair ? 2 : 1;
           const int n = pair ? n2 : n1;
-          tr_layout(s, p->P, n / cgt, cgt, o.filter_run, tr_stg, &p->halo, &halo_smem);
+          tr_layout(s, p->P, n / cgt, cgt, o.filter_run, tr_stg, &p->halo, &halo_smem, o.halo_loads == 3);
           p->kernel_variant = pair ? 5 : 4;
           p->cta_group = cgt;
           groups = pair ? pair_groups : tr_groups;
@@ -826,6 +913,9 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     if (p->num_n_tiles == 1 && ksplit == 1 && nsplit == 1 && unit_stages <= p->halo.nbs) {
       p->halo.nbs = unit_stages;
       p->halo.resident = 1;
+      // the stages beyond the filter's own are not needed: the barriers move down
+      p->halo.off_bar = p->halo.off_b + static_cast<uint32_t>(unit_stages * p->halo.bgroup * (bn / p->cta_group) * 64);
+      halo_smem = static_cast<int>(p->halo.off_bar) + i8c::kHaloBarBytes + 1024;
     }
     p->halo.full_units = ksplit > 1 || nsplit > 1 ? p->num_tiles - rem : p->num_tiles;
     p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0) + (nsplit > 1 ? rem * 2 : 0);
@@ -1073,6 +1163,12 @@ void fill_layout(const i8c_plan* pl, i8c_layout* L) {
     L->filter_stage_bytes = h.bgroup * rows * 64;
     L->off_out = static_cast<int32_t>(h.off_out);
     L->off_bar = static_cast<int32_t>(h.off_bar);
+    L->tma_halo = h.tma_halo;
+    L->x8_slots = h.nxs;
+    L->off_x8 = static_cast<int32_t>(h.off_x8);
+    L->x8_bytes = static_cast<int32_t>(h.x8_bytes);
+    L->box_w = h.box_w;
+    L->box_h = h.box_h;
     L->bar_bytes = i8c::kHaloBarBytes;
     for (int f = 0; f < 9; ++f) L->phase_off[f] = h.phase_off[f];
   } else {

@@ -24,10 +24,12 @@ cudaError_t launch_conv(int block_n, const CUtensorMap& tmap, const ConvParams& 
 // CTAs and on CTA pairs (clusters of two); prepare allows the full dynamic
 // shared memory, max_clusters is the number of pairs that fit at once.
 cudaError_t halo_prepare_single(int block_n);
-cudaError_t halo_launch_single(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes,
+cudaError_t halo_launch_single(int block_n, const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p,
+                               int smem_bytes,
                                int num_ctas, cudaStream_t stream);
 cudaError_t halo_prepare_pair(int block_n);
-cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const HaloParams& p, int smem_bytes,
+cudaError_t halo_launch_pair(int block_n, const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p,
+                             int smem_bytes,
                              int num_ctas, cudaStream_t stream);
 int halo_pair_max_clusters(int block_n, int bgroup, int S, int smem_bytes);
 int halo_single_max_ctas(int block_n, int bgroup, int S, int smem_bytes);  // resident at once
@@ -35,12 +37,14 @@ int halo_single_max_ctas(int block_n, int bgroup, int S, int smem_bytes);  // re
 // tr_kernels.cu: the transposed-tile kernel (128 output channels x tile_px
 // pixels per tile, stride-1 layers)
 cudaError_t tr_prepare();
-cudaError_t tr_launch(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+cudaError_t tr_launch(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem_bytes,
+                      int num_ctas,
                       cudaStream_t stream);
 // tr_kernels_pair.cu: the same on CTA pairs (clusters of two; tile_px is each
 // CTA's half of the MMA's N); max_clusters is the number of pairs that fit
 cudaError_t tr_prepare_pair();
-cudaError_t tr_launch_pair(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+cudaError_t tr_launch_pair(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem_bytes,
+                           int num_ctas,
                            cudaStream_t stream);
 int tr_pair_max_clusters(int bgroup, int S, int mma_n, int smem_bytes);
 constexpr int kMaxDynamicSmem = 232448;
@@ -49,7 +53,8 @@ constexpr int kMaxDynamicSmem = 232448;
 // filter taps per N = 128 MMA, CTA pairs) and its filter conversion into the
 // stacked fp16 order
 cudaError_t stack_prepare();
-cudaError_t stack_launch(const CUtensorMap& tmap, const HaloParams& p, int smem_bytes, int num_ctas,
+cudaError_t stack_launch(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem_bytes,
+                         int num_ctas,
                          cudaStream_t stream);
 int stack_max_clusters(int slots, int smem_bytes);
 cudaError_t launch_filter_to_f16_stacked(const int8_t* f, uint16_t* f16, int CB, int R, int S, cudaStream_t stream);

@@ -63,7 +63,7 @@ cudaError_t launch_filter_to_f16_stacked(const int8_t* f, uint16_t* f16, int CB,
   return cudaGetLastError();
 }
 
-using StackKernel = void (*)(const CUtensorMap, const HaloParams);
+using StackKernel = void (*)(const CUtensorMap, const CUtensorMap, const HaloParams);
 
 // One instantiation per tap-pair count ceil(S/2) = 1 .. 8.
 StackKernel stack_kernel_for(int slots) {
@@ -90,10 +90,11 @@ cudaError_t stack_prepare() {
 
 // Launched like the halo kernel on pairs: clusters of two, a programmatic
 // dependent of the filter conversion.
-cudaError_t stack_launch(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas, cudaStream_t stream) {
+cudaError_t stack_launch(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem,
+                         int num_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = halo_launch_config<2>(smem, num_ctas, stream, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, stack_kernel_for(p.slots), tmap, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, stack_kernel_for(p.slots), tmap, tmap_x, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -6,9 +6,9 @@ namespace i8c {
 
 cudaError_t tr_prepare_pair() { return tr_prepare_cg<2>(); }
 
-cudaError_t tr_launch_pair(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas,
+cudaError_t tr_launch_pair(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem, int num_ctas,
                            cudaStream_t stream) {
-  return tr_launch_cg<2>(tmap, p, smem, num_ctas, stream);
+  return tr_launch_cg<2>(tmap, tmap_x, p, smem, num_ctas, stream);
 }
 
 // Clusters of two that can be resident at once (0 if the query fails).

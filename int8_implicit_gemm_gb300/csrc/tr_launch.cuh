@@ -8,7 +8,7 @@
 
 namespace i8c {
 
-using TrKernel = void (*)(const CUtensorMap, const HaloParams);
+using TrKernel = void (*)(const CUtensorMap, const CUtensorMap, const HaloParams);
 
 // Stages of 9 whole-row taps (a 3x3 channel block, three rows of a 1x3
 // filter, a row of a 9-wide one) take the unrolled instantiation; MMAs of at
@@ -34,10 +34,11 @@ cudaError_t tr_prepare_cg() {
 // the filter conversion (their prologue overlaps its tail), pairs as
 // clusters of two.
 template <int CG>
-cudaError_t tr_launch_cg(const CUtensorMap& tmap, const HaloParams& p, int smem, int num_ctas, cudaStream_t stream) {
+cudaError_t tr_launch_cg(const CUtensorMap& tmap, const CUtensorMap& tmap_x, const HaloParams& p, int smem,
+                         int num_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, tr_kernel_for<CG>(p.bgroup, p.c.S, CG * p.tile_px), tmap, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tr_kernel_for<CG>(p.bgroup, p.c.S, CG * p.tile_px), tmap, tmap_x, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

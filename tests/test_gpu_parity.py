@@ -39,8 +39,11 @@ def _data(shape, seed, lo=-128, hi=127):
 @pytest.mark.parametrize("kernel", [dict(kernel_variant=1), dict(kernel_variant=2),
                                     dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
                                     dict(kernel_variant=3), dict(kernel_variant=3, block_n=64),
-                                    dict(kernel_variant=3, block_n=256, halo_loads=1)],
-                         ids=["gather", "halo", "halo-staged", "halo-direct", "pair", "pair-64", "pair-256-staged"])
+                                    dict(kernel_variant=3, block_n=256, halo_loads=1),
+                                    dict(kernel_variant=2, halo_loads=3), dict(kernel_variant=3, halo_loads=3),
+                                    dict(kernel_variant=3, block_n=64, halo_loads=3)],
+                         ids=["gather", "halo", "halo-staged", "halo-direct", "pair", "pair-64", "pair-256-staged",
+                              "halo-tma", "pair-tma", "pair-64-tma"])
 def test_small_shapes_exact(shape, alpha, kernel):
     x, f = _data(shape, 1000 + sum(shape))
     y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, alpha)
@@ -108,7 +111,9 @@ def test_extreme_magnitudes_exact_stacked(kw):
                                 dict(kernel_variant=3), dict(kernel_variant=3, block_n=256),
                                 dict(kernel_variant=4), dict(kernel_variant=4, tile_px=256),
                                 dict(kernel_variant=5), dict(kernel_variant=5, tile_px=128),
-                                dict(kernel_variant=4, filter_run=3, max_chunk_slices=30)],
+                                dict(kernel_variant=4, filter_run=3, max_chunk_slices=30),
+                                dict(kernel_variant=2, halo_loads=3), dict(kernel_variant=3, halo_loads=3),
+                                dict(kernel_variant=4, halo_loads=3), dict(kernel_variant=5, halo_loads=3)],
                          ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_extreme_magnitudes_exact(kw):
     """Products near 2^14 and odd chunk sums just below 2^24 on every kernel
@@ -176,8 +181,11 @@ def _full_oracle(wl):
 
 @pytest.mark.parametrize("kw", [{}, dict(kernel_variant=2, halo_loads=1), dict(kernel_variant=2, halo_loads=2),
                                 dict(kernel_variant=3), dict(kernel_variant=4), dict(kernel_variant=5),
-                                dict(kernel_variant=6)],
-                         ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair", "stacked"])
+                                dict(kernel_variant=6), dict(kernel_variant=2, halo_loads=3),
+                                dict(kernel_variant=3, halo_loads=3), dict(kernel_variant=4, halo_loads=3),
+                                dict(kernel_variant=5, halo_loads=3)],
+                         ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair", "stacked",
+                              "halo-tma", "pair-tma", "transposed-tma", "transposed-pair-tma"])
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
 def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
@@ -258,7 +266,8 @@ TRANSPOSED_EXTRA = [
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("kw", [dict(), dict(tile_px=16), dict(tile_px=176), dict(tile_px=256),
                                 dict(tile_px=64, filter_run=3), dict(tile_px=128, filter_run=1, max_chunk_slices=5),
-                                dict(num_ctas=3, tile_px=96), dict(halo_loads=1), dict(tile_px=240, halo_loads=1)],
+                                dict(num_ctas=3, tile_px=96), dict(halo_loads=1), dict(tile_px=240, halo_loads=1),
+                                dict(halo_loads=3), dict(tile_px=176, halo_loads=3), dict(tile_px=64, halo_loads=3)],
                          ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()) or "auto")
 @pytest.mark.parametrize("variant", [4, 5], ids=["single", "pair"])
 def test_transposed_tiles_exact(shape, kw, variant):

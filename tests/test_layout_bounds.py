@@ -26,7 +26,7 @@ from tests.test_gpu_parity import SMALL, STACKED_SHAPES, TRANSPOSED_EXTRA
 
 KMAX_SMEM = 232448          # opt-in dynamic shared memory per block on sm_103
 KMAX_FILTER_STAGES = 16     # filter stages the kernels have barriers for
-KHALO_BARRIER_WORDS = 48    # 8-byte barrier and control words the halo and transposed kernels use
+KHALO_BARRIER_WORDS = 52    # 8-byte barrier and control words the halo and transposed kernels use
 
 
 def _taps(shape):
@@ -120,9 +120,32 @@ def check_layout(shape, L):
         assert 2 * L["block_n"] <= tc, "two accumulator buffers of BN columns"
         assert L["tile_px"] in (0, 128)
     assert end <= L["off_bar"], "operands overlap the barriers"
+    if L["tma_halo"]:
+        check_tma_halo(shape, L, pos)
     assert KHALO_BARRIER_WORDS * 8 <= L["bar_bytes"]
     assert L["off_bar"] + L["bar_bytes"] + 1024 <= L["smem_bytes"], "barriers past the allocation"
     assert P >= 1 and Q >= 1
+
+
+def check_tma_halo(shape, L, pos):
+    """TMA-fed halos: every box (32 bytes x box_w x box_h, at most 256 per
+    dimension) fits its int8 slot, the slots sit between the halo stages and
+    the filter stages, and every position the converters read lies in the box."""
+    N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw = shape
+    bw, bh = L["box_w"], L["box_h"]
+    assert 1 <= bw <= 256 and 1 <= bh <= 256, "TMA box dimensions"
+    assert L["x8_bytes"] >= 32 * bw * bh and L["x8_bytes"] % 1024 == 0
+    assert L["x8_slots"] in (1, 2)
+    assert L["off_x8"] % 1024 == 0
+    assert L["off_x8"] >= L["halo_stages"] * L["halo_bytes"] + L["staging_slots"] * L["staging_bytes"]
+    assert L["off_x8"] + L["x8_slots"] * L["x8_bytes"] <= L["off_filter"], "int8 slots overlap the filter"
+    CW = L["halo_cw"]
+    if L["kernel_variant"] >= 4 or L["flat_tiles"]:
+        # a flat run starts anywhere in the box's first padded row
+        assert bw == W + 2 * pw == CW
+        assert (CW - 1) + pos - 1 < bw * bh, "the flat run reaches past the box"
+    else:
+        assert bw == CW and bh >= L["halo_rows"], "the box covers the halo region"
 
 
 XBUF_BYTES = 2 * 8 * 8 * 32 * 4   # the stacked kernel's epilogue shift buffers: 2 tiles x 8 warps x 8 lanes x 32 words
@@ -169,6 +192,10 @@ PLAN_FORMS = [
     dict(kernel_variant=4, halo_loads=1), dict(kernel_variant=5), dict(kernel_variant=5, tile_px=128),
     dict(kernel_variant=5, tile_px=240, halo_loads=1), dict(max_chunk_slices=5), dict(kernel_variant=2, max_chunk_slices=7),
     dict(kernel_variant=6), dict(kernel_variant=6, max_chunk_slices=4),
+    dict(halo_loads=3), dict(kernel_variant=2, halo_loads=3), dict(kernel_variant=3, halo_loads=3),
+    dict(kernel_variant=2, tile_shape=2, halo_loads=3), dict(kernel_variant=3, block_n=64, halo_loads=3),
+    dict(kernel_variant=4, halo_loads=3), dict(kernel_variant=4, tile_px=256, halo_loads=3),
+    dict(kernel_variant=5, halo_loads=3), dict(kernel_variant=5, tile_px=128, halo_loads=3),
 ]
 
 SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + STACKED_SHAPES + [
@@ -206,7 +233,7 @@ def test_every_plan_form_stays_in_bounds(ext, shape):
 
 
 @pytest.mark.parametrize("plant", ["positions", "plane_bytes", "off_bar", "off_staging", "tmem_cols", "off_out",
-                                   "stacked_positions", "stacked_xbuf"])
+                                   "stacked_positions", "stacked_xbuf", "tma_box", "tma_slots"])
 def test_planted_off_by_one_is_caught(ext, plant):
     """Each planted mistake shrinks one region by the smallest step the
     layout allows; the check must notice."""
@@ -219,6 +246,8 @@ def test_planted_off_by_one_is_caught(ext, plant):
         "off_out": ((8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=4), None),
         "stacked_positions": ((8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=6), None),
         "stacked_xbuf": ((8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=6), None),
+        "tma_box": ((8, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=4, halo_loads=3), None),
+        "tma_slots": ((32, 128, 112, 112, 256, 3, 3, 1, 1, 2, 2, 1, 1), dict(kernel_variant=2, halo_loads=3), None),
     }
     shape, opts, _ = cases[plant]
     L = _layout(ext, shape, opts)
@@ -241,5 +270,9 @@ def test_planted_off_by_one_is_caught(ext, plant):
         bad["positions"] -= 1
     elif plant == "stacked_xbuf":        # shift buffers one row into the filter stages
         bad["off_out"] = L["off_filter"] - XBUF_BYTES + 128
+    elif plant == "tma_box":             # a box one padded row short of the flat run
+        bad["box_h"] -= 1
+    elif plant == "tma_slots":           # int8 slots reaching one KB into the filter stages
+        bad["off_x8"] += 1024
     with pytest.raises(AssertionError):
         check_layout(shape, bad)
