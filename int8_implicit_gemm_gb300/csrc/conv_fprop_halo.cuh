@@ -348,8 +348,8 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
         v[k] = make_uint4(0, 0, 0, 0);
         if (e < positions) {
           const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
-          if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
-            v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
+          v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
+                                    t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
           e += kHaloStep;
           b += w.b_step;
           pos += w.pos_step;
@@ -445,8 +445,8 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
       v[k] = make_uint4(0, 0, 0, 0);
       if (e < positions) {
         const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
-        if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
-          v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
+        v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
+                                  t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
         e += step;
         b += b_step;
         pos += pos_step;

@@ -94,8 +94,8 @@ __device__ __forceinline__ bool stack_produce(const HaloParams& hp, const TileSc
           v[k] = make_uint4(0, 0, 0, 0);
           if (e < positions) {
             const int hh = t.p + r * p.dil_h - p.pad_h, ww = t.q0 + o - p.pad_w;
-            if (t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W)
-              v[k] = __ldg(reinterpret_cast<const uint4*>(img + (hh * p.W + ww) * 32 + h * 16));
+            v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
+                                      t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
             e += kProducers / 2;
             o += kProducers / 2;
             if (o >= L) {

@@ -234,6 +234,20 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 16-byte read-only global load, or zeros where `pred` is false (nothing is
+// read then): the registers are zeroed and the load is predicated in one
+// block, so no instruction waits for the loaded value until it is used --
+// several of these issue back to back with their round trips overlapping.
+__device__ __forceinline__ uint4 ldg16_or_zero(const void* ptr, bool pred) {
+  uint4 v;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\tmov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\t"
+      "mov.b32 %3, 0;\n\t@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(ptr), "r"(pred ? 1 : 0));
+  return v;
+}
+
 // ---------------------------------------------------------------- cp.async
 // 16-byte global->shared copy cached in L1 (taps of neighbouring output pixels
 // re-read the same input vectors).  src_bytes == 0 writes 16 zero bytes and
