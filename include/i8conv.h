@@ -109,11 +109,21 @@ typedef struct {
                                 16x8 patch, 2 = 128 consecutive pixels of the output laid out
                                 with the zero-padded input's row width (stride 1 only; the
                                 pixels past Q in each row are computed and discarded)       */
-  int32_t fused_filter;      /* halo kernel on single CTAs: 0 = convert the int8 filter to the
-                                fp16 operand copy in a separate kernel launched first (the
-                                convolution's prologue overlaps its tail), 1 = inside the
-                                convolution kernel (one launch per run; cooperative launch,
-                                all CTAs resident; measured slower)                         */
+  int32_t fused_filter;      /* where the int8 filter becomes the fp16 MMA operand:
+                                0 = auto (2 where the halo kernel keeps the whole filter
+                                resident in shared memory, else 3);
+                                1 = halo kernel on single CTAs: inside the convolution kernel,
+                                each CTA converting a share into a global fp16 copy behind a
+                                grid barrier (one launch per run; all CTAs resident;
+                                measured slower);
+                                2 = halo kernel (single CTAs or pairs) with a resident filter:
+                                every CTA converts the rows and K-slices it keeps straight
+                                into its shared-memory filter stages before its warps split
+                                into roles (one launch per run, no fp16 copy);
+                                I8C_ERR_UNSUPPORTED where the filter is not resident;
+                                3 = a separate conversion kernel launched first, writing the
+                                fp16 copy the filter TMA reads (the convolution's prologue
+                                overlaps its tail)                                           */
   int32_t tile_px;           /* transposed tiles: output pixels per tile (the MMA's N; on
                                 pairs split between the two CTAs), 0 = auto (the width whose
                                 tile count fills the SMs' waves best), else a multiple of 16

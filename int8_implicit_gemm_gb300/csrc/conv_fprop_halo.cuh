@@ -85,6 +85,12 @@ struct HaloParams {
   // for every run) as a parameter of its own.
   int tma_halo, nxs, box_w, box_h;
   uint32_t off_x8, x8_bytes, x8_box;
+  // Resident filter written by the kernel itself (f_smem = 1): all threads
+  // convert the int8 CxRSKx<32> filter f_src straight into the filter stages
+  // before the warp roles split; there is no fp16 copy in global memory and
+  // no filter TMA, so a run is one launch.
+  int f_smem;
+  const int8_t* f_src;
 };
 
 
@@ -587,6 +593,65 @@ __device__ __forceinline__ bool halo_produce_tma(const HaloParams& hp, const Til
 // CG == 2: CTA pairs (clusters of two) issue M = 256 MMAs whose A rows come
 // from the two CTAs' patches and whose B columns are split between them, so
 // each CTA stages half of every filter tile; rank 0 issues the MMAs, both
+// The resident filter straight from the int8 CxRSKx<32> filter into shared
+// memory, in the layout the filter TMA would give it: stage st holds K-slices
+// st*G .. st*G + G - 1 of the first unit, each BN/CG rows (output channels
+// n0 ..) of 32 fp16 channels, 64 bytes per row in the 64-byte swizzle (the
+// 16-byte chunk c of row j at chunk c ^ ((j >> 1) & 3) of an 8-row, 512-byte
+// atom).  Rows past K and slices past the filter are zeros, as the TMA's
+// out-of-bounds fill would make them.  Run by all the CTA's threads before
+// the warp roles split, kBatch 16-byte loads in flight per thread; the
+// caller's CTA (and cluster) barrier then orders the stores, made visible to
+// the tensor core's proxy here, before the first MMA.  (Measured: the same
+// work done by the non-producer warps after the split, overlapping the first
+// halo loads, made the whole kernel slower.)
+template <int BN, int CG>
+__device__ __forceinline__ void resident_filter_to_smem(const HaloParams& hp, uint8_t* smem, int G) {
+  constexpr int kBatch = 8;
+  constexpr int BNH = BN / CG;
+  const ConvParams& p = hp.c;
+  const TileSched ts = tile_sched<CG>();
+  if (ts.first >= hp.num_units) return;  // no unit, no MMA reads these stages
+  const WorkUnit wu = decode_unit(ts.first, hp);
+  const int n0 = (wu.tile % p.num_n_tiles) * BN + ts.rank * BNH;
+  const int kk0 = wu.cb0 * p.R * p.S;
+  const int kk_end = p.CB * p.R * p.S;
+  const int per_stage = G * BNH * 2;
+  const int total = hp.nbs * per_stage;
+  ptx::griddep_wait();  // the filter may come from the kernel before this one
+  for (int b0 = 0; b0 < total; b0 += kBatch * kHaloThreads) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = b0 + q * kHaloThreads + static_cast<int>(threadIdx.x);
+      const int st = i / per_stage, r = i - st * per_stage;
+      const int j = (r >> 1) % BNH, t = (r >> 1) / BNH;
+      const int kk = kk0 + st * G + t, n = n0 + j;
+      const bool live = i < total && kk < kk_end && n < p.K;
+      v[q] = ptx::ldg16_or_zero(
+          hp.f_src + ((static_cast<int64_t>(live ? kk : 0) * p.K + (live ? n : 0)) * 32 + (r & 1) * 16), live);
+    }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q) {
+      const int i = b0 + q * kHaloThreads + static_cast<int>(threadIdx.x);
+      if (i < total) {
+        const int st = i / per_stage, r = i - st * per_stage;
+        const int j = (r >> 1) % BNH, t = (r >> 1) / BNH, half = r & 1;
+        uint8_t* row = smem + hp.off_b + (static_cast<uint32_t>(st * G + t) * BNH + j) * 64;
+        const int sw = (j >> 1) & 3;
+        uint4 c0, c1;
+        i8x4_to_f16x4(v[q].x, c0.x, c0.y);
+        i8x4_to_f16x4(v[q].y, c0.z, c0.w);
+        i8x4_to_f16x4(v[q].z, c1.x, c1.y);
+        i8x4_to_f16x4(v[q].w, c1.z, c1.w);
+        *reinterpret_cast<uint4*>(row + (((2 * half) ^ sw) << 4)) = c0;
+        *reinterpret_cast<uint4*>(row + (((2 * half + 1) ^ sw) << 4)) = c1;
+      }
+    }
+  }
+  ptx::fence_proxy_async_smem();
+}
+
 // CTAs produce their own halo and drain their own 128 accumulator rows.
 template <int BN, int GT, int CG>
 __global__ void __launch_bounds__(kHaloThreads, 1)
@@ -654,11 +719,16 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::tmem_alloc_cg<CG>(tmem_slot, p.tmem_cols);
     ptx::tmem_relinquish_cg<CG>();
   }
+  if (hp.f_smem) resident_filter_to_smem<BN, CG>(hp, smem, GT > 0 ? GT : hp.bgroup);
   ptx::tc_fence_before();
   __syncthreads();
   if (CG == 2) ptx::cluster_sync();  // the peer's barriers are initialised before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // a filter written above (both CTAs of a pair, ordered by the barriers just
+  // passed) is complete: its stages are announced once, as the TMA would
+  if (hp.f_smem && threadIdx.x == 0)
+    for (int i = 0; i < nbs; ++i) ptx::mbar_arrive(&b_full[i]);
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -967,7 +1037,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     uint32_t g = 0, st = 0, bph = 0;
     bool ok = true;
     const int RS = p.R * p.S;
-    for (int unit = ts.first; ok && unit < hp.num_units; unit += ts.step) {
+    // (nothing to load when the epilogue warps write the filter)
+    for (int unit = ts.first; ok && !hp.f_smem && unit < hp.num_units; unit += ts.step) {
       if (hp.resident && unit != ts.first) break;  // every unit reuses the first unit's stages
       const WorkUnit wu = decode_unit(unit, hp);
       const int n0 = (wu.tile % p.num_n_tiles) * BN + ts.rank * BNH;

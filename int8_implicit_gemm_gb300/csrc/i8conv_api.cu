@@ -471,7 +471,8 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
   if (pl->kernel_variant == 6) {
     e = i8c::launch_filter_to_f16_stacked(f, pl->f16, s.C / 32, s.R, s.S, stream);
     if (e != cudaSuccess) return from_cuda(e);
-  } else if (pl->gbar == nullptr) {  // else the halo kernel converts the filter itself
+  } else if (pl->gbar == nullptr && !(pl->kernel_variant >= 2 && pl->halo.f_smem)) {
+    // else the halo kernel converts the filter itself
     e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
     if (e != cudaSuccess) return from_cuda(e);
   }
@@ -508,6 +509,7 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
         return I8C_ERR_CUDA;
       pl->tmap_x_ptr = x;
     }
+    hp.f_src = f;  // read only when the kernel writes its resident filter itself
     if (pl->gbar != nullptr) {
       hp.f_int8 = f;
       hp.f16 = pl->f16;
@@ -589,7 +591,7 @@ bool options_valid(const i8c_options& o) {
            o.timing_events < 0 || o.timing_events > 65536 || o.host_staging < 0 || o.host_staging > 2 ||
            o.kernel_variant < 0 || o.kernel_variant > 6 || o.halo_loads < 0 || o.halo_loads > 3 ||
            o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
-           o.fused_filter > 1 || o.filter_run < 0 || o.filter_run > 32 ||
+           o.fused_filter > 3 || o.filter_run < 0 || o.filter_run > 32 ||
            (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)));
 }
 
@@ -605,9 +607,9 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
   p->P = static_cast<int>(P);
   p->Q = static_cast<int>(Q);
   p->M = static_cast<int64_t>(s.N) * P * Q;
-  if (o.kernel_variant == 6 || (kStackAuto && o.kernel_variant == 0 && o.block_n == 0 && o.halo_loads == 0 &&
-                                 o.tile_shape == 0 && o.tail_split == 0 && o.fused_filter == 0 && o.tile_px == 0 &&
-                                 o.filter_run == 0)) {
+  if (o.kernel_variant == 6 ||
+      (kStackAuto && o.kernel_variant == 0 && o.block_n == 0 && o.halo_loads == 0 && o.tile_shape == 0 &&
+       o.tail_split == 0 && (o.fused_filter == 0 || o.fused_filter == 3) && o.tile_px == 0 && o.filter_run == 0)) {
     // The stacked-tap kernel: two taps per N = 128 MMA on CTA pairs.
     int smem = 0;
     if (!stack_layout(s, p->P, p->Q, &p->halo, &smem) || (o.kernel_variant == 0 && !p->halo.resident)) {
@@ -647,7 +649,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
       p->acc_buffers = 2;
       p->tmem_cols = 256;
       p->smem_bytes = smem;
-      return I8C_OK;
+      return o.fused_filter == 2 ? I8C_ERR_UNSUPPORTED : I8C_OK;  // its filter order has its own conversion
     }
   }
   // Kernel and tile width.  The halo kernel (16x8 output patches) is preferred
@@ -786,7 +788,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     // (2 x 306).
     bool use_tr = false;
     if (o.kernel_variant == 0 && o.block_n == 0 && o.halo_loads == 0 && o.tile_shape == 0 && o.tail_split == 0 &&
-        o.fused_filter == 0 && best.bn == 256 && cg == 1) {
+        (o.fused_filter == 0 || o.fused_filter == 3) && best.bn == 256 && cg == 1) {
       i8c::HaloParams h;
       int sm = 0;
       if (halo_layout(s, p->P, p->Q, 256, 1, 0, best.flat, &h, &sm)) {
@@ -917,6 +919,15 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
       p->halo.off_bar = p->halo.off_b + static_cast<uint32_t>(unit_stages * p->halo.bgroup * (bn / p->cta_group) * 64);
       halo_smem = static_cast<int>(p->halo.off_bar) + i8c::kHaloBarBytes + 1024;
     }
+    // fused_filter = 2, and auto: a resident filter is converted by the
+    // kernel itself into its stages (no fp16 copy, no conversion launch).
+    // Measured on the 64-channel 5x9 layer: 318.3-319.0 us per run against
+    // 318.9-319.3 with the conversion kernel; on the 32-channel 16x16 layer
+    // 6.5 against 8.4 us.
+    if (o.fused_filter == 2 || (o.fused_filter == 0 && p->halo.resident)) {
+      if (!p->halo.resident) return I8C_ERR_UNSUPPORTED;
+      p->halo.f_smem = 1;
+    }
     p->halo.full_units = ksplit > 1 || nsplit > 1 ? p->num_tiles - rem : p->num_tiles;
     p->halo.num_units = p->halo.full_units + (ksplit > 1 ? rem * ksplit : 0) + (nsplit > 1 ? rem * 2 : 0);
     if (ksplit > 1)
@@ -951,6 +962,9 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     p->tmem_cols = static_cast<uint32_t>(next_pow2(p->acc_buffers * bn + run_cols));
   }
   p->smem_bytes = p->kernel_variant >= 2 ? halo_smem : i8c::conv_smem_bytes(bn);
+  // the in-kernel resident filter exists for the halo kernels (single and pairs) only
+  if (o.fused_filter == 2 && !((p->kernel_variant == 2 || p->kernel_variant == 3) && p->halo.f_smem))
+    return I8C_ERR_UNSUPPORTED;
   return I8C_OK;
 }
 
@@ -1241,7 +1255,7 @@ i8c_status i8c_plan_get_info(const i8c_plan* pl, i8c_plan_info* info) {
   info->chunk_slices = pl->chunk_slices;
   info->acc_buffers = pl->acc_buffers;
   info->smem_bytes = pl->smem_bytes;
-  info->kernels_per_run = pl->gbar != nullptr ? 1 : 2;
+  info->kernels_per_run = pl->gbar != nullptr || (pl->kernel_variant >= 2 && pl->halo.f_smem) ? 1 : 2;
   info->kernel_variant = pl->kernel_variant;
   info->halo_staging = pl->kernel_variant >= 2 ? pl->halo.nstg : 0;
   info->filter_run = pl->kernel_variant >= 2 ? pl->halo.bgroup : 1;

@@ -137,7 +137,8 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     after 20 ms, every role stops, the kernel returns and the plan reports
     I8C_ERR_TIMEOUT (gather kernel, halo kernel, halo kernel on CTA pairs,
     transposed tiles, on single CTAs and on pairs, stacked taps; halos by
-    registers and by TMA).
+    registers and by TMA; resident filters written by the kernel itself and
+    loaded by TMA from the conversion kernel's copy).
     The same context then runs a correct convolution."""
     import int8_implicit_gemm_gb300 as ext
     torch = torch_cuda
@@ -147,11 +148,13 @@ def test_bounded_wait_reports_timeout_and_context_survives(torch_cuda):
     xp, fp = gpu_util.packed_inputs(x, f)
     xd, fd = torch.from_numpy(xp).cuda(), torch.from_numpy(fp).cuda()
     y = torch.zeros(2 * 64 * 256, dtype=torch.int8, device="cuda")
-    for kernel, loads in ((1, 0), (2, 0), (3, 0), (4, 0), (5, 0), (6, 0), (2, 3), (3, 3), (4, 3), (5, 3)):
+    for kernel, loads, fused in ((1, 0, 0), (2, 0, 0), (3, 0, 0), (4, 0, 0), (5, 0, 0), (6, 0, 0), (2, 3, 0),
+                                 (3, 3, 0), (4, 3, 0), (5, 3, 0), (2, 0, 2), (3, 0, 2), (3, 0, 3)):
         bad = ext.Plan(shape, wait_timeout_us=20000, debug_flags=ext.I8C_DEBUG_SKIP_FIRST_ARRIVE,
-                       kernel_variant=kernel, halo_loads=loads)
+                       kernel_variant=kernel, halo_loads=loads, fused_filter=fused,
+                       block_n=64 if fused == 2 else 0)  # one 64-channel tile: a resident filter
         bad.run(xd, fd, y, 1.0)
-        assert bad.status() == ext.I8C_ERR_TIMEOUT, (kernel, loads)
+        assert bad.status() == ext.I8C_ERR_TIMEOUT, (kernel, loads, fused)
         assert bad.status() == ext.I8C_OK          # the status word was cleared
     y_ref, _ = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
     y2, _ = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, want_acc=False)

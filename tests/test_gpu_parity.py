@@ -183,9 +183,11 @@ def _full_oracle(wl):
                                 dict(kernel_variant=3), dict(kernel_variant=4), dict(kernel_variant=5),
                                 dict(kernel_variant=6), dict(kernel_variant=2, halo_loads=3),
                                 dict(kernel_variant=3, halo_loads=3), dict(kernel_variant=4, halo_loads=3),
-                                dict(kernel_variant=5, halo_loads=3)],
+                                dict(kernel_variant=5, halo_loads=3), dict(fused_filter=3),
+                                dict(kernel_variant=2, fused_filter=2)],
                          ids=["auto", "staged", "direct", "pair", "transposed", "transposed-pair", "stacked",
-                              "halo-tma", "pair-tma", "transposed-tma", "transposed-pair-tma"])
+                              "halo-tma", "pair-tma", "transposed-tma", "transposed-pair-tma", "filter-conversion-kernel",
+                              "single-filter-in-kernel"])
 @pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
 def test_full_size_workloads(wl, kw):
     """The five workloads at full size, in the launch configuration the
@@ -383,13 +385,28 @@ def test_channel_epilogue_full_size_bench_workload():
     ((3, 64, 20, 20, 64, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, block_n=64, num_ctas=2)),
     ((2, 96, 17, 17, 32, 3, 3, 1, 1, 2, 2, 1, 1), dict(kernel_variant=2, num_ctas=2)),
     ((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(num_ctas=1)),
-], ids=["dilated-pair", "dilated-single", "3x3-two-blocks", "stride2-three-blocks", "16x16"])
-def test_resident_filter_exact(shape, opts):
+    ((2, 64, 20, 20, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, block_n=64, num_ctas=2)),
+    ((2, 32, 24, 24, 32, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=3, block_n=64, num_ctas=2)),
+], ids=["dilated-pair", "dilated-single", "3x3-two-blocks", "stride2-three-blocks", "16x16",
+        "rows-past-K", "pair-rows-past-K"])
+@pytest.mark.parametrize("fused", [3, 2, 0], ids=["tma", "in-kernel", "auto"])
+def test_resident_filter_exact(shape, opts, fused):
     """One output-channel tile and whole-tile units: the filter stages are
     loaded once per CTA and reused by every later tile (few CTAs, so each runs
-    many tiles); bit-exact against the oracle."""
+    many tiles), either by TMA from the fp16 copy the conversion kernel wrote
+    (fused_filter = 3) or written by the kernel's own threads straight from
+    the int8 filter before the warp roles split (fused_filter = 2, the auto
+    choice for a resident filter; the tile's rows past K are zeros);
+    bit-exact against the oracle."""
     import int8_implicit_gemm_gb300 as ext
-    plan = ext.Plan(shape, **opts)
+    opts = dict(opts, fused_filter=fused)
+    try:
+        plan = ext.Plan(shape, **opts)
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED and shape[4] < opts.get("block_n", 0):
+            pytest.skip("block_n wider than K is not planned")
+        raise
+    assert plan.info["kernels_per_run"] == (2 if fused == 3 else 1)
     assert plan.info["filter_resident"] == 1
     assert plan.info["work_units"] > plan.info["num_ctas"] // (2 if plan.info["kernel_variant"] == 3 else 1)
     plan.destroy()

@@ -196,6 +196,8 @@ PLAN_FORMS = [
     dict(kernel_variant=2, tile_shape=2, halo_loads=3), dict(kernel_variant=3, block_n=64, halo_loads=3),
     dict(kernel_variant=4, halo_loads=3), dict(kernel_variant=4, tile_px=256, halo_loads=3),
     dict(kernel_variant=5, halo_loads=3), dict(kernel_variant=5, tile_px=128, halo_loads=3),
+    dict(fused_filter=2), dict(kernel_variant=2, fused_filter=2), dict(kernel_variant=3, fused_filter=2),
+    dict(kernel_variant=3, halo_loads=3, fused_filter=2), dict(fused_filter=3), dict(kernel_variant=3, fused_filter=3),
 ]
 
 SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + STACKED_SHAPES + [
@@ -276,3 +278,21 @@ def test_planted_off_by_one_is_caught(ext, plant):
         bad["off_x8"] += 1024
     with pytest.raises(AssertionError):
         check_layout(shape, bad)
+
+
+def test_in_kernel_resident_filter_needs_a_resident_halo_plan(ext):
+    """fused_filter = 2 (the kernel writes its resident filter into shared
+    memory itself) is planned only where the halo kernel keeps the whole
+    filter resident; elsewhere the planner refuses it on the host."""
+    dilated = (8, 32, 512, 512, 64, 5, 9, 2, 4, 1, 1, 2, 3)      # 45 K-slices x 32 rows per CTA: resident
+    wide = (32, 128, 112, 112, 256, 3, 3, 1, 1, 2, 2, 1, 1)      # 36 K-slices x 256 rows: streamed
+    L = ext.i8c_plan_layout(dilated, 152, kernel_variant=3, fused_filter=2)
+    check_layout(dilated, L)
+    assert L["filter_stages"] * L["filter_run"] == 45
+    for shape, opts in ((wide, dict(kernel_variant=2, fused_filter=2)),
+                        (dilated, dict(kernel_variant=4, fused_filter=2)),
+                        (dilated, dict(kernel_variant=6, fused_filter=2)),
+                        (dilated, dict(kernel_variant=1, fused_filter=2))):
+        with pytest.raises(ext.I8ConvError) as e:
+            ext.i8c_plan_layout(shape, 152, **opts)
+        assert e.value.status == ext.I8C_ERR_UNSUPPORTED, opts
