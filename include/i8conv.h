@@ -353,6 +353,26 @@ i8c_status i8c_plan_run_ex(const i8c_plan* plan, const int8_t* x, const int8_t* 
 i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t* f, int32_t* acc,
                             cudaStream_t stream);
 
+/* Weight prepacking.  The filter operand transform (int8 -> the fp16
+ * operand copy, or the stacked-tap order) is done once, for filters that
+ * stay fixed across runs (inference weights): i8c_plan_set_filter converts
+ * the int8 CxRSKx<32> filter f (DEVICE, 16-byte aligned; read on `stream`
+ * before the call's work completes) into plan-owned memory -- for plans
+ * whose kernel writes its resident filter itself, an int8 copy of f that
+ * every run converts in shared memory -- and i8c_plan_run_prepacked(_ex)
+ * then run the convolution alone on x (DEVICE) into y (DEVICE), as
+ * i8c_plan_run(_ex) would with that filter: one kernel launch per run.
+ * The copy is the plan's: f may change or be freed after set_filter's work
+ * is done.  Any i8c_plan_run* call that takes a filter replaces the copy;
+ * run_prepacked then returns I8C_ERR_INVALID_ARG until set_filter is called
+ * again (also before the first set_filter).  Not thread-safe per plan, like
+ * every other plan call. */
+i8c_status i8c_plan_set_filter(const i8c_plan* plan, const int8_t* f, cudaStream_t stream);
+i8c_status i8c_plan_run_prepacked(const i8c_plan* plan, const int8_t* x, int8_t* y, float alpha,
+                                  cudaStream_t stream);
+i8c_status i8c_plan_run_prepacked_ex(const i8c_plan* plan, const int8_t* x, int8_t* y, float alpha,
+                                     const i8c_epilogue* ep, cudaStream_t stream);
+
 /* End-to-end run on HOST buffers: copies x and f from host memory into the
  * plan's staging buffers, runs, and copies y back, all on `stream`.  The plan
  * must have been created with host_staging = 1.  Pinned (page-locked) host

@@ -69,6 +69,29 @@ i8c_status i8c_probe_imma_s8(int32_t num_ctas, int32_t warps_per_cta, int32_t it
 i8c_status i8c_probe_mma_f8(int32_t n, int32_t num_ctas, int32_t iters, long long* cycles, float* elapsed_ms,
                             cudaStream_t stream);
 
+/* L2 -> shared memory read rate of the SMs (the bound on how fast a CTA can
+ * stream filter stages and halos): num_ctas CTAs of 512 threads, one per SM,
+ * each moving `iters` chunks of chunk_bytes (a multiple of 16, at most 49152)
+ * from the DEVICE buffer src (16-byte aligned, region_bytes long, a multiple
+ * of chunk_bytes; small enough to stay in L2 once read, or not, as the
+ * measurement wants) into four shared-memory buffers.  Step i of CTA c reads
+ * chunk (c + i * num_ctas) mod (region_bytes / chunk_bytes).  mode 0: one
+ * thread keeps four untiled bulk copies (cp.async.bulk, the TMA) in flight;
+ * mode 1: every thread loads 16-byte vectors, four in flight, and stores
+ * them to shared memory (chunk_bytes a multiple of 32768); mode 2: clusters
+ * of two CTAs (num_ctas even, chunk_bytes a multiple of 32), each copying
+ * half of every chunk into both CTAs' buffer with one multicast bulk copy
+ * (this GPU's memory only), four chunks in flight, a buffer refilled once
+ * both CTAs hold its previous chunk; step i of cluster c reads chunk
+ * (c + i * num_ctas / 2) mod (region_bytes / chunk_bytes), and the bytes
+ * counted per CTA are the bytes it received.
+ *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles of the
+ *           loop, bytes moved, 1 if every bounded wait succeeded
+ *   elapsed_ms as for i8c_probe_mma_f16.  Synchronises `stream`. */
+i8c_status i8c_probe_l2_ingress(const void* src, int64_t region_bytes, int32_t chunk_bytes, int32_t mode,
+                                int32_t num_ctas, int32_t iters, long long* cycles, float* elapsed_ms,
+                                cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -125,6 +125,9 @@ def _load() -> ctypes.CDLL:
         "i8c_plan_create": [S, ctypes.POINTER(Options), ctypes.POINTER(P)],
         "i8c_plan_run": [P, P, P, P, F, P],
         "i8c_plan_run_ex": [P, P, P, P, F, ctypes.POINTER(Epilogue), P],
+        "i8c_plan_set_filter": [P, P, P],
+        "i8c_plan_run_prepacked": [P, P, P, F, P],
+        "i8c_plan_run_prepacked_ex": [P, P, P, F, ctypes.POINTER(Epilogue), P],
         "i8c_conv2d_fprop_ex": [P, P, P, S, F, ctypes.POINTER(Epilogue), P],
         "i8c_plan_run_acc": [P, P, P, P, P],
         "i8c_plan_run_host": [P, P, P, P, F, P],
@@ -153,6 +156,8 @@ def _load() -> ctypes.CDLL:
     lib.i8c_probe_imma_s8.restype = ctypes.c_int
     lib.i8c_probe_mma_f8.argtypes = [I32, I32, I32, P, ctypes.POINTER(F), P]
     lib.i8c_probe_mma_f8.restype = ctypes.c_int
+    lib.i8c_probe_l2_ingress.argtypes = [P, I64, I32, I32, I32, I32, P, ctypes.POINTER(F), P]
+    lib.i8c_probe_l2_ingress.restype = ctypes.c_int
     lib.i8c_status_string.argtypes = [ctypes.c_int]
     lib.i8c_status_string.restype = ctypes.c_char_p
     lib.i8c_launch_count.argtypes = []
@@ -339,6 +344,18 @@ def i8c_probe_imma_s8(num_ctas: int, warps_per_cta: int, iters: int, stream=None
     return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
 
 
+def i8c_probe_l2_ingress(src, region_bytes: int, chunk_bytes: int, mode: int, num_ctas: int, iters: int,
+                         stream=None):
+    """L2 -> shared memory read-rate probe over the device tensor `src`:
+    (per-CTA [cycles, bytes, ok] as [num_ctas, 3], elapsed ms)."""
+    import torch
+    buf = torch.zeros(3 * num_ctas, dtype=torch.int64, device="cuda")
+    ms = ctypes.c_float()
+    _check(lib.i8c_probe_l2_ingress(src.data_ptr(), region_bytes, chunk_bytes, mode, num_ctas, iters, buf.data_ptr(),
+                                    ctypes.byref(ms), _stream(stream)), "i8c_probe_l2_ingress")
+    return buf.cpu().numpy().reshape(num_ctas, 3), ms.value
+
+
 def i8c_probe_mma_f8(n: int, num_ctas: int, iters: int, stream=None):
     """tcgen05 kind::f8f6f4 (e4m3) probe: (per-CTA cycles [num_ctas, 3], elapsed ms)."""
     import torch
@@ -377,6 +394,21 @@ class Plan:
         ep = Epilogue(None if alpha_k is None else _ptr(alpha_k), None if bias is None else _ptr(bias), int(bool(relu)))
         _check(lib.i8c_plan_run_ex(self.handle, _ptr(x), _ptr(f), _ptr(y), ctypes.c_float(alpha), ctypes.byref(ep),
                                    _stream(stream)), "i8c_plan_run_ex")
+
+    def set_filter(self, f, stream=None) -> None:
+        """Weight prepacking: convert the filter once into the plan's operand
+        copy (i8c_plan_set_filter), for run_prepacked."""
+        _check(lib.i8c_plan_set_filter(self.handle, _ptr(f), _stream(stream)), "i8c_plan_set_filter")
+
+    def run_prepacked(self, x, y, alpha: float, stream=None, alpha_k=None, bias=None, relu: bool = False) -> None:
+        """As run, with the filter given to set_filter (no conversion launch)."""
+        if alpha_k is None and bias is None and not relu:
+            _check(lib.i8c_plan_run_prepacked(self.handle, _ptr(x), _ptr(y), ctypes.c_float(alpha), _stream(stream)),
+                   "i8c_plan_run_prepacked")
+            return
+        ep = Epilogue(None if alpha_k is None else _ptr(alpha_k), None if bias is None else _ptr(bias), int(bool(relu)))
+        _check(lib.i8c_plan_run_prepacked_ex(self.handle, _ptr(x), _ptr(y), ctypes.c_float(alpha), ctypes.byref(ep),
+                                             _stream(stream)), "i8c_plan_run_prepacked_ex")
 
     def run_acc(self, x, f, acc, stream=None) -> None:
         _check(lib.i8c_plan_run_acc(self.handle, _ptr(x), _ptr(f), _ptr(acc), _stream(stream)), "i8c_plan_run_acc")

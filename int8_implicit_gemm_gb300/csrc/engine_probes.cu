@@ -102,6 +102,115 @@ __global__ void __launch_bounds__(128, 1) f8_rate_kernel(int iters, long long* o
   }
 }
 
+// L2 -> shared memory read rate of one SM.  Mode 0: one thread keeps
+// kIngressBufs untiled bulk copies (TMA) of `chunk` bytes in flight into a
+// ring of shared-memory buffers; mode 1: all threads load 16-byte vectors
+// (ld.global.nc, kIngressVecs in flight per thread) and store them to shared
+// memory.  Step i of CTA c reads chunk (c + i * gridDim.x) mod nchunks.
+constexpr int kIngressBufs = 4;
+constexpr int kIngressThreads = 512;
+constexpr int kIngressVecs = 4;
+
+__global__ void __launch_bounds__(kIngressThreads, 1)
+    ingress_kernel(const uint8_t* __restrict__ src, int64_t nchunks, int chunk, int mode, int iters,
+                   long long* out) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar[kIngressBufs];
+  __shared__ uint64_t empty[kIngressBufs];  // mode 2: both CTAs of the cluster hold the buffer's chunk
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kIngressBufs; ++b) {
+      ptx::mbar_init(&bar[b], 1);
+      ptx::mbar_init(&empty[b], 2);
+    }
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (mode == 2) ptx::cluster_sync();  // both CTAs' barriers exist before any multicast lands
+  bool ok = true;
+  const long long t0 = clock64();
+  if (mode == 2) {
+    // clusters of two: each CTA copies its half of every chunk into both
+    // CTAs' buffer (multicast); a buffer is refilled only after both CTAs
+    // have received its previous chunk whole
+    if (threadIdx.x == 0) {
+      const uint32_t rank = blockIdx.x & 1u;
+      const int64_t cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+      const int half = chunk / 2;
+      int issued = 0;
+      for (int i = 0; i < iters && ok; ++i) {
+        const int b = i % kIngressBufs;
+        if (i >= kIngressBufs) {
+          const uint32_t ph = ((i / kIngressBufs) - 1) & 1u;
+          if (!ptx::mbar_wait(&bar[b], ph, 2000000000ull, nullptr)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive(&empty[b]);
+          ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_addr(&empty[b]), rank ^ 1u), 1);
+          if (!ptx::mbar_wait<true>(&empty[b], ph, 2000000000ull, nullptr)) {
+            ok = false;
+            break;
+          }
+        }
+        const int64_t c = (cl + static_cast<int64_t>(i) * ncl) % nchunks;
+        ptx::mbar_arrive_expect_tx(&bar[b], static_cast<uint32_t>(chunk));
+        ptx::bulk_load_multicast(smem + static_cast<size_t>(b) * chunk + rank * half, src + c * chunk + rank * half,
+                                 static_cast<uint32_t>(half), &bar[b], 3);
+        issued = i + 1;
+      }
+      // every chunk issued into this CTA has landed (a step whose gate failed
+      // was not issued); the peer's halves are covered by the same barriers
+      const int first = issued > kIngressBufs ? issued - kIngressBufs : 0;
+      for (int i = first; i < issued; ++i)
+        if (!ptx::mbar_wait(&bar[i % kIngressBufs], (i / kIngressBufs) & 1u, 2000000000ull, nullptr)) ok = false;
+    }
+  } else if (mode == 0) {
+    if (threadIdx.x == 0) {
+      int issued = 0;
+      for (int i = 0; i < iters && ok; ++i) {
+        const int b = i % kIngressBufs;
+        // the buffer's previous copy (kIngressBufs steps ago) has landed
+        if (i >= kIngressBufs && !ptx::mbar_wait(&bar[b], ((i / kIngressBufs) - 1) & 1u, 2000000000ull, nullptr)) {
+          ok = false;
+          break;
+        }
+        const int64_t c = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) % nchunks;
+        ptx::mbar_arrive_expect_tx(&bar[b], static_cast<uint32_t>(chunk));
+        ptx::bulk_load(smem + static_cast<size_t>(b) * chunk, src + c * chunk, static_cast<uint32_t>(chunk), &bar[b]);
+        issued = i + 1;
+      }
+      // the copies still in flight
+      const int first = issued > kIngressBufs ? issued - kIngressBufs : 0;
+      for (int i = first; i < issued; ++i)
+        if (!ptx::mbar_wait(&bar[i % kIngressBufs], (i / kIngressBufs) & 1u, 2000000000ull, nullptr)) ok = false;
+    }
+  } else {
+    const int vecs = chunk / 16;  // a multiple of kIngressThreads * kIngressVecs
+    for (int i = 0; i < iters; ++i) {
+      const int64_t c = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) % nchunks;
+      const uint4* s = reinterpret_cast<const uint4*>(src + c * chunk);
+      uint4* d = reinterpret_cast<uint4*>(smem + static_cast<size_t>(i % kIngressBufs) * chunk);
+      for (int v0 = 0; v0 < vecs; v0 += kIngressThreads * kIngressVecs) {
+        uint4 v[kIngressVecs];
+#pragma unroll
+        for (int q = 0; q < kIngressVecs; ++q) v[q] = ptx::ldg16_or_zero(s + v0 + q * kIngressThreads + threadIdx.x, true);
+#pragma unroll
+        for (int q = 0; q < kIngressVecs; ++q) d[v0 + q * kIngressThreads + threadIdx.x] = v[q];
+      }
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  // the peer may still be delivering into this CTA (mode 2): leave together
+  if (mode == 2) ptx::cluster_sync();
+  if (threadIdx.x == 0) {
+    out[3 * blockIdx.x + 0] = t1 - t0;
+    out[3 * blockIdx.x + 1] = static_cast<long long>(iters) * chunk;
+    out[3 * blockIdx.x + 2] = ok ? 1 : 0;
+  }
+}
+
 static cudaError_t timed(void (*launch)(cudaStream_t), float* ms, cudaStream_t stream) {
   cudaEvent_t e0, e1;
   cudaError_t e = cudaEventCreate(&e0);
@@ -139,6 +248,31 @@ void launch_f8(cudaStream_t s) {
   i8c::f8_rate_kernel<N><<<g_f8.ctas, 128, g_f8.smem, s>>>(g_f8.iters, g_f8.out);
   i8c::g_launches.fetch_add(1, std::memory_order_relaxed);
 }
+struct IngressArgs {
+  const uint8_t* src;
+  int64_t nchunks;
+  int chunk, mode, ctas, iters, smem;
+  long long* out;
+} g_ingress;
+void launch_ingress(cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(g_ingress.ctas));
+  cfg.blockDim = dim3(i8c::kIngressThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(g_ingress.smem);
+  cfg.stream = s;
+  if (g_ingress.mode == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaLaunchKernelEx(&cfg, i8c::ingress_kernel, g_ingress.src, g_ingress.nchunks, g_ingress.chunk, g_ingress.mode,
+                     g_ingress.iters, g_ingress.out);
+  i8c::g_launches.fetch_add(1, std::memory_order_relaxed);
+}
 void launch_imma(cudaStream_t s) {
   i8c::imma_rate_kernel<<<g_imma.ctas, 32 * g_imma.warps, 0, s>>>(g_imma.iters, g_imma.out, g_imma.sink);
   i8c::g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -170,4 +304,22 @@ extern "C" i8c_status i8c_probe_mma_f8(int32_t n, int32_t num_ctas, int32_t iter
     return I8C_ERR_CUDA;
   g_f8 = {num_ctas, iters, smem, cycles};
   return i8c::timed(launch, elapsed_ms, stream) == cudaSuccess ? I8C_OK : I8C_ERR_CUDA;
+}
+
+extern "C" i8c_status i8c_probe_l2_ingress(const void* src, int64_t region_bytes, int32_t chunk_bytes, int32_t mode,
+                                           int32_t num_ctas, int32_t iters, long long* cycles, float* elapsed_ms,
+                                           cudaStream_t stream) {
+  if (src == nullptr || cycles == nullptr || elapsed_ms == nullptr || num_ctas < 1 || iters < 1 ||
+      mode < 0 || mode > 2 || chunk_bytes < 16 || chunk_bytes > 49152 || chunk_bytes % 16 != 0 ||
+      (mode == 2 && (chunk_bytes % 32 != 0 || num_ctas % 2 != 0)) ||
+      (mode == 1 && chunk_bytes % (16 * i8c::kIngressThreads * i8c::kIngressVecs) != 0) ||
+      region_bytes < chunk_bytes || region_bytes % chunk_bytes != 0 || (reinterpret_cast<uintptr_t>(src) & 15u))
+    return I8C_ERR_INVALID_ARG;
+  const int smem = i8c::kIngressBufs * chunk_bytes + 1024;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void*>(i8c::ingress_kernel),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return I8C_ERR_CUDA;
+  g_ingress = {static_cast<const uint8_t*>(src), region_bytes / chunk_bytes, chunk_bytes, mode, num_ctas, iters,
+               smem, cycles};
+  return i8c::timed(launch_ingress, elapsed_ms, stream) == cudaSuccess ? I8C_OK : I8C_ERR_CUDA;
 }

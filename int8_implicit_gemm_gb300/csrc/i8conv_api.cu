@@ -53,6 +53,9 @@ struct i8c_plan {
   // optional per-launch timing of the convolution kernel
   std::vector<cudaEvent_t> ev_start, ev_end;
   mutable int64_t ev_recorded = 0;
+  // i8c_plan_set_filter was called: f16 holds the operand copy (or, for a
+  // kernel that writes its resident filter itself, an int8 copy of f)
+  mutable bool prepacked = false;
 };
 
 namespace {
@@ -464,16 +467,34 @@ ConvParams make_params(const i8c_plan* pl, const int8_t* x, float alpha) {
   return p;
 }
 
+// The filter operand transform of a plan: the stacked order for the
+// stacked-tap kernel, else the fp16 copy in the CxRSKx<32> order; nothing
+// for the kernels that convert the filter themselves.
+cudaError_t convert_filter(const i8c_plan* pl, const int8_t* f, cudaStream_t stream) {
+  const i8c_conv_shape& s = pl->shape;
+  if (pl->kernel_variant == 6) return i8c::launch_filter_to_f16_stacked(f, pl->f16, s.C / 32, s.R, s.S, stream);
+  return i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
+}
+
+bool converts_in_kernel(const i8c_plan* pl) {
+  return pl->gbar != nullptr || (pl->kernel_variant >= 2 && pl->kernel_variant <= 3 && pl->halo.f_smem);
+}
+
+// prepacked: the filter was converted by i8c_plan_set_filter; f is unused
+// (the kernels that write their resident filter themselves read the plan's
+// int8 copy instead)
 i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t* y, int32_t* acc, float alpha,
-                    cudaStream_t stream, const i8c_epilogue* ep = nullptr) {
+                    cudaStream_t stream, const i8c_epilogue* ep = nullptr, bool prepacked = false) {
   const i8c_conv_shape& s = pl->shape;
   cudaError_t e = cudaSuccess;
-  if (pl->kernel_variant == 6) {
-    e = i8c::launch_filter_to_f16_stacked(f, pl->f16, s.C / 32, s.R, s.S, stream);
-    if (e != cudaSuccess) return from_cuda(e);
-  } else if (pl->gbar == nullptr && !(pl->kernel_variant >= 2 && pl->halo.f_smem)) {
-    // else the halo kernel converts the filter itself
-    e = i8c::launch_filter_to_f16(f, pl->f16, static_cast<int64_t>(s.K) * s.C * s.R * s.S, stream);
+  if (prepacked) {
+    f = reinterpret_cast<const int8_t*>(pl->f16);
+  } else {
+    pl->prepacked = false;  // a run with its own filter replaces the prepacked copy
+  }
+  if (prepacked) {
+  } else if (pl->kernel_variant == 6 || !converts_in_kernel(pl)) {
+    e = convert_filter(pl, f, stream);
     if (e != cudaSuccess) return from_cuda(e);
   }
   ConvParams p = make_params(pl, x, alpha);
@@ -510,7 +531,7 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
       pl->tmap_x_ptr = x;
     }
     hp.f_src = f;  // read only when the kernel writes its resident filter itself
-    if (pl->gbar != nullptr) {
+    if (pl->gbar != nullptr && !prepacked) {  // prepacked: the TMA reads the converted copy
       hp.f_int8 = f;
       hp.f16 = pl->f16;
       hp.f_vecs = static_cast<int64_t>(s.K) * s.C * s.R * s.S / 16;
@@ -1323,6 +1344,36 @@ i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t*
   if (plan == nullptr || x == nullptr || f == nullptr || acc == nullptr) return I8C_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(f) || !aligned16(acc)) return I8C_ERR_MISALIGNED;
   return run_plan(plan, x, f, nullptr, acc, 1.0f, stream);
+}
+
+i8c_status i8c_plan_set_filter(const i8c_plan* plan, const int8_t* f, cudaStream_t stream) {
+  if (plan == nullptr || f == nullptr) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(f)) return I8C_ERR_MISALIGNED;
+  // the kernels that write their resident filter themselves read an int8
+  // copy of it at every run; every other kernel reads the converted operand
+  const cudaError_t e =
+      plan->kernel_variant != 6 && converts_in_kernel(plan) && plan->gbar == nullptr
+          ? cudaMemcpyAsync(plan->f16, f, plan->f_bytes, cudaMemcpyDeviceToDevice, stream)
+          : convert_filter(plan, f, stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  plan->prepacked = true;
+  return I8C_OK;
+}
+
+i8c_status i8c_plan_run_prepacked(const i8c_plan* plan, const int8_t* x, int8_t* y, float alpha,
+                                  cudaStream_t stream) {
+  if (plan == nullptr || x == nullptr || y == nullptr || !plan->prepacked) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  return run_plan(plan, x, nullptr, y, nullptr, alpha, stream, nullptr, true);
+}
+
+i8c_status i8c_plan_run_prepacked_ex(const i8c_plan* plan, const int8_t* x, int8_t* y, float alpha,
+                                     const i8c_epilogue* ep, cudaStream_t stream) {
+  if (plan == nullptr || x == nullptr || y == nullptr || !plan->prepacked) return I8C_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return I8C_ERR_MISALIGNED;
+  if (ep != nullptr && ((ep->alpha != nullptr && !aligned16(ep->alpha)) || (ep->bias != nullptr && !aligned16(ep->bias))))
+    return I8C_ERR_MISALIGNED;
+  return run_plan(plan, x, nullptr, y, nullptr, alpha, stream, ep, true);
 }
 
 i8c_status i8c_plan_run_host(const i8c_plan* pl, const int8_t* x_host, const int8_t* f_host, int8_t* y_host,

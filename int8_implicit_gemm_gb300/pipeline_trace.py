@@ -13,10 +13,14 @@ per run configuration:
     wait's fixed cost); nr_*: how many of those waits found the phase still
     open (halo kernel);
   - issue / post (transposed tiles): cycles inside the MMA issue blocks and in
-    the loop bookkeeping after them;
+    the loop bookkeeping after them; per-CTA timeline (median, max in
+    microseconds): entry to the MMA loop, the loop, loop end to exit, and
+    the first entry to the last exit over all CTAs;
   - prod_* (halo kernel): producer thread 0's time from its halo stage being
     free to its arrival, from its arrival to the next stage being free, and
-    its period per channel block, in microseconds;
+    its period per channel block, in microseconds (the *_cta1 keys: the same
+    for CTA 1, a pair's rank 1; cta1_arrive_lag_us: how much later rank 1
+    announces each halo stage than rank 0);
   - cb_interval_us: median and maximum time between consecutive halo
     acquisitions of the MMA warp.
 
@@ -60,6 +64,18 @@ def trace_workload(shape, alpha, runs: int = 6, **opts) -> dict:
         out.update(cycles=t1 - t0, slices=slices, per_slice=round((t1 - t0) / max(1, slices), 1),
                    stall_acc=int(tr[4][1]), stall_b=int(tr[4][2]), stall_h=int(tr[4][3]), issue=int(tr[4][7]),
                    post=int(tr[4][8]), stall_h_first=int(tr[4][9]))
+        # per-CTA global-timer marks: kernel entry (8), MMA loop start (24)
+        # and end (25), kernel exit (9)
+        st, ls, le, en = tr[8][:512], tr[24][:512], tr[25][:512], tr[9][:512]
+        ok = (st > 0) & (ls > 0) & (le > 0) & (en > 0)
+        if ok.any():
+            us = lambda v: round(float(v) / 1e3, 2)
+            out["cta_span_us"] = [us(np.min(en[ok] - st[ok])), us(np.max(en[ok] - st[ok]))]
+            out["entry_to_loop_us"] = [us(np.median(ls[ok] - st[ok])), us(np.max(ls[ok] - st[ok]))]
+            out["loop_us"] = [us(np.median(le[ok] - ls[ok])), us(np.max(le[ok] - ls[ok]))]
+            out["loop_to_exit_us"] = [us(np.median(en[ok] - le[ok])), us(np.max(en[ok] - le[ok]))]
+            out["first_entry_to_last_exit_us"] = us(np.max(en[ok]) - np.min(st[ok]))
+            out["entry_skew_us"] = us(np.max(st[ok]) - np.min(st[ok]))
     elif info["kernel_variant"] >= 2:
         slices = int(tr[4][0])  # K-slices issued by CTA 0
         out.update(cycles=t1 - t0, slices=slices, per_slice=round((t1 - t0) / max(1, slices), 1),
@@ -70,12 +86,21 @@ def trace_workload(shape, alpha, runs: int = 6, **opts) -> dict:
         if ok.any():
             out["cta_span_us"] = [round(float(np.min(en[ok] - st[ok])) / 1e3, 2),
                                   round(float(np.max(en[ok] - st[ok])) / 1e3, 2)]
-        free, arrive = tr[16], tr[17]
-        m = int(np.sum((free > 0) & (arrive > 0)))
-        if m > 3:
-            out["prod_free_to_arrive_us"] = round(float(np.median(arrive[1:m] - free[1:m])) / 1e3, 3)
-            out["prod_arrive_to_next_free_us"] = round(float(np.median(free[2:m] - arrive[1:m - 1])) / 1e3, 3)
-            out["prod_period_us"] = round(float(np.median(np.diff(arrive[1:m]))) / 1e3, 3)
+        # producer thread 0 of CTA 0 and of CTA 1 (a pair's rank 1)
+        for cta, suffix in ((0, ""), (1, "_cta1")):
+            free, arrive = tr[16 + 2 * cta], tr[17 + 2 * cta]
+            m = int(np.sum((free > 0) & (arrive > 0)))
+            if m > 3:
+                out["prod_free_to_arrive_us" + suffix] = round(float(np.median(arrive[1:m] - free[1:m])) / 1e3, 3)
+                out["prod_arrive_to_next_free_us" + suffix] = round(
+                    float(np.median(free[2:m] - arrive[1:m - 1])) / 1e3, 3)
+                out["prod_period_us" + suffix] = round(float(np.median(np.diff(arrive[1:m]))) / 1e3, 3)
+        if info["kernel_variant"] == 3:
+            a0, a1 = tr[17], tr[19]
+            m = int(min(np.sum(a0 > 0), np.sum(a1 > 0)))
+            if m > 3:
+                # how much later the pair's rank 1 announces the same halo stage
+                out["cta1_arrive_lag_us"] = round(float(np.median(a1[1:m] - a0[1:m])) / 1e3, 3)
         acq = tr[20]
         n = int(np.sum(acq > 0))
         if n > 2:

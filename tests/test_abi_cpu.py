@@ -78,6 +78,15 @@ def test_null_pointers_rejected(ext):
     assert st == ext.I8C_ERR_INVALID_ARG
 
 
+def test_prepacked_argument_checks(ext):
+    """Weight prepacking refuses a missing plan, filter or buffer before
+    touching a device."""
+    a = ctypes.c_void_p(16)
+    assert ext.lib.i8c_plan_set_filter(None, a, None) == ext.I8C_ERR_INVALID_ARG
+    assert ext.lib.i8c_plan_run_prepacked(None, a, a, ctypes.c_float(1.0), None) == ext.I8C_ERR_INVALID_ARG
+    assert ext.lib.i8c_plan_run_prepacked_ex(None, a, a, ctypes.c_float(1.0), None, None) == ext.I8C_ERR_INVALID_ARG
+
+
 def test_autotune_argument_checks(ext):
     """The tuner rejects bad arguments on the host, before touching a device."""
     shape = ctypes.byref(ext.ConvShape.of((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1)))

@@ -482,3 +482,66 @@ def test_stacked_taps_rejects_unsuited_shapes():
         with pytest.raises(ext.I8ConvError) as ei:
             ext.Plan(shape, kernel_variant=6)
         assert ei.value.status == ext.I8C_ERR_UNSUPPORTED, shape
+
+
+@pytest.mark.parametrize("shape,kw", [
+    ((2, 64, 13, 11, 96, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=1)),
+    ((2, 64, 13, 11, 96, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2)),
+    ((2, 64, 13, 11, 128, 3, 3, 1, 1, 2, 2, 1, 1), dict(kernel_variant=3)),
+    ((2, 64, 13, 11, 128, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=4)),
+    ((2, 64, 13, 11, 256, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=5)),
+    ((2, 64, 12, 40, 64, 3, 5, 1, 2, 1, 1, 1, 1), dict(kernel_variant=6)),
+    ((2, 96, 13, 11, 128, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, fused_filter=1)),
+    ((2, 32, 24, 24, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=3, fused_filter=2)),
+    ((2, 32, 24, 24, 64, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=3, fused_filter=3)),
+], ids=["gather", "halo", "halo-pair-s2", "transposed", "transposed-pair", "stacked", "grid-barrier-filter",
+        "resident-in-kernel", "resident-tma"])
+def test_prepacked_filter_exact(shape, kw):
+    """Weight prepacking: set_filter converts the filter once, run_prepacked
+    runs the convolution alone; outputs bit-exact against the oracle on two
+    different activations, unchanged after the caller overwrites its filter
+    buffer, with the per-channel epilogue too; an ordinary run with another
+    filter withdraws the prepacked copy."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    N, C, H, W, K = shape[:5]
+    x1, f = _data(shape, 9100 + sum(shape))
+    x2, _ = _data(shape, 9200 + sum(shape))
+    orc = oracle.Oracle()
+    try:
+        plan = ext.Plan(shape, **kw)
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED:
+            pytest.skip("plan form not available for this shape")
+        raise
+    P, Q = plan.info["P"], plan.info["Q"]
+    xp1, fp = gpu_util.packed_inputs(x1, f)
+    xp2, _ = gpu_util.packed_inputs(x2, f)
+    fd = torch.from_numpy(fp).cuda()
+    xd1, xd2 = torch.from_numpy(xp1).cuda(), torch.from_numpy(xp2).cuda()
+    y = torch.full((N, K // 32, P, Q, 32), 55, dtype=torch.int8, device="cuda")
+    with pytest.raises(ext.I8ConvError):
+        plan.run_prepacked(xd1, y, 2.0 ** -10)   # no filter set yet
+    plan.set_filter(fd)
+    fd.zero_()                                    # the plan keeps its own copy
+    for xd, xn in ((xd1, x1), (xd2, x2)):
+        plan.run_prepacked(xd, y, 2.0 ** -10)
+        torch.cuda.synchronize()
+        y_ref, _ = gpu_util.oracle_packed(shape, xn, f, 2.0 ** -10)
+        assert np.array_equal(y.cpu().numpy(), y_ref)
+    rng = np.random.default_rng(11)
+    scale = rng.uniform(2.0 ** -12, 2.0 ** -8, K).astype(np.float32)
+    bias = rng.uniform(-40, 40, K).astype(np.float32)
+    plan.run_prepacked(xd2, y, 1.0, alpha_k=torch.from_numpy(scale).cuda(), bias=torch.from_numpy(bias).cuda(),
+                       relu=True)
+    torch.cuda.synchronize()
+    acc = orc.conv2d_fprop(x2, f, shape, 1.0)[1].astype(np.int64)
+    assert np.array_equal(y.cpu().numpy(), oracle.nchw_to_ncxhwx32(orc.requantize_channels(acc, 1.0, scale, bias,
+                                                                                            relu=True)))
+    plan.run(xd1, fd, y, 2.0 ** -10)              # an ordinary run with the (zeroed) filter
+    torch.cuda.synchronize()
+    assert not y.cpu().numpy().any()
+    with pytest.raises(ext.I8ConvError):
+        plan.run_prepacked(xd1, y, 2.0 ** -10)
+    assert plan.status() == 0
+    plan.destroy()
