@@ -365,8 +365,13 @@ i8c_status i8c_plan_run_acc(const i8c_plan* plan, const int8_t* x, const int8_t*
  * The copy is the plan's: f may change or be freed after set_filter's work
  * is done.  Any i8c_plan_run* call that takes a filter replaces the copy;
  * run_prepacked then returns I8C_ERR_INVALID_ARG until set_filter is called
- * again (also before the first set_filter).  Not thread-safe per plan, like
- * every other plan call. */
+ * again (also before the first set_filter).  The convolution kernels are
+ * dependent launches: a run's kernel starts on SMs as soon as the kernel
+ * ahead of it frees them and waits for that kernel only before reading
+ * memory it may have written (the activations; the filter copy right after
+ * set_filter), so successive prepacked runs load their filter stages while
+ * the previous run finishes.  Not thread-safe per plan, like every other
+ * plan call. */
 i8c_status i8c_plan_set_filter(const i8c_plan* plan, const int8_t* f, cudaStream_t stream);
 i8c_status i8c_plan_run_prepacked(const i8c_plan* plan, const int8_t* x, int8_t* y, float alpha,
                                   cudaStream_t stream);

@@ -91,6 +91,10 @@ struct HaloParams {
   // no filter TMA, so a run is one launch.
   int f_smem;
   const int8_t* f_src;
+  // 1: the filter operand (the fp16 copy, or f_src) was not written by the
+  // kernel launched just before this one (a prepacked run after the first),
+  // so it is read without waiting for that kernel
+  int filter_ready;
 };
 
 
@@ -618,7 +622,7 @@ __device__ __forceinline__ void resident_filter_to_smem(const HaloParams& hp, ui
   const int kk_end = p.CB * p.R * p.S;
   const int per_stage = G * BNH * 2;
   const int total = hp.nbs * per_stage;
-  ptx::griddep_wait();  // the filter may come from the kernel before this one
+  if (!hp.filter_ready) ptx::griddep_wait();  // the filter may come from the kernel before this one
   for (int b0 = 0; b0 < total; b0 += kBatch * kHaloThreads) {
     uint4 v[kBatch];
 #pragma unroll
@@ -683,6 +687,12 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nbs = hp.nbs;
   constexpr int BNH = BN / CG;  // filter rows (output channels) this CTA stages per K-slice
+  // A dependent launch after this one (the next run) may start as soon as
+  // SMs free up: every read of memory an earlier kernel may write (the
+  // activations, the filter or its converted copy) and every write of the
+  // fp16 copy waits for the earlier grid (griddep_wait); the outputs are
+  // written only after those reads.
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 #if defined(I8C_PIPELINE_TRACE)
   // per-CTA span (global timer) and SM, for the pipeline analysis build only
   if (p.trace != nullptr && threadIdx.x == 0 && blockIdx.x < kTraceSlots) {
@@ -1026,7 +1036,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       }
       ptx::fence_proxy_async_global();
       if (!fine && lane == 0) raise_timeout(p, abort_flag);
-    } else {
+    } else if (!hp.filter_ready) {
       // the fp16 filter is written by the conversion kernel launched just
       // before this one, which this kernel may overlap (dependent launch)
       ptx::griddep_wait();
@@ -1095,6 +1105,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // memory, which leaves room for longer filter stages).  Either way the
     // bytes are converted to fp16 and stored into the free halo stage.
     ptx::setmaxnreg_dec<kWorkerRegs>();
+    ptx::griddep_wait();  // the activations may come from the kernel before this one
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
     const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,
@@ -1111,6 +1122,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // accumulator that overlaps the MMAs of the next chunk.
     ptx::setmaxnreg_inc<kEpilogueRegs>();
     if (hp.f_int8 != nullptr) {
+      ptx::griddep_wait();  // the kernel before this one may still read the fp16 copy
       // this CTA's share of the int8 -> f16 filter copy (same layout), then
       // one arrival per CTA on the grid barrier; the generation it saw goes to
       // the TMA warp

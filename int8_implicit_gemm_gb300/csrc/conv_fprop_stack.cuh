@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
+  // the next run may launch as soon as SMs free up; every read of memory an
+  // earlier kernel may write waits for it (griddep_wait in the producers and
+  // the filter TMA warp), and the outputs are written only after those reads
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
   const int nbs = hp.nbs;
   constexpr int U = SLOTS;              // MMAs per filter row and 16-channel half
   const bool odd = (p.S & 1) != 0;      // the last slot is a single tap (N = 64)
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<kWorkerRegs>();
     // the fp16 filter is written by the conversion kernel launched just
     // before this one, which this kernel may overlap (dependent launch)
-    ptx::griddep_wait();
+    if (!hp.filter_ready) ptx::griddep_wait();
     const TileSched ts = tile_sched<CG>();
     const uint32_t stage_bytes = static_cast<uint32_t>(U * kStackSlotBytes);
     uint32_t g = 0, st = 0, bph = 0;
@@ -348,6 +352,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   } else if (warp < 8) {
     // ------------------------------------------------------------ halo producers
     ptx::setmaxnreg_dec<kWorkerRegs>();
+    ptx::griddep_wait();  // the activations may come from the kernel before this one
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     if (!stack_produce<kHaloSplitBatch + 2>(hp, tile_sched<CG>(), smem, h_full, h_empty, abort_flag, pt))
       raise_timeout(p, abort_flag);

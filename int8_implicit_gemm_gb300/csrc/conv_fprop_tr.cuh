@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
+  // the next run may launch as soon as SMs free up; every read of memory an
+  // earlier kernel may write waits for it (griddep_wait in the producers and
+  // the filter TMA warp), and the outputs are written only after those reads
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
   const int nbs = hp.nbs;
   const int NP = CG * hp.tile_px;  // the MMA's N: pixels per tile over the CTA group
   const int RS = p.R * p.S;
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<Regs::kWorker>();
     // the fp16 filter is written by the conversion kernel launched just
     // before this one, which this kernel may overlap (dependent launch)
-    ptx::griddep_wait();
+    if (!hp.filter_ready) ptx::griddep_wait();
     const TileSched ts = tile_sched<CG>();
     const uint32_t stage_bytes = static_cast<uint32_t>(G * kTrRows * 64);
     uint32_t g = 0, st = 0, bph = 0;
@@ -388,6 +392,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     // ring), converted to fp16 and stored as four 8-channel planes: the same
     // producers as the halo kernel's flat tiles, with tile_px pixels per tile.
     ptx::setmaxnreg_dec<Regs::kWorker>();
+    ptx::griddep_wait();  // the activations may come from the kernel before this one
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
     const TileSched ts = tile_sched<CG>();
     const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,

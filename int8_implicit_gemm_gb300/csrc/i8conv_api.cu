@@ -56,6 +56,9 @@ struct i8c_plan {
   // i8c_plan_set_filter was called: f16 holds the operand copy (or, for a
   // kernel that writes its resident filter itself, an int8 copy of f)
   mutable bool prepacked = false;
+  // set_filter's conversion (or copy) may be the kernel launched just before
+  // the next prepacked run, which must then wait for it before reading
+  mutable bool filter_fresh = false;
 };
 
 namespace {
@@ -531,6 +534,8 @@ i8c_status run_plan(const i8c_plan* pl, const int8_t* x, const int8_t* f, int8_t
       pl->tmap_x_ptr = x;
     }
     hp.f_src = f;  // read only when the kernel writes its resident filter itself
+    hp.filter_ready = prepacked && !pl->filter_fresh ? 1 : 0;
+    if (prepacked) pl->filter_fresh = false;
     if (pl->gbar != nullptr && !prepacked) {  // prepacked: the TMA reads the converted copy
       hp.f_int8 = f;
       hp.f16 = pl->f16;
@@ -1357,6 +1362,7 @@ i8c_status i8c_plan_set_filter(const i8c_plan* plan, const int8_t* f, cudaStream
           : convert_filter(plan, f, stream);
   if (e != cudaSuccess) return from_cuda(e);
   plan->prepacked = true;
+  plan->filter_fresh = true;
   return I8C_OK;
 }
 

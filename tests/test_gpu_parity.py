@@ -545,3 +545,45 @@ def test_prepacked_filter_exact(shape, kw):
         plan.run_prepacked(xd1, y, 2.0 ** -10)
     assert plan.status() == 0
     plan.destroy()
+
+
+@pytest.mark.parametrize("kw", [dict(kernel_variant=2), dict(kernel_variant=3), dict(kernel_variant=4),
+                                dict(kernel_variant=6), dict(kernel_variant=2, fused_filter=2)],
+                         ids=["halo", "halo-pair", "transposed", "stacked", "resident-in-kernel"])
+@pytest.mark.parametrize("prepacked", [False, True], ids=["runs", "prepacked"])
+def test_chained_runs_ping_pong(kw, prepacked):
+    """Each run reads the previous run's output and writes the buffer the run
+    before it read (two buffers, six runs back to back on one stream): the
+    dependent launches must order every activation read after the previous
+    kernel's writes and every output write after its reads.  Bit-exact
+    against the oracle applied six times."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 1, 1)
+    x, f = _data(shape, 4711)
+    try:
+        plan = ext.Plan(shape, **kw)
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED:
+            pytest.skip("plan form not available for this shape")
+        raise
+    xp, fp = gpu_util.packed_inputs(x, f)
+    fd = torch.from_numpy(fp).cuda()
+    bufs = [torch.from_numpy(xp).cuda(), torch.empty_like(torch.from_numpy(xp)).cuda()]
+    alpha = 2.0 ** -11  # keeps six generations spread out (mean |y| about 19, none saturated)
+    if prepacked:
+        plan.set_filter(fd)
+    for i in range(6):
+        src, dst = bufs[i % 2], bufs[(i + 1) % 2]
+        if prepacked:
+            plan.run_prepacked(src, dst, alpha)
+        else:
+            plan.run(src, fd, dst, alpha)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    orc = oracle.Oracle()
+    cur = x
+    for _ in range(6):
+        cur = orc.conv2d_fprop(cur, f, shape, alpha)[0]
+    assert np.array_equal(bufs[0].cpu().numpy(), oracle.nchw_to_ncxhwx32(cur))
+    plan.destroy()
