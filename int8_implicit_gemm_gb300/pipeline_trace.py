@@ -25,6 +25,9 @@ per run configuration:
     acquisitions of the MMA warp.
 
   python -m int8_implicit_gemm_gb300.pipeline_trace n32c128h112k256r3s2 '{"num_ctas": 19}'
+
+Plan options go in the JSON object; "prepacked": true traces prepacked runs
+(the filter converted once by set_filter, then run_prepacked).
 """
 from __future__ import annotations
 
@@ -48,9 +51,15 @@ def trace_workload(shape, alpha, runs: int = 6, **opts) -> dict:
     sets = [(torch.randint(-128, 128, (xb,), dtype=torch.int8, device="cuda", generator=g),
              torch.randint(-128, 128, (fb,), dtype=torch.int8, device="cuda", generator=g),
              torch.empty(yb, dtype=torch.int8, device="cuda")) for _ in range(nsets)]
+    prepacked = bool(opts.pop("prepacked", False))
     plan = ext.Plan(shape, debug_flags=2, **opts)
+    if prepacked:  # the filter converted once, then the convolution alone, back to back
+        plan.set_filter(sets[0][1])
     for i in range(runs):
-        plan.run(*sets[i % nsets], alpha)
+        if prepacked:
+            plan.run_prepacked(sets[i % nsets][0], sets[i % nsets][2], alpha)
+        else:
+            plan.run(*sets[i % nsets], alpha)
     torch.cuda.synchronize()
     if plan.status() != 0:
         raise RuntimeError("a bounded wait ran out during the traced runs")
@@ -101,6 +110,11 @@ def trace_workload(shape, alpha, runs: int = 6, **opts) -> dict:
             if m > 3:
                 # how much later the pair's rank 1 announces the same halo stage
                 out["cta1_arrive_lag_us"] = round(float(np.median(a1[1:m] - a0[1:m])) / 1e3, 3)
+                # and how much later it sees the same stage freed by the MMA's commit
+                f0, f1 = tr[16], tr[18]
+                mf = int(min(np.sum(f0 > 0), np.sum(f1 > 0)))
+                if mf > 3:
+                    out["cta1_free_lag_us"] = round(float(np.median(f1[1:mf] - f0[1:mf])) / 1e3, 3)
         acq = tr[20]
         n = int(np.sum(acq > 0))
         if n > 2:
