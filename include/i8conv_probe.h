@@ -84,7 +84,9 @@ i8c_status i8c_probe_mma_f8(int32_t n, int32_t num_ctas, int32_t iters, long lon
  * (this GPU's memory only), four chunks in flight, a buffer refilled once
  * both CTAs hold its previous chunk; step i of cluster c reads chunk
  * (c + i * num_ctas / 2) mod (region_bytes / chunk_bytes), and the bytes
- * counted per CTA are the bytes it received.
+ * counted per CTA are the bytes it received; mode 3: every thread copies
+ * its 16-byte pieces of each chunk with cp.async (global -> shared, no
+ * registers), one commit group per chunk, three groups in flight.
  *   cycles: DEVICE buffer of 3*num_ctas int64, per CTA: SM cycles of the
  *           loop, bytes moved, 1 if every bounded wait succeeded
  *   elapsed_ms as for i8c_probe_mma_f16.  Synchronises `stream`. */

@@ -185,6 +185,21 @@ __global__ void __launch_bounds__(kIngressThreads, 1)
       for (int i = first; i < issued; ++i)
         if (!ptx::mbar_wait(&bar[i % kIngressBufs], (i / kIngressBufs) & 1u, 2000000000ull, nullptr)) ok = false;
     }
+  } else if (mode == 3) {
+    // every thread copies its 16-byte pieces of each chunk with cp.async
+    // (global -> shared, no registers), one commit group per chunk, at most
+    // kIngressBufs - 1 groups in flight
+    const int vecs = chunk / 16;
+    const uint32_t base = ptx::smem_addr(smem);
+    for (int i = 0; i < iters; ++i) {
+      const int64_t c = (blockIdx.x + static_cast<int64_t>(i) * gridDim.x) % nchunks;
+      const uint8_t* s = src + c * chunk;
+      const uint32_t d = base + static_cast<uint32_t>((i % kIngressBufs) * chunk);
+      for (int v = threadIdx.x; v < vecs; v += kIngressThreads) ptx::cp_async_16_cg(d + v * 16, s + v * 16);
+      ptx::cp_async_commit();
+      ptx::cp_async_wait<kIngressBufs - 1>();
+    }
+    ptx::cp_async_wait_all();
   } else {
     const int vecs = chunk / 16;  // a multiple of kIngressThreads * kIngressVecs
     for (int i = 0; i < iters; ++i) {
@@ -310,7 +325,7 @@ extern "C" i8c_status i8c_probe_l2_ingress(const void* src, int64_t region_bytes
                                            int32_t num_ctas, int32_t iters, long long* cycles, float* elapsed_ms,
                                            cudaStream_t stream) {
   if (src == nullptr || cycles == nullptr || elapsed_ms == nullptr || num_ctas < 1 || iters < 1 ||
-      mode < 0 || mode > 2 || chunk_bytes < 16 || chunk_bytes > 49152 || chunk_bytes % 16 != 0 ||
+      mode < 0 || mode > 3 || chunk_bytes < 16 || chunk_bytes > 49152 || chunk_bytes % 16 != 0 ||
       (mode == 2 && (chunk_bytes % 32 != 0 || num_ctas % 2 != 0)) ||
       (mode == 1 && chunk_bytes % (16 * i8c::kIngressThreads * i8c::kIngressVecs) != 0) ||
       region_bytes < chunk_bytes || region_bytes % chunk_bytes != 0 || (reinterpret_cast<uintptr_t>(src) & 15u))
