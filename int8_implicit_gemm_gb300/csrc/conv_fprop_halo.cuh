@@ -339,11 +339,15 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
 
 // Producer that loads straight into registers, kBatch positions at a time
 // (zeros outside the image).  Returns false when a wait timed out.
+// kBatch loads per thread and batch: the batch the thread keeps in flight
+// while it waits for its halo stage is the whole halo when it fits (6 loads
+// for the 561 positions of a stride-2 16x8 patch, 8 for the 768 of the
+// dilated 5x9 layer); the smaller batch where 6 suffice keeps the loop short.
+template <int kBatch>
 __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                    uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                    int pt) {
   const ConvParams& p = hp.c;
-  constexpr int kBatch = 6;  // stride-2 halos: one load round trip per stage instead of two
   const int h = halo_lane_half(pt);
   const int positions = hp.positions;
   const HaloWalk w = halo_walk(hp, pt);
@@ -508,7 +512,8 @@ __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, con
                                                       int pt) {
   const int ng = halo_groups<kB>(hp);
   if (ng > 0) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt, ng);
-  return halo_produce_direct(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+  return hp.positions > 6 * kHaloStep ? halo_produce_direct<8>(hp, ts, smem, h_full, h_empty, abort_flag, pt)
+                                      : halo_produce_direct<6>(hp, ts, smem, h_full, h_empty, abort_flag, pt);
 }
 
 // Producer fed by TMA: thread 0 issues, nxs channel blocks ahead, one box
