@@ -587,3 +587,43 @@ def test_chained_runs_ping_pong(kw, prepacked):
         cur = orc.conv2d_fprop(cur, f, shape, alpha)[0]
     assert np.array_equal(bufs[0].cpu().numpy(), oracle.nchw_to_ncxhwx32(cur))
     plan.destroy()
+
+
+@pytest.mark.parametrize("kw", [dict(kernel_variant=4), dict(kernel_variant=3), dict(kernel_variant=6),
+                                dict(kernel_variant=3, fused_filter=2), dict(kernel_variant=2, fused_filter=1)],
+                         ids=["transposed", "halo-pair", "stacked", "resident-in-kernel", "grid-barrier-filter"])
+def test_prepacked_filter_switch_on_one_stream(kw):
+    """set_filter with a second filter right after prepacked runs with the
+    first, then a prepacked run at once on the same stream: the conversion (or
+    copy) of the new filter is the work just before that run's kernel, which
+    must wait for it before reading the filter; alternating three times, each
+    run bit-exact against the oracle with its own filter."""
+    import torch
+    import int8_implicit_gemm_gb300 as ext
+    shape = (2, 64, 12, 40, 64, 3, 5, 1, 2, 1, 1, 1, 1)
+    N, C, H, W, K = shape[:5]
+    x, f1 = _data(shape, 7100)
+    _, f2 = _data(shape, 7200)
+    try:
+        plan = ext.Plan(shape, **kw)
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED:
+            pytest.skip("plan form not available for this shape")
+        raise
+    P, Q = plan.info["P"], plan.info["Q"]
+    xp, fp1 = gpu_util.packed_inputs(x, f1)
+    _, fp2 = gpu_util.packed_inputs(x, f2)
+    xd = torch.from_numpy(xp).cuda()
+    fds = [torch.from_numpy(fp1).cuda(), torch.from_numpy(fp2).cuda()]
+    refs = [gpu_util.oracle_packed(shape, x, ff, 2.0 ** -10)[0] for ff in (f1, f2)]
+    ys = [torch.full((N, K // 32, P, Q, 32), 33, dtype=torch.int8, device="cuda") for _ in range(6)]
+    s = torch.cuda.current_stream()
+    for i in range(6):
+        plan.set_filter(fds[i % 2], s)
+        plan.run_prepacked(xd, ys[i], 2.0 ** -10, s)
+        plan.run_prepacked(xd, ys[i], 2.0 ** -10, s)   # a second run: no wait for the filter
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    for i in range(6):
+        assert np.array_equal(ys[i].cpu().numpy(), refs[i % 2]), i
+    plan.destroy()
