@@ -105,10 +105,16 @@ typedef struct {
                                 last wave is partial, 3 = halve them along the output channels
                                 (N = BN/2 MMAs, disjoint outputs) when the halves fit in the
                                 wave and the tile is 128 or 256 wide                         */
-  int32_t tile_shape;        /* halo kernel, the 128 output pixels of a tile: 0 = auto, 1 = a
-                                16x8 patch, 2 = 128 consecutive pixels of the output laid out
-                                with the zero-padded input's row width (stride 1 only; the
-                                pixels past Q in each row are computed and discarded)       */
+  int32_t tile_shape;        /* halo kernel, the output pixels of a tile: 0 = auto, 1 = a 16x8
+                                patch, 2 = 128 consecutive pixels of the output laid out with
+                                the zero-padded input's row width (stride 1 only; the pixels
+                                past Q in each row are computed and discarded), 3 = a 16x16
+                                patch: two 16x8 sub-tiles on one halo, two MMAs per tap and K
+                                half (block_n <= 64, whole filter rows per filter stage,
+                                register or staged halo loads, no split tail; else
+                                I8C_ERR_UNSUPPORTED).  Auto takes 16x16 patches where they
+                                keep the filter resident (one output-channel tile) and the
+                                planner's cost model prefers them                          */
   int32_t fused_filter;      /* where the int8 filter becomes the fp16 MMA operand:
                                 0 = auto (2 where the halo kernel keeps the whole filter
                                 resident in shared memory, else 3);
@@ -230,6 +236,8 @@ typedef struct {
   /* per-tap gather kernel (variant 1; 0 otherwise) */
   int32_t gather_stages, gather_off_a, gather_stage_a, gather_off_b, gather_stage_b;
   int32_t gather_off_staging, gather_staging_slots, gather_staging_bytes, gather_off_bar;
+  /* halo kernel, 2-D patches: 16x8 sub-tiles per patch (2 for 16x16 patches) */
+  int32_t subtiles;
 } i8c_layout;
 
 /* The layout i8c_plan_create would give `shape` with `opts` (may be NULL) on

@@ -75,7 +75,8 @@ class Layout(ctypes.Structure):
         "filter_stage_bytes", "off_out", "off_bar", "bar_bytes")] + [("phase_off", ctypes.c_int32 * 9)] + [
         (n, ctypes.c_int32) for n in ("tma_halo", "x8_slots", "off_x8", "x8_bytes", "box_w", "box_h",
             "gather_stages", "gather_off_a", "gather_stage_a", "gather_off_b", "gather_stage_b",
-            "gather_off_staging", "gather_staging_slots", "gather_staging_bytes", "gather_off_bar")]
+            "gather_off_staging", "gather_staging_slots", "gather_staging_bytes", "gather_off_bar",
+            "subtiles")]
 
     def asdict(self):
         d = {n: getattr(self, n) for n, _ in self._fields_}

@@ -95,6 +95,11 @@ struct HaloParams {
   // kernel launched just before this one (a prepacked run after the first),
   // so it is read without waiting for that kernel
   int filter_ready;
+  // 2-D patches of 16 x (8 * subtiles) output pixels: subtiles = 2 puts two
+  // 16x8 sub-tiles side by side on one halo (16x16 patches); every tap then
+  // issues two M = 128 MMAs per K half, the second on the halo 8 positions
+  // on, into an accumulator pair (BN columns each) per buffer.  0 or 1: one.
+  int subtiles;
 };
 
 
@@ -146,7 +151,7 @@ __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp
   const int qt = patch % hp.TQW;
   const int rest = patch / hp.TQW;
   const int pt = rest % hp.TPH;
-  return {rest / hp.TPH, pt * 16, qt * 8, nt, patch < hp.num_patches, 0};
+  return {rest / hp.TPH, pt * 16, qt * (hp.subtiles == 2 ? 16 : 8), nt, patch < hp.num_patches, 0};
 }
 
 // Arrive on a barrier of the MMA-issuing CTA, called by all 32 lanes of a
@@ -342,7 +347,8 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
 // kBatch loads per thread and batch: the batch the thread keeps in flight
 // while it waits for its halo stage is the whole halo when it fits (6 loads
 // for the 561 positions of a stride-2 16x8 patch, 8 for the 768 of the
-// dilated 5x9 layer); the smaller batch where 6 suffice keeps the loop short.
+// dilated 5x9 layer; 10 would not fit the producers' registers); the smaller
+// batch where 6 suffice keeps the loop short.
 template <int kBatch>
 __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                    uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
@@ -675,11 +681,14 @@ __device__ __forceinline__ void resident_filter_to_smem(const HaloParams& hp, ui
 }
 
 // CTAs produce their own halo and drain their own 128 accumulator rows.
-template <int BN, int GT, int CG>
+template <int BN, int GT, int CG, int SUB = 1>
 __global__ void __launch_bounds__(kHaloThreads, 1)
     conv_fprop_halo_kernel(const __grid_constant__ CUtensorMap tmap_f, const __grid_constant__ CUtensorMap tmap_x,
                            const HaloParams hp) {
   static_assert(CG == 1 || CG == 2, "CTA group");
+  // SUB = 2: 16x16 patches (hp.subtiles == 2), issued through the whole-row
+  // run block below, with two BN-column accumulators per buffer
+  static_assert(SUB == 1 || (SUB == 2 && GT > 0 && BN <= 64), "16x16 patches");
   static_assert(CG == 1 || BN >= 64, "a CTA pair splits B into halves of at least 32 rows");
   const ConvParams& p = hp.c;
   extern __shared__ uint8_t smem_raw[];
@@ -778,6 +787,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       const uint32_t lbo = hp.plane_bytes;
       const uint64_t a_desc0 = ptx::smem_desc_noswizzle_kmajor(0, lbo, sbo);
       const uint64_t b_desc0 = ptx::smem_desc_sw64_kmajor(0);
+      constexpr bool wide = SUB == 2;  // 16x16 patches
       // start-address fields (16-byte units)
       const uint32_t h_lo = ptx::smem_addr(smem) >> 4;
       const uint32_t b_lo = ptx::smem_addr(smem + hp.off_b) >> 4;
@@ -887,7 +897,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
             if (tracing) stall_acc += clock64() - ta;
             trace_mark(p, 0, 3, u);
 #endif
-            d_tmem = tmem_base + buf * BN + nh_cols;
+            d_tmem = tmem_base + buf * BN * static_cast<uint32_t>(SUB) + nh_cols;
             next_chunk = kk + p.chunk_slices;
             acc_flag = 0;
           }
@@ -930,6 +940,20 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
                 } else {
                   ptx::mma_f16_ss(d_tmem, adv0[t], bdv[t], idesc_u, t == 0 ? acc_flag : 1u);
                   ptx::mma_f16_ss(d_tmem, adv1[t], bdv[t] + 2, idesc_u, 1u);
+                }
+              }
+              if constexpr (wide) {
+                // the second 16x8 sub-tile: its 8-column groups start 8 halo
+                // positions on (128 bytes, 8 in the 16-byte address field)
+#pragma unroll
+                for (int t = 0; t < GT; ++t) {
+                  if constexpr (CG == 2) {
+                    ptx::mma_f16_ss_pair(d_tmem + BN, adv0[t] + 8, bdv[t], idesc, t == 0 ? acc_flag : 1u);
+                    ptx::mma_f16_ss_pair(d_tmem + BN, adv1[t] + 8, bdv[t] + 2, idesc, 1u);
+                  } else {
+                    ptx::mma_f16_ss(d_tmem + BN, adv0[t] + 8, bdv[t], idesc_u, t == 0 ? acc_flag : 1u);
+                    ptx::mma_f16_ss(d_tmem + BN, adv1[t] + 8, bdv[t] + 2, idesc_u, 1u);
+                  }
                 }
               }
               if (!resident) commit_all(&b_empty[st]);
@@ -1185,7 +1209,10 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     constexpr int kColsPerWarp = BN >= 64 ? BN / 2 : BN;
     const int col0 = BN >= 64 ? eh * kColsPerWarp : 0;
     const bool col_owner = BN >= 64 || eh == 0;
-    uint32_t run[kColsPerWarp];  // running int32 sums of this thread's pixel over its columns
+    // 16x16 patches: this thread's pixel in each 16x8 sub-tile
+    constexpr int kSub = SUB;
+    constexpr int sub = SUB;
+    uint32_t run[kSub * kColsPerWarp];  // running int32 sums of this thread's pixel(s) over its columns
     uint32_t u = 0, esync = hp.f_int8 != nullptr ? 1u : 0u;  // epi_sync phases used so far
     bool ok = true;
     const int RS = p.R * p.S;
@@ -1215,18 +1242,23 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t t_acc = tmem_base + lane_addr + buf * BN + col0;
+        const uint32_t t_acc = tmem_base + lane_addr + buf * BN * static_cast<uint32_t>(sub) + col0;
         const bool first = c == 0;
         if (mine) {
 #pragma unroll
-          for (int g = 0; g < kColsPerWarp / 32; ++g) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(t_acc + g * 32, v);
-            ptx::tmem_wait_ld();
+          for (int sb = 0; sb < kSub; ++sb) {
+            if (sb >= sub) break;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const uint32_t a = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
-              run[g * 32 + i] = first ? a : run[g * 32 + i] + a;
+            for (int g = 0; g < kColsPerWarp / 32; ++g) {
+              uint32_t v[32];
+              ptx::tmem_ld_32x32b_x32(t_acc + sb * BN + g * 32, v);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const uint32_t a = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+                const int j = sb * kColsPerWarp + g * 32 + i;
+                run[j] = first ? a : run[j] + a;
+              }
             }
           }
         }
@@ -1290,16 +1322,21 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
         if (!mine) continue;
         const PatchTile t = decode_patch(wu.tile, hp, tile_sched<CG>());
         const int pp = hp.flat ? (t.m0 + row) / hp.CW : t.p0 + (row >> 3);
-        const int qq = hp.flat ? (t.m0 + row) - pp * hp.CW : t.q0 + (row & 7);
-        if (t.valid && pp < p.P && qq < p.Q) {
+        const int qq0 = hp.flat ? (t.m0 + row) - pp * hp.CW : t.q0 + (row & 7);
+#pragma unroll
+        for (int sb = 0; sb < kSub; ++sb) {
+          if (sb >= sub) break;
+          const int qq = qq0 + 8 * sb;  // the sub-tile's column (2-D patches only)
+          if (!(t.valid && pp < p.P && qq < p.Q)) continue;
 #pragma unroll
           for (int g = 0; g < kColsPerWarp / 32; ++g) {
             const int k0 = t.nt * BN + col0 + g * 32;
+            const int j0 = sb * kColsPerWarp + g * 32;
             if (k0 < p.K) {
               const int64_t off = ((static_cast<int64_t>(t.n) * p.KB + (k0 >> 5)) * p.P + pp) * p.Q + qq;
               if (p.out_mode == 0) {
                 uint32_t o[8];
-                requant32(p, k0, [&](int i) { return static_cast<int>(run[g * 32 + i]); }, o);
+                requant32(p, k0, [&](int i) { return static_cast<int>(run[j0 + i]); }, o);
                 uint4* dst = reinterpret_cast<uint4*>(p.y + off * 32);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -1307,8 +1344,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
                 uint4* dst = reinterpret_cast<uint4*>(p.acc + off * 32);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                  dst[i] = make_uint4(run[g * 32 + 4 * i], run[g * 32 + 4 * i + 1], run[g * 32 + 4 * i + 2],
-                                      run[g * 32 + 4 * i + 3]);
+                  dst[i] = make_uint4(run[j0 + 4 * i], run[j0 + 4 * i + 1], run[j0 + 4 * i + 2], run[j0 + 4 * i + 3]);
               }
             }
           }

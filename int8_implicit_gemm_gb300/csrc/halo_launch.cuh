@@ -13,8 +13,16 @@ using HaloKernel = void (*)(const CUtensorMap, const CUtensorMap, const HaloPara
 // of whole filter rows (S divides the run length): 3 (a row of a 3x3
 // filter) and 9 (a whole 3x3 channel block, or a row of a 9-wide filter);
 // every other run takes the generic instantiation (GT = 0).
+// 16x16 patches (subtiles 2; whole-row runs and BN <= 64 only) have
+// instantiations of their own, so that the 16x8 kernels compile as before.
 template <int BN, int CG>
-HaloKernel halo_kernel_for(int bgroup, int S) {
+HaloKernel halo_kernel_for(int bgroup, int S, int subtiles = 1) {
+  if constexpr (BN <= 64) {
+    if (subtiles == 2) {
+      if (bgroup == 3 && 3 % S == 0) return conv_fprop_halo_kernel<BN, 3, CG, 2>;
+      if (bgroup == 9 && 9 % S == 0) return conv_fprop_halo_kernel<BN, 9, CG, 2>;
+    }
+  }
   if (bgroup == 3 && 3 % S == 0) return conv_fprop_halo_kernel<BN, 3, CG>;
   if (bgroup == 9 && 9 % S == 0) return conv_fprop_halo_kernel<BN, 9, CG>;
   return conv_fprop_halo_kernel<BN, 0, CG>;
@@ -22,11 +30,12 @@ HaloKernel halo_kernel_for(int bgroup, int S) {
 
 template <int BN, int CG>
 cudaError_t halo_prepare_bn() {
-  for (int g : {3, 9, 0}) {
-    const cudaError_t e = cudaFuncSetAttribute(halo_kernel_for<BN, CG>(g, 1),
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
-    if (e != cudaSuccess) return e;
-  }
+  for (int sub : {1, 2})
+    for (int g : {3, 9, 0}) {
+      const cudaError_t e = cudaFuncSetAttribute(halo_kernel_for<BN, CG>(g, 1, sub),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+      if (e != cudaSuccess) return e;
+    }
   return cudaSuccess;
 }
 
@@ -70,7 +79,8 @@ cudaError_t halo_launch_bn(const CUtensorMap& tmap, const CUtensorMap& tmap_x, c
                            int num_ctas, cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = halo_launch_config<CG>(smem, num_ctas, stream, attr, p.f_int8 != nullptr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S), tmap, tmap_x, p);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, halo_kernel_for<BN, CG>(p.bgroup, p.c.S, p.subtiles), tmap, tmap_x, p);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

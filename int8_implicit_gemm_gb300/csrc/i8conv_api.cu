@@ -159,11 +159,17 @@ bool tma_halo_box(const i8c_conv_shape& s, const i8c::HaloParams& h, i8c::HaloPa
 // loads: 0 = auto, 1 = staging ring only, 2 = register loads only.  Returns
 // false when the halo does not fit with at least three filter stages.
 bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int loads, bool flat, i8c::HaloParams* h,
-                 int* smem_bytes) {
+                 int* smem_bytes, bool wide = false) {
   if (s.stride_w > 8) return false;
   if (flat && (s.stride_h != 1 || s.stride_w != 1)) return false;
+  // 16x16 patches (two 16x8 sub-tiles on one halo): 2-D patches, at most 64
+  // channels per tile, register or staged halo loads, whole filter rows per
+  // filter stage (checked by the caller)
+  if (wide && (flat || bn > 64 || loads == 3)) return false;
   *h = i8c::HaloParams{};
   h->flat = flat ? 1 : 0;
+  h->subtiles = wide ? 2 : 1;
+  const int pw_out = wide ? 16 : 8;  // output columns per patch
   int64_t HR, CW, npos, patches;
   if (flat) {
     // flat tiles: 128 consecutive pixels of the output laid out with the
@@ -178,10 +184,10 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
     patches = static_cast<int64_t>(s.N) * tpi;
   } else {
     h->TPH = (P + 15) / 16;
-    h->TQW = (Q + 7) / 8;
+    h->TQW = (Q + pw_out - 1) / pw_out;
     patches = static_cast<int64_t>(s.N) * h->TPH * h->TQW;
     HR = 15LL * s.stride_h + static_cast<int64_t>(s.R - 1) * s.dil_h + 1;
-    CW = 7LL * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
+    CW = static_cast<int64_t>(pw_out - 1) * s.stride_w + static_cast<int64_t>(s.S - 1) * s.dil_w + 1;
     npos = HR * CW;
   }
   if (patches > kMaxI32) return false;
@@ -616,7 +622,7 @@ bool options_valid(const i8c_options& o) {
   return !(o.num_ctas < 0 || o.max_chunk_slices < 0 || o.max_chunk_slices > 32 || o.wait_timeout_us < 0 ||
            o.timing_events < 0 || o.timing_events > 65536 || o.host_staging < 0 || o.host_staging > 2 ||
            o.kernel_variant < 0 || o.kernel_variant > 6 || o.halo_loads < 0 || o.halo_loads > 3 ||
-           o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 2 || o.fused_filter < 0 ||
+           o.tail_split < 0 || o.tail_split > 3 || o.tile_shape < 0 || o.tile_shape > 3 || o.fused_filter < 0 ||
            o.fused_filter > 3 || o.filter_run < 0 || o.filter_run > 32 ||
            (o.tile_px != 0 && (o.tile_px < 16 || o.tile_px > 256 || o.tile_px % 16 != 0)));
 }
@@ -748,14 +754,17 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     // tile shapes: 16x8 patches, and flat tiles for stride 1 unless forced
     struct Choice {
       int bn, groups;
-      bool flat;
+      bool flat, wide;
     };
     auto search = [&](int cg, int only_bn) -> Choice {
-      Choice bestc{0, 0, false};
+      Choice bestc{0, 0, false, false};
       double best = -1.0;
-      for (int geo = 0; geo < 2; ++geo)
+      for (int geo = 0; geo < 3; ++geo)
       for (int cand : {256, 128, 64, 32}) {
-        const bool flat = geo == 1;
+        const bool flat = geo == 1, wide = geo == 2;
+        // tile_shape 3: 16x16 patches only; auto considers them too (below)
+        if (o.tile_shape == 3 && !wide) continue;
+        if (wide && o.tile_shape != 3 && o.tile_shape != 0) continue;
         if ((flat && o.tile_shape == 1) || (!flat && o.tile_shape == 2)) continue;
         if (o.block_n != 0 && cand != o.block_n) continue;
         if (only_bn != 0 && cand != only_bn) continue;
@@ -763,7 +772,14 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
         if (o.block_n == 0 && cand > 32 * cg && cand / 2 >= s.K) continue;  // half the tile would be empty
         i8c::HaloParams h;
         int sm = 0;
-        if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, flat, &h, &sm)) continue;
+        if (!halo_layout(s, p->P, p->Q, cand, cg, o.halo_loads, flat, &h, &sm, wide)) continue;
+        // 16x16 patches issue through the whole-row run path only; auto takes
+        // them only where the filter stays resident beside their larger halo
+        // (one output-channel tile, every filter stage in the ring)
+        if (wide && !((h.bgroup == 3 || h.bgroup == 9) && h.bgroup % s.S == 0)) continue;
+        if (wide && o.tile_shape == 0 &&
+            !((s.K + cand - 1) / cand == 1 && (s.C / 32) * s.R * s.S / h.bgroup <= h.nbs))
+          continue;
         int g = ctas / cg;
         if (cg == 2) {
           // pairs that fit on the GPU at once (clusters need both SMs free)
@@ -780,15 +796,19 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
         double width_eff = cand == 256 ? 1.0 : cand == 128 ? 0.62 : cand == 64 ? 0.45 : 0.3;
         // runs of one K-slice (no room for longer filter stages) issue poorly
         if (h.bgroup == 1 && s.S > 1) width_eff *= 0.6;
+        // 16x16 patches: twice the MMAs per tile boundary and per run, and a
+        // third fewer halo loads per pixel (measured on the dilated 5x9 layer
+        // on CTA pairs: 259.8 against 291 us)
+        if (wide) width_eff *= 1.12;
         // share of a tile's 128 rows that are real output pixels
         const double m_util =
             static_cast<double>(p->P) * p->Q /
-            (flat ? 128.0 * h.tpi : 128.0 * h.TPH * h.TQW);
+            (flat ? 128.0 * h.tpi : 128.0 * h.subtiles * h.TPH * h.TQW);
         const double score = wave_efficiency(t, g) * m_util * width_eff * static_cast<double>(s.K) /
                              (static_cast<double>(nt) * cand);
         if (score > best * 1.02) {
           best = score;
-          bestc = {cand, g, flat};
+          bestc = {cand, g, flat, wide};
         }
       }
       return bestc;
@@ -868,7 +888,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
       groups = best.groups;
       p->kernel_variant = cg == 2 ? 3 : 2;
       p->cta_group = cg;
-      halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, best.flat, &p->halo, &halo_smem);
+      halo_layout(s, p->P, p->Q, bn, cg, o.halo_loads, best.flat, &p->halo, &halo_smem, best.wide);
     } else if (o.kernel_variant >= 2) {
       return I8C_ERR_UNSUPPORTED;
     }
@@ -913,7 +933,7 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     // a half unit takes nearly a whole tile's time: measured no faster on the
     // 8x256x56x56 layer, hence only on request.
     if (rem > 0 && p->cta_group == 1 && bn >= 128 && 2 * rem <= g && o.tail_split == 3) nsplit = 2;
-    if (nsplit == 1 && rem > 0 && o.tail_split != 1 && o.tail_split != 3) {
+    if (nsplit == 1 && rem > 0 && o.tail_split != 1 && o.tail_split != 3 && p->halo.subtiles != 2) {
       ksplit = g / rem;
       if (ksplit > s.C / 32) ksplit = s.C / 32;
       if (ksplit < 2) ksplit = 1;
@@ -981,7 +1001,8 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
     // halo kernel: two fp32 chunk accumulators; running sums live in registers
     p->acc_buffers = 2;
     p->tmem_cols = static_cast<uint32_t>(
-        next_pow2(2 * (p->kernel_variant >= 4 ? p->cta_group * p->halo.tile_px : bn)));
+        next_pow2(2 * (p->kernel_variant >= 4 ? p->cta_group * p->halo.tile_px
+                                              : bn * (p->halo.subtiles == 2 ? 2 : 1))));
   } else {
     const int run_cols = p->num_chunks > 1 ? bn : 0;
     p->acc_buffers = (2 * bn + run_cols <= 512) ? 2 : 1;
@@ -1211,6 +1232,7 @@ void fill_layout(const i8c_plan* pl, i8c_layout* L) {
     L->box_h = h.box_h;
     L->bar_bytes = i8c::kHaloBarBytes;
     for (int f = 0; f < 9; ++f) L->phase_off[f] = h.phase_off[f];
+    L->subtiles = h.subtiles == 2 ? 2 : 1;
   } else {
     auto gather = [&](auto cfg) {
       using Cfg = decltype(cfg);

@@ -109,7 +109,7 @@ def test_autotune_argument_checks(ext):
 
 @pytest.mark.parametrize("opts", [
     dict(block_n=48), dict(block_n=512), dict(num_ctas=-1), dict(max_chunk_slices=33), dict(wait_timeout_us=-5),
-    dict(timing_events=70000), dict(kernel_variant=7), dict(halo_loads=4), dict(tail_split=4), dict(tile_shape=3),
+    dict(timing_events=70000), dict(kernel_variant=7), dict(halo_loads=4), dict(tail_split=4), dict(tile_shape=4),
     dict(fused_filter=4), dict(tile_px=20), dict(tile_px=272), dict(tile_px=8), dict(filter_run=33),
 ], ids=lambda o: ",".join(f"{k}={v}" for k, v in o.items()))
 def test_plan_options_rejected_on_the_host(ext, opts):

@@ -387,8 +387,9 @@ def test_channel_epilogue_full_size_bench_workload():
     ((1, 32, 16, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(num_ctas=1)),
     ((2, 64, 20, 20, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(kernel_variant=2, block_n=64, num_ctas=2)),
     ((2, 32, 24, 24, 32, 5, 9, 2, 4, 1, 1, 2, 3), dict(kernel_variant=3, block_n=64, num_ctas=2)),
+    ((2, 64, 24, 40, 32, 3, 3, 1, 1, 1, 1, 1, 1), dict(tile_shape=3, num_ctas=2)),
 ], ids=["dilated-pair", "dilated-single", "3x3-two-blocks", "stride2-three-blocks", "16x16",
-        "rows-past-K", "pair-rows-past-K"])
+        "rows-past-K", "pair-rows-past-K", "wide-patches"])
 @pytest.mark.parametrize("fused", [3, 2, 0], ids=["tma", "in-kernel", "auto"])
 def test_resident_filter_exact(shape, opts, fused):
     """One output-channel tile and whole-tile units: the filter stages are
@@ -400,6 +401,7 @@ def test_resident_filter_exact(shape, opts, fused):
     bit-exact against the oracle."""
     import int8_implicit_gemm_gb300 as ext
     opts = dict(opts, fused_filter=fused)
+    opts.setdefault("tile_shape", 1)  # 16x8 tiles unless the case asks for 16x16 patches: many units per CTA
     try:
         plan = ext.Plan(shape, **opts)
     except ext.I8ConvError as e:
@@ -627,3 +629,35 @@ def test_prepacked_filter_switch_on_one_stream(kw):
     for i in range(6):
         assert np.array_equal(ys[i].cpu().numpy(), refs[i % 2]), i
     plan.destroy()
+
+
+WIDE_SHAPES = [
+    (2, 32, 24, 40, 64, 5, 9, 2, 4, 1, 1, 2, 3),    # the dilated 5x9 layer's geometry, small
+    (2, 64, 20, 37, 64, 3, 3, 1, 1, 1, 1, 1, 1),    # ragged last patch column
+    (1, 32, 33, 45, 32, 3, 3, 1, 1, 2, 2, 1, 1),    # stride 2
+]
+
+
+@pytest.mark.parametrize("shape", WIDE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("kw", [dict(tile_shape=3), dict(tile_shape=3, kernel_variant=3),
+                                dict(tile_shape=3, kernel_variant=3, num_ctas=4),
+                                dict(tile_shape=3, kernel_variant=3, halo_loads=1)],
+                         ids=["auto", "pair", "pair-4-ctas", "pair-staged"])
+def test_wide_patches_exact(shape, kw):
+    """16x16 patches (two 16x8 sub-tiles on one halo, two MMAs per tap and K
+    half into an accumulator pair): every int32 accumulator and int8 output
+    bit-exact against the oracle, ragged patch columns included."""
+    import int8_implicit_gemm_gb300 as ext
+    try:
+        plan = ext.Plan(shape, **kw)
+    except ext.I8ConvError as e:
+        if e.status == ext.I8C_ERR_UNSUPPORTED:
+            pytest.skip("16x16 patches not available for this plan form")
+        raise
+    assert plan.layout()["subtiles"] == 2
+    plan.destroy()
+    x, f = _data(shape, 9900 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **kw)
+    assert np.array_equal(acc, acc_ref.astype(np.int32))
+    assert np.array_equal(y, y_ref)

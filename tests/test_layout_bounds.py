@@ -94,17 +94,21 @@ def check_layout(shape, L):
         reach = max(r * dh * CW + s * dw for r, s in _taps(shape)) + npx - 1
         assert pos >= npx + (R - 1) * dh * CW + (S - 1) * dw
     else:
-        # 16 x 8 patches: 8-row groups sh halo rows apart, 8 consecutive
-        # positions of the tap's column phase within a row
-        assert L["halo_rows"] >= 15 * sh + (R - 1) * dh + 1 and CW >= 7 * sw + (S - 1) * dw + 1
+        # 16 x 8 patches (16 x 16 with two sub-tiles side by side): 8-row
+        # groups sh halo rows apart, 8 consecutive positions of the tap's
+        # column phase within a row, the second sub-tile 8 positions on
+        sub = L["subtiles"]
+        assert sub in (1, 2)
+        last_col = 8 * sub - 1
+        assert L["halo_rows"] >= 15 * sh + (R - 1) * dh + 1 and CW >= last_col * sw + (S - 1) * dw + 1
         assert pos == L["halo_rows"] * CW
         ph_off = L["phase_off"]
         assert ph_off[0] == 0 and ph_off[sw] == CW
         reach = 0
         for r, s in _taps(shape):
             f, idx = (s * dw) % sw, (s * dw) // sw
-            assert idx + 7 < ph_off[f + 1] - ph_off[f], "a tap's 8 columns run past its column phase"
-            reach = max(reach, r * dh * CW + ph_off[f] + idx + 15 * sh * CW + 7)
+            assert idx + last_col < ph_off[f + 1] - ph_off[f], "a tap's columns run past its column phase"
+            reach = max(reach, r * dh * CW + ph_off[f] + idx + 15 * sh * CW + last_col)
     assert reach < pos, f"an operand view reaches halo position {reach} of {pos}"
     # both MMAs of a K-slice: planes 0-1 and 2-3 (start + 2 planes, + LBO = 1 plane)
     assert 3 * plane + 16 * reach + 15 < L["halo_bytes"], "a descriptor reaches past its halo stage"
@@ -117,7 +121,7 @@ def check_layout(shape, L):
         assert 2 * np_mma <= tc, "two accumulator buffers of N columns"
         assert L["off_out"] + 8 * np_mma * 16 <= L["off_bar"]
     else:
-        assert 2 * L["block_n"] <= tc, "two accumulator buffers of BN columns"
+        assert 2 * L["subtiles"] * L["block_n"] <= tc, "two accumulator buffers of BN columns per sub-tile"
         assert L["tile_px"] in (0, 128)
     assert end <= L["off_bar"], "operands overlap the barriers"
     if L["tma_halo"]:
@@ -198,6 +202,8 @@ PLAN_FORMS = [
     dict(kernel_variant=5, halo_loads=3), dict(kernel_variant=5, tile_px=128, halo_loads=3),
     dict(fused_filter=2), dict(kernel_variant=2, fused_filter=2), dict(kernel_variant=3, fused_filter=2),
     dict(kernel_variant=3, halo_loads=3, fused_filter=2), dict(fused_filter=3), dict(kernel_variant=3, fused_filter=3),
+    dict(tile_shape=3), dict(tile_shape=3, kernel_variant=3), dict(tile_shape=3, kernel_variant=2, block_n=64),
+    dict(tile_shape=3, kernel_variant=3, halo_loads=1),
 ]
 
 SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + STACKED_SHAPES + [
