@@ -110,7 +110,7 @@ typedef struct {
                                 the zero-padded input's row width (stride 1 only; the pixels
                                 past Q in each row are computed and discarded), 3 = a 16x16
                                 patch: two 16x8 sub-tiles on one halo, two MMAs per tap and K
-                                half (block_n <= 64, whole filter rows per filter stage,
+                                half (block_n <= 128, whole filter rows per filter stage,
                                 register or staged halo loads, no split tail; else
                                 I8C_ERR_UNSUPPORTED).  Auto takes 16x16 patches where they
                                 keep the filter resident (one output-channel tile) and the

@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   static_assert(CG == 1 || CG == 2, "CTA group");
   // SUB = 2: 16x16 patches (hp.subtiles == 2), issued through the whole-row
   // run block below, with two BN-column accumulators per buffer
-  static_assert(SUB == 1 || (SUB == 2 && GT > 0 && BN <= 64), "16x16 patches");
+  static_assert(SUB == 1 || (SUB == 2 && GT > 0 && BN <= 128), "16x16 patches");
   static_assert(CG == 1 || BN >= 64, "a CTA pair splits B into halves of at least 32 rows");
   const ConvParams& p = hp.c;
   extern __shared__ uint8_t smem_raw[];

@@ -13,11 +13,11 @@ using HaloKernel = void (*)(const CUtensorMap, const CUtensorMap, const HaloPara
 // of whole filter rows (S divides the run length): 3 (a row of a 3x3
 // filter) and 9 (a whole 3x3 channel block, or a row of a 9-wide filter);
 // every other run takes the generic instantiation (GT = 0).
-// 16x16 patches (subtiles 2; whole-row runs and BN <= 64 only) have
+// 16x16 patches (subtiles 2; whole-row runs and BN <= 128 only) have
 // instantiations of their own, so that the 16x8 kernels compile as before.
 template <int BN, int CG>
 HaloKernel halo_kernel_for(int bgroup, int S, int subtiles = 1) {
-  if constexpr (BN <= 64) {
+  if constexpr (BN <= 128) {
     if (subtiles == 2) {
       if (bgroup == 3 && 3 % S == 0) return conv_fprop_halo_kernel<BN, 3, CG, 2>;
       if (bgroup == 9 && 9 % S == 0) return conv_fprop_halo_kernel<BN, 9, CG, 2>;

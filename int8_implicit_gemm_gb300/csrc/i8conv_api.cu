@@ -162,10 +162,10 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
                  int* smem_bytes, bool wide = false) {
   if (s.stride_w > 8) return false;
   if (flat && (s.stride_h != 1 || s.stride_w != 1)) return false;
-  // 16x16 patches (two 16x8 sub-tiles on one halo): 2-D patches, at most 64
+  // 16x16 patches (two 16x8 sub-tiles on one halo): 2-D patches, at most 128
   // channels per tile, register or staged halo loads, whole filter rows per
   // filter stage (checked by the caller)
-  if (wide && (flat || bn > 64 || loads == 3)) return false;
+  if (wide && (flat || bn > 128 || loads == 3)) return false;
   *h = i8c::HaloParams{};
   h->flat = flat ? 1 : 0;
   h->subtiles = wide ? 2 : 1;
@@ -780,6 +780,10 @@ i8c_status plan_geometry(const i8c_conv_shape& s, const i8c_options& o, int64_t 
         if (wide && o.tile_shape == 0 &&
             !((s.K + cand - 1) / cand == 1 && (s.C / 32) * s.R * s.S / h.bgroup <= h.nbs))
           continue;
+        // 128-wide 16x16 patches only when asked for: their larger halos pace
+        // the producers (stride-2 112x112 layer: 115 against 63 us; 8x256x56x56
+        // layer: 36 against 26 us)
+        if (wide && o.tile_shape == 0 && cand > 64) continue;
         int g = ctas / cg;
         if (cg == 2) {
           // pairs that fit on the GPU at once (clusters need both SMs free)

@@ -635,14 +635,18 @@ WIDE_SHAPES = [
     (2, 32, 24, 40, 64, 5, 9, 2, 4, 1, 1, 2, 3),    # the dilated 5x9 layer's geometry, small
     (2, 64, 20, 37, 64, 3, 3, 1, 1, 1, 1, 1, 1),    # ragged last patch column
     (1, 32, 33, 45, 32, 3, 3, 1, 1, 2, 2, 1, 1),    # stride 2
+    (2, 96, 35, 37, 256, 3, 3, 1, 1, 2, 2, 1, 1),   # stride 2, three channel blocks, two 128-wide channel tiles
+    (1, 64, 21, 30, 160, 3, 3, 1, 1, 1, 1, 1, 1),   # K = 160: a ragged 128-wide channel tile
 ]
 
 
 @pytest.mark.parametrize("shape", WIDE_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("kw", [dict(tile_shape=3), dict(tile_shape=3, kernel_variant=3),
                                 dict(tile_shape=3, kernel_variant=3, num_ctas=4),
-                                dict(tile_shape=3, kernel_variant=3, halo_loads=1)],
-                         ids=["auto", "pair", "pair-4-ctas", "pair-staged"])
+                                dict(tile_shape=3, kernel_variant=3, halo_loads=1),
+                                dict(tile_shape=3, kernel_variant=2, block_n=128),
+                                dict(tile_shape=3, kernel_variant=3, block_n=128, num_ctas=6)],
+                         ids=["auto", "pair", "pair-4-ctas", "pair-staged", "single-128", "pair-128"])
 def test_wide_patches_exact(shape, kw):
     """16x16 patches (two 16x8 sub-tiles on one halo, two MMAs per tap and K
     half into an accumulator pair): every int32 accumulator and int8 output

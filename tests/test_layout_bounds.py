@@ -203,7 +203,8 @@ PLAN_FORMS = [
     dict(fused_filter=2), dict(kernel_variant=2, fused_filter=2), dict(kernel_variant=3, fused_filter=2),
     dict(kernel_variant=3, halo_loads=3, fused_filter=2), dict(fused_filter=3), dict(kernel_variant=3, fused_filter=3),
     dict(tile_shape=3), dict(tile_shape=3, kernel_variant=3), dict(tile_shape=3, kernel_variant=2, block_n=64),
-    dict(tile_shape=3, kernel_variant=3, halo_loads=1),
+    dict(tile_shape=3, kernel_variant=3, halo_loads=1), dict(tile_shape=3, kernel_variant=2, block_n=128),
+    dict(tile_shape=3, kernel_variant=3, block_n=128),
 ]
 
 SHAPES = [wl.shape_tuple() for wl in synth.WORKLOADS] + SMALL + TRANSPOSED_EXTRA + STACKED_SHAPES + [
