@@ -128,9 +128,11 @@ struct PatchTile {
 
 // Tile schedule of one CTA: tiles first, first + step, ...; a tile is
 // (group of cg patches, N-tile) and this CTA computes patch `rank` of the
-// group (cg = 2 for CTA pairs, whose two CTAs walk the same tiles).
+// group (cg = 2 for CTA pairs, whose two CTAs walk the same tiles).  fwd:
+// a pair's rank 1 arrives on its own halo barriers, whose completions one
+// lane forwards to rank 0 (the halo kernel's producers).
 struct TileSched {
-  int first, step, rank, cg;
+  int first, step, rank, cg, fwd;
 };
 
 // Derived from the block index alone, so the compiler can recompute it
@@ -163,7 +165,7 @@ __device__ __forceinline__ PatchTile decode_patch(int tile, const HaloParams& hp
 // arrive per warp as well, after the same warp barrier, measured slower:
 // 326.7 against 314.6 us on the 64-channel 5x9 layer.)
 __device__ __forceinline__ void arrive_on_leader(uint64_t* bar, const TileSched& ts, bool mine = true) {
-  if (ts.rank == 0) {
+  if (ts.rank == 0 || ts.fwd) {
     if (mine) ptx::mbar_arrive(bar);
   } else {
     __syncwarp();  // orders every lane's prior shared-memory writes before lane 0's release
@@ -208,6 +210,17 @@ __device__ __forceinline__ void halo_walk_origin(const HaloParams& hp, int m0, i
     pos -= hp.CW;
     ++b;
   }
+}
+
+// Index in its row of the halo position that holds input column c (relative
+// to the halo's first column): positions are ordered by column phase (column
+// mod stride_w), phase f from phase_off[f].  The inverse of halo_column.
+__device__ __forceinline__ int halo_phase_index(const HaloParams& hp, int c) {
+  const int sw = hp.c.stride_w;
+  if (sw == 1) return c;
+  if (sw == 2) return (c >> 1) + ((c & 1) ? hp.phase_off[1] : 0);
+  const int f = c % sw;
+  return hp.phase_off[f] + c / sw;
 }
 
 // Input column (relative to the halo's first column) of halo position pos in
@@ -373,14 +386,22 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     int e = w.e_first, b = w.b_first, pos = w.pos_first;
     halo_walk_origin(hp, t.m0, b, pos);
     bool stage_free = false;
+#if defined(I8C_PIPELINE_TRACE)
+    if (ptrace && tseq < kTraceSlots)
+      p.trace[(30 + blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
+#endif
     do {
+      // The walk visits the halo's input pixels in natural order (pos: the
+      // input column within the halo, e: row * CW + pos), so that a warp's
+      // loads are contiguous and no column needs a phase lookup; each pixel
+      // is stored at its column-phase position in the row.
       uint4 v[kBatch];
-      const int e0 = e;  // position of v[k]: e0 + k * kHaloStep
+      const int e0 = e, pos0 = pos;  // the walk's start: v[k] is k steps on
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         v[k] = make_uint4(0, 0, 0, 0);
         if (e < positions) {
-          const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+          const int hh = hb0 + b, ww = wb0 + pos;
           v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
                                     t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
           e += kHaloStep;
@@ -393,6 +414,10 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
         }
       }
       if (!stage_free) {
+#if defined(I8C_PIPELINE_TRACE)
+        if (ptrace && tseq < kTraceSlots)
+          p.trace[(28 + blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
+#endif
         // every lane runs the first batch, so the warp is converged here; the
         // outcome is made warp-uniform because the arrive below is warp-wide
         if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag)))
@@ -403,10 +428,19 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
           p.trace[(16 + 2 * blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
 #endif
       }
+      int ps = pos0;
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-        if (e0 + k * kHaloStep < positions) halo_store_f16(hp, halo, e0 + k * kHaloStep, h, v[k]);
+      for (int k = 0; k < kBatch; ++k) {
+        const int ek = e0 + k * kHaloStep;
+        if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
+        ps += w.pos_step;
+        ps -= ps >= hp.CW ? hp.CW : 0;
+      }
     } while (e < positions);
+#if defined(I8C_PIPELINE_TRACE)
+    if (ptrace && tseq < kTraceSlots)
+      p.trace[(26 + blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
+#endif
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
     skip = false;
@@ -709,6 +743,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   volatile uint32_t* fconv_gen = reinterpret_cast<volatile uint32_t*>(h_full + 15);  // grid barrier generation seen
   uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded
   uint64_t* x_done = h_full + 18;  // TMA-fed halo: int8 slot converted
+  uint64_t* h_fwd = h_full + 20;   // a pair's rank 1: its own producers' halo arrivals (up to three stages)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -736,6 +771,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     for (int i = 0; i < hp.nhs; ++i) {
       ptx::mbar_init(&h_full[i], halo_arrivals<kHaloSplitBatch>(hp) * CG);  // a pair's rank 0 counts both CTAs'
       ptx::mbar_init(&h_empty[i], 1);
+      if (CG == 2) ptx::mbar_init(&h_fwd[i], halo_arrivals<kHaloSplitBatch>(hp));
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&acc_full[i], 1);
@@ -1056,6 +1092,25 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       }
       __syncwarp();
       if (!ptx::mbar_wait(drain, 0, p.timeout_ns, nullptr) && lane == 0) raise_timeout(p, abort_flag);
+    } else if constexpr (CG == 2) {
+      // A pair's rank 1: forward each completed fill of its own halo stages
+      // as one arrival (all of its producers' count) on rank 0's barrier.
+      // The producers' stores are ordered before it by their release on the
+      // local barrier and this lane's acquire of it; rank 0's MMAs read them
+      // after acquiring its barrier.  It never runs two fills ahead: a stage
+      // is refilled only after the MMAs have consumed the forwarded fill.
+      const uint32_t n = halo_arrivals<kHaloSplitBatch>(hp);
+      uint32_t hs = 0, hph = 0;
+      bool fine = true;
+      for (StageIter it(hp, ts); it.valid(hp); it.next(hp, ts)) {
+        fine = __all_sync(0xffffffffu, ptx::mbar_wait(&h_fwd[hs], hph, p.timeout_ns, abort_flag));
+        if (!fine) break;
+        if (lane == 0) ptx::mbar_arrive_remote(ptx::mapa(ptx::smem_addr(&h_full[hs]), 0), n);
+        __syncwarp();
+        hs = hs + 1 == static_cast<uint32_t>(hp.nhs) ? 0u : hs + 1;
+        hph ^= hs == 0 ? 1u : 0u;
+      }
+      if (!fine && lane == 0) raise_timeout(p, abort_flag);
     }
   } else if (warp == kTmaWarp) {
     // ------------------------------------------------------------ filter TMA producer
@@ -1149,11 +1204,18 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::setmaxnreg_dec<kWorkerRegs>();
     ptx::griddep_wait();  // the activations may come from the kernel before this one
     const int pt = (warp < kTmaWarp ? warp - 1 : warp - 2) * 32 + lane;
-    const TileSched ts = tile_sched<CG>();
-    const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,
+    TileSched ts = tile_sched<CG>();
+    // a pair's rank 1 arrives on its own barriers (warp 0 forwards them):
+    // its producer warps do not wait for a cluster-scope release
+    uint64_t* hf = h_full;
+    if (CG == 2 && ts.rank == 1) {
+      ts.fwd = 1;
+      hf = h_fwd;
+    }
+    const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, hf, h_empty, x_full, x_done, &tmap_x,
                                                    abort_flag, pt)
-                    : hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                  : halo_produce_registers<kHaloSplitBatch>(hp, ts, smem, h_full, h_empty,
+                    : hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, hf, h_empty, abort_flag, pt)
+                                  : halo_produce_registers<kHaloSplitBatch>(hp, ts, smem, hf, h_empty,
                                                                              abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else if (warp >= 8) {

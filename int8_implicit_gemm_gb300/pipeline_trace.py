@@ -18,7 +18,11 @@ per run configuration:
     the first entry to the last exit over all CTAs;
   - prod_* (halo kernel): producer thread 0's time from its halo stage being
     free to its arrival, from its arrival to the next stage being free, and
-    its period per channel block, in microseconds (the *_cta1 keys: the same
+    its period per channel block, in microseconds; for the register-load
+    producer also from its arrival to the next channel block's first load,
+    the time to issue that block's loads, from their issue to the stage being free, from the
+    stage being free to its stores done, and from the stores to its arrival
+    (the fence and the arrive) (the *_cta1 keys: the same
     for CTA 1, a pair's rank 1; cta1_arrive_lag_us: how much later rank 1
     announces each halo stage than rank 0);
   - cb_interval_us: median and maximum time between consecutive halo
@@ -104,6 +108,18 @@ def trace_workload(shape, alpha, runs: int = 6, **opts) -> dict:
                 out["prod_arrive_to_next_free_us" + suffix] = round(
                     float(np.median(free[2:m] - arrive[1:m - 1])) / 1e3, 3)
                 out["prod_period_us" + suffix] = round(float(np.median(np.diff(arrive[1:m]))) / 1e3, 3)
+            # direct register-load producer: loads issued, stores done
+            issued, stored = tr[28 + cta], tr[26 + cta]
+            k = int(np.sum((issued > 0) & (stored > 0) & (free > 0) & (arrive > 0)))
+            if k > 3:
+                out["prod_issue_to_free_us" + suffix] = round(float(np.median(free[1:k] - issued[1:k])) / 1e3, 3)
+                out["prod_free_to_stored_us" + suffix] = round(float(np.median(stored[1:k] - free[1:k])) / 1e3, 3)
+                out["prod_stored_to_arrive_us" + suffix] = round(float(np.median(arrive[1:k] - stored[1:k])) / 1e3, 3)
+                before = tr[30 + cta]  # before the first load of the channel block
+                if int(np.sum(before > 0)) > k - 1:
+                    out["prod_arrive_to_before_loads_us" + suffix] = round(
+                        float(np.median(before[2:k] - arrive[1:k - 1])) / 1e3, 3)
+                    out["prod_loads_issue_us" + suffix] = round(float(np.median(issued[1:k] - before[1:k])) / 1e3, 3)
         if info["kernel_variant"] == 3:
             a0, a1 = tr[17], tr[19]
             m = int(min(np.sum(a0 > 0), np.sum(a1 > 0)))

@@ -26,7 +26,7 @@ from tests.test_gpu_parity import SMALL, STACKED_SHAPES, TRANSPOSED_EXTRA
 
 KMAX_SMEM = 232448          # opt-in dynamic shared memory per block on sm_103
 KMAX_FILTER_STAGES = 16     # filter stages the kernels have barriers for
-KHALO_BARRIER_WORDS = 52    # 8-byte barrier and control words the halo and transposed kernels use
+KHALO_BARRIER_WORDS = 55    # 8-byte barrier and control words the halo and transposed kernels use
 
 
 def _taps(shape):
