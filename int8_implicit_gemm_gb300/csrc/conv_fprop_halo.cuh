@@ -214,21 +214,13 @@ __device__ __forceinline__ void halo_walk_origin(const HaloParams& hp, int m0, i
 
 // Index in its row of the halo position that holds input column c (relative
 // to the halo's first column): positions are ordered by column phase (column
-// mod stride_w), phase f from phase_off[f].  The inverse of halo_column.
+// mod stride_w), phase f from phase_off[f].
 __device__ __forceinline__ int halo_phase_index(const HaloParams& hp, int c) {
   const int sw = hp.c.stride_w;
   if (sw == 1) return c;
   if (sw == 2) return (c >> 1) + ((c & 1) ? hp.phase_off[1] : 0);
   const int f = c % sw;
   return hp.phase_off[f] + c / sw;
-}
-
-// Input column (relative to the halo's first column) of halo position pos in
-// its row: positions are ordered by column phase (column mod stride_w).
-__device__ __forceinline__ int halo_column(const HaloParams& hp, int pos) {
-  int f = hp.c.stride_w - 1;
-  while (pos < hp.phase_off[f]) --f;
-  return (pos - hp.phase_off[f]) * hp.c.stride_w + f;
 }
 
 // A work unit: channel blocks [cb0, cb1) of one tile; part < 0 for a whole
@@ -301,8 +293,8 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
       const uint32_t dst0 = stg_base + slot * hp.stg_bytes;
       int b = w.b_first, pos = w.pos_first;
       halo_walk_origin(hp, t.m0, b, pos);
-      for (int e = w.e_first; e < positions; e += kHaloStep) {
-        const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+      for (int e = w.e_first; e < positions; e += kHaloStep) {  // natural order: pos is the input column
+        const int hh = hb0 + b, ww = wb0 + pos;
         const bool in = t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
         const int8_t* src = in ? img + (hh * p.W + ww) * 32 + h * 16 : p.x;
         ptx::cp_async_16_ca(dst0 + e * 32 + h * 16, src, in ? 16u : 0u);
@@ -340,8 +332,15 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
 #endif
     const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
     uint8_t* halo = smem + hs * hp.halo_bytes;
-    for (int e = w.e_first; e < positions; e += kHaloStep)
-      halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+    // the ring holds the pixels in natural order; the halo by column phase
+    int ps = w.pos_first;
+    if (hp.flat) ps = 0;  // stride 1: the phase order is the natural order
+    for (int e = w.e_first; e < positions; e += kHaloStep) {
+      halo_store_f16(hp, halo, e - ps + halo_phase_index(hp, ps), h,
+                     *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+      ps += w.pos_step;
+      ps -= ps >= hp.CW ? hp.CW : 0;
+    }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
 #if defined(I8C_PIPELINE_TRACE)
@@ -510,8 +509,8 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
       v[k] = make_uint4(0, 0, 0, 0);
-      if (e < positions) {
-        const int hh = hb0 + b, ww = wb0 + halo_column(hp, pos);
+      if (e < positions) {  // natural order: pos is the input column
+        const int hh = hb0 + b, ww = wb0 + pos;
         v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
                                   t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
         e += step;
@@ -529,10 +528,13 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
     // warp-uniform outcome: the arrive below is a warp-wide operation
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) return false;
     uint8_t* halo = smem + hs * hp.halo_bytes;
+    int ps = hp.flat ? 0 : pos_first;  // stride 1 (flat tiles): the phase order is the natural order
 #pragma unroll
     for (int k = 0; k < kB; ++k) {
       const int ek = e_first + k * step;
-      if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
+      if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
+      ps += pos_step;
+      ps -= ps >= hp.CW ? hp.CW : 0;
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
@@ -613,20 +615,18 @@ __device__ __forceinline__ bool halo_produce_tma(const HaloParams& hp, const Til
     const PatchTile t = decode_patch(it.tile, hp, ts);
     const uint8_t* x8 = smem + hp.off_x8 + slot * hp.x8_bytes;
     uint8_t* halo = smem + hs * hp.halo_bytes;
-    // halo position e in the box: flat tiles f0 + e (the run starts f0
-    // positions into the box's first padded row); 2-D patches row b, natural
-    // column halo_column(pos) of the phase-ordered position pos
+    // the box in natural order: flat tiles (stride 1) store position e
+    // from f0 + e (the run starts f0 positions into the box's first padded
+    // row); 2-D patches walk the box's pixels e = row * CW + column and store
+    // each at its column-phase position in the row
     const int f0 = hp.flat ? t.m0 - (t.m0 / hp.CW) * hp.CW : 0;
-    int b = w.b_first, pos = w.pos_first;
+    int pos = w.pos_first;
     for (int e = w.e_first; e < positions; e += kHaloStep) {
-      const int src = hp.flat ? f0 + e : b * hp.CW + halo_column(hp, pos);
-      halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(x8 + src * 32 + h * 16));
-      b += w.b_step;
+      const int src = hp.flat ? f0 + e : e;
+      const int dst = hp.flat ? e : e - pos + halo_phase_index(hp, pos);
+      halo_store_f16(hp, halo, dst, h, *reinterpret_cast<const uint4*>(x8 + src * 32 + h * 16));
       pos += w.pos_step;
-      if (pos >= hp.CW) {
-        pos -= hp.CW;
-        ++b;
-      }
+      pos -= pos >= hp.CW ? hp.CW : 0;
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
@@ -741,9 +741,9 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   volatile int* split_last = reinterpret_cast<volatile int*>(h_full + 13);  // this CTA combines a split tile
   uint64_t* fconv_done = h_full + 14;  // this CTA's share of the filter is converted and announced
   volatile uint32_t* fconv_gen = reinterpret_cast<volatile uint32_t*>(h_full + 15);  // grid barrier generation seen
-  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded
-  uint64_t* x_done = h_full + 18;  // TMA-fed halo: int8 slot converted
-  uint64_t* h_fwd = h_full + 20;   // a pair's rank 1: its own producers' halo arrivals (up to three stages)
+  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded (up to three slots)
+  uint64_t* x_done = h_full + 19;  // TMA-fed halo: int8 slot converted
+  uint64_t* h_fwd = h_full + 22;   // a pair's rank 1: its own producers' halo arrivals (up to three stages)
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -780,7 +780,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     ptx::mbar_init(drain, 1);
     ptx::mbar_init(epi_sync, kEpilogue);
     ptx::mbar_init(fconv_done, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&x_full[i], 1);
       ptx::mbar_init(&x_done[i], kProducers);
     }

@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
   uint64_t* drain = h_full + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(h_full + 11) + 1;
-  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded
-  uint64_t* x_done = h_full + 18;  // TMA-fed halo: int8 slot converted
+  uint64_t* x_full = h_full + 16;  // TMA-fed halo: int8 slot loaded (up to three slots)
+  uint64_t* x_done = h_full + 19;  // TMA-fed halo: int8 slot converted
 
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 5, 0);
   const int lane = threadIdx.x & 31;
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
       ptx::mbar_init(&acc_empty[i], kEpilogue * CG);
     }
     ptx::mbar_init(drain, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&x_full[i], 1);
       ptx::mbar_init(&x_done[i], kProducers);
     }

@@ -218,9 +218,9 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
   static const int kSlots[3] = {3, 2, 0};
   const int first = loads == 1 ? 0 : 2, last = loads == 1 ? 1 : 2;
   const int RS = s.R * s.S;
-  // TMA-fed halos (loads == 3): one or two int8 slots of one box each; two
-  // unless the second would cost the filter its residency (one output-channel
-  // tile whose every stage fits)
+  // TMA-fed halos (loads == 3): one to three int8 slots of one box each; the
+  // most that leave the filter enough stages, and one where more would cost
+  // the filter its residency (one output-channel tile whose every stage fits)
   const bool tma = loads == 3;
   if (tma && !tma_halo_box(s, *h, h)) return false;
   const int n_tiles = (s.K + bn - 1) / bn;
@@ -241,7 +241,7 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
       const int64_t need_resident = (s.C / 32) * RS / G;
       int64_t off_x8 = 0, off_b = 0, nbs = 0;
       int nxs = 0;
-      for (int nx = tma ? 2 : 0; nx >= 0; --nx) {  // TMA: two slots, else one; no TMA: none
+      for (int nx = tma ? 3 : 0; nx >= 0; --nx) {  // TMA: three slots, else fewer; no TMA: none
         const int64_t off_stg = static_cast<int64_t>(nhs) * h->halo_bytes;
         const int64_t ox = (off_stg + static_cast<int64_t>(nstg) * h->stg_bytes + 1023) / 1024 * 1024;
         const int64_t ob = (ox + static_cast<int64_t>(nx) * h->x8_bytes + 1023) / 1024 * 1024;
@@ -251,7 +251,7 @@ bool halo_layout(const i8c_conv_shape& s, int P, int Q, int bn, int cg, int load
           if (tma && nx > 1) continue;
           break;
         }
-        if (tma && nx == 2 && n_tiles == 1 && n < need_resident) {
+        if (tma && nx >= 2 && n_tiles == 1 && n < need_resident) {
           // would one slot keep the filter resident?
           const int64_t ob1 = (ox + h->x8_bytes + 1023) / 1024 * 1024;
           const int64_t n1 = (budget - ob1) / stage;
