@@ -333,13 +333,17 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
     const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
     uint8_t* halo = smem + hs * hp.halo_bytes;
     // the ring holds the pixels in natural order; the halo by column phase
-    int ps = w.pos_first;
-    if (hp.flat) ps = 0;  // stride 1: the phase order is the natural order
-    for (int e = w.e_first; e < positions; e += kHaloStep) {
-      halo_store_f16(hp, halo, e - ps + halo_phase_index(hp, ps), h,
-                     *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
-      ps += w.pos_step;
-      ps -= ps >= hp.CW ? hp.CW : 0;
+    if (p.stride_w == 1) {  // the same order (always so for flat tiles)
+      for (int e = w.e_first; e < positions; e += kHaloStep)
+        halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+    } else {
+      int ps = w.pos_first;
+      for (int e = w.e_first; e < positions; e += kHaloStep) {
+        halo_store_f16(hp, halo, e - ps + halo_phase_index(hp, ps), h,
+                       *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+        ps += w.pos_step;
+        ps -= ps >= hp.CW ? hp.CW : 0;
+      }
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
@@ -427,13 +431,19 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
           p.trace[(16 + 2 * blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
 #endif
       }
-      int ps = pos0;
+      if (p.stride_w == 1) {  // the phase order is the natural order
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int ek = e0 + k * kHaloStep;
-        if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
-        ps += w.pos_step;
-        ps -= ps >= hp.CW ? hp.CW : 0;
+        for (int k = 0; k < kBatch; ++k)
+          if (e0 + k * kHaloStep < positions) halo_store_f16(hp, halo, e0 + k * kHaloStep, h, v[k]);
+      } else {
+        int ps = pos0;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int ek = e0 + k * kHaloStep;
+          if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
+          ps += w.pos_step;
+          ps -= ps >= hp.CW ? hp.CW : 0;
+        }
       }
     } while (e < positions);
 #if defined(I8C_PIPELINE_TRACE)
@@ -528,13 +538,21 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
     // warp-uniform outcome: the arrive below is a warp-wide operation
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) return false;
     uint8_t* halo = smem + hs * hp.halo_bytes;
-    int ps = hp.flat ? 0 : pos_first;  // stride 1 (flat tiles): the phase order is the natural order
+    if (p.stride_w == 1) {  // the phase order is the natural order (always so for flat tiles)
 #pragma unroll
-    for (int k = 0; k < kB; ++k) {
-      const int ek = e_first + k * step;
-      if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
-      ps += pos_step;
-      ps -= ps >= hp.CW ? hp.CW : 0;
+      for (int k = 0; k < kB; ++k) {
+        const int ek = e_first + k * step;
+        if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
+      }
+    } else {
+      int ps = pos_first;
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        const int ek = e_first + k * step;
+        if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
+        ps += pos_step;
+        ps -= ps >= hp.CW ? hp.CW : 0;
+      }
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !skip);
