@@ -333,17 +333,13 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
     const uint8_t* stg = smem + hp.off_stg + (s % nstg) * hp.stg_bytes;
     uint8_t* halo = smem + hs * hp.halo_bytes;
     // the ring holds the pixels in natural order; the halo by column phase
-    if (p.stride_w == 1) {  // the same order (always so for flat tiles)
-      for (int e = w.e_first; e < positions; e += kHaloStep)
-        halo_store_f16(hp, halo, e, h, *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
-    } else {
-      int ps = w.pos_first;
-      for (int e = w.e_first; e < positions; e += kHaloStep) {
-        halo_store_f16(hp, halo, e - ps + halo_phase_index(hp, ps), h,
-                       *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
-        ps += w.pos_step;
-        ps -= ps >= hp.CW ? hp.CW : 0;
-      }
+    int ps = w.pos_first;
+    if (hp.flat) ps = 0;  // stride 1: the phase order is the natural order
+    for (int e = w.e_first; e < positions; e += kHaloStep) {
+      halo_store_f16(hp, halo, e - ps + halo_phase_index(hp, ps), h,
+                     *reinterpret_cast<const uint4*>(stg + e * 32 + h * 16));
+      ps += w.pos_step;
+      ps -= ps >= hp.CW ? hp.CW : 0;
     }
     ptx::fence_proxy_async_smem();
     arrive_on_leader(&h_full[hs], ts, !((p.debug_flags & 1) && s == 0 && pt == 0));
@@ -364,8 +360,9 @@ __device__ __forceinline__ bool halo_produce_staged(const HaloParams& hp, const 
 // while it waits for its halo stage is the whole halo when it fits (6 loads
 // for the 561 positions of a stride-2 16x8 patch, 8 for the 768 of the
 // dilated 5x9 layer; 10 would not fit the producers' registers); the smaller
-// batch where 6 suffice keeps the loop short.
-template <int kBatch>
+// batch where 6 suffice keeps the loop short.  kUnit: the kernel runs
+// stride-1 layers only, whose column-phase order is the natural order.
+template <int kBatch, bool kUnit = false>
 __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                    uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                    int pt) {
@@ -389,6 +386,9 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
     int e = w.e_first, b = w.b_first, pos = w.pos_first;
     halo_walk_origin(hp, t.m0, b, pos);
     bool stage_free = false;
+    // the tile's next channel block (the same pixels one channel-block plane
+    // on) is prefetched into L2 from these loads, one lane per 32-byte pixel
+    const bool pf = h == 0 && it.cb + 1 < it.cb_end;
 #if defined(I8C_PIPELINE_TRACE)
     if (ptrace && tseq < kTraceSlots)
       p.trace[(30 + blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
@@ -405,8 +405,10 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
         v[k] = make_uint4(0, 0, 0, 0);
         if (e < positions) {
           const int hh = hb0 + b, ww = wb0 + pos;
-          v[k] = ptx::ldg16_or_zero(img + (hh * p.W + ww) * 32 + h * 16,
-                                    t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W);
+          const bool in = t.valid && hh >= 0 && hh < p.H && ww >= 0 && ww < p.W;
+          const int8_t* src = img + (hh * p.W + ww) * 32 + h * 16;
+          v[k] = ptx::ldg16_or_zero(src, in);
+          if (pf && in) ptx::prefetch_l2(src + HW32);
           e += kHaloStep;
           b += w.b_step;
           pos += w.pos_step;
@@ -431,15 +433,13 @@ __device__ __forceinline__ bool halo_produce_direct(const HaloParams& hp, const 
           p.trace[(16 + 2 * blockIdx.x) * kTraceSlots + tseq] = static_cast<long long>(ptx::globaltimer_ns());
 #endif
       }
-      if (p.stride_w == 1) {  // the phase order is the natural order
+      int ps = pos0;
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k)
-          if (e0 + k * kHaloStep < positions) halo_store_f16(hp, halo, e0 + k * kHaloStep, h, v[k]);
-      } else {
-        int ps = pos0;
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int ek = e0 + k * kHaloStep;
+      for (int k = 0; k < kBatch; ++k) {
+        const int ek = e0 + k * kHaloStep;
+        if constexpr (kUnit) {
+          if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
+        } else {
           if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
           ps += w.pos_step;
           ps -= ps >= hp.CW ? hp.CW : 0;
@@ -489,7 +489,7 @@ __device__ __forceinline__ uint32_t halo_arrivals(const HaloParams& hp) {
   return ng > 0 ? kProducers / ng : kProducers;
 }
 
-template <int kB>
+template <int kB, bool kUnit = false>
 __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                   uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                   int pt, int ng) {
@@ -538,17 +538,13 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
     // warp-uniform outcome: the arrive below is a warp-wide operation
     if (!__all_sync(0xffffffffu, ptx::mbar_wait(&h_empty[hs], hph ^ 1u, p.timeout_ns, abort_flag))) return false;
     uint8_t* halo = smem + hs * hp.halo_bytes;
-    if (p.stride_w == 1) {  // the phase order is the natural order (always so for flat tiles)
+    int ps = hp.flat ? 0 : pos_first;  // stride 1 (flat tiles): the phase order is the natural order
 #pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        const int ek = e_first + k * step;
+    for (int k = 0; k < kB; ++k) {
+      const int ek = e_first + k * step;
+      if constexpr (kUnit) {
         if (ek < positions) halo_store_f16(hp, halo, ek, h, v[k]);
-      }
-    } else {
-      int ps = pos_first;
-#pragma unroll
-      for (int k = 0; k < kB; ++k) {
-        const int ek = e_first + k * step;
+      } else {
         if (ek < positions) halo_store_f16(hp, halo, ek - ps + halo_phase_index(hp, ps), h, v[k]);
         ps += pos_step;
         ps -= ps >= hp.CW ? hp.CW : 0;
@@ -566,14 +562,15 @@ __device__ __forceinline__ bool halo_produce_split(const HaloParams& hp, const T
 // producers on every channel block.
 constexpr int kHaloSplitBatch = 4;  // the halo kernel's producers: the most that fits 72 registers
 
-template <int kB>
+template <int kB, bool kUnit = false>
 __device__ __forceinline__ bool halo_produce_registers(const HaloParams& hp, const TileSched& ts, uint8_t* smem,
                                                       uint64_t* h_full, uint64_t* h_empty, volatile int* abort_flag,
                                                       int pt) {
   const int ng = halo_groups<kB>(hp);
-  if (ng > 0) return halo_produce_split<kB>(hp, ts, smem, h_full, h_empty, abort_flag, pt, ng);
-  return hp.positions > 6 * kHaloStep ? halo_produce_direct<8>(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                      : halo_produce_direct<6>(hp, ts, smem, h_full, h_empty, abort_flag, pt);
+  if (ng > 0) return halo_produce_split<kB, kUnit>(hp, ts, smem, h_full, h_empty, abort_flag, pt, ng);
+  return hp.positions > 6 * kHaloStep
+             ? halo_produce_direct<8, kUnit>(hp, ts, smem, h_full, h_empty, abort_flag, pt)
+             : halo_produce_direct<6, kUnit>(hp, ts, smem, h_full, h_empty, abort_flag, pt);
 }
 
 // Producer fed by TMA: thread 0 issues, nxs channel blocks ahead, one box

@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kHaloThreads, 1)
     const bool ok = hp.tma_halo ? halo_produce_tma(hp, ts, smem, h_full, h_empty, x_full, x_done, &tmap_x,
                                                    abort_flag, pt)
                     : hp.nstg > 0 ? halo_produce_staged(hp, ts, smem, h_full, h_empty, abort_flag, pt)
-                                  : halo_produce_registers<Regs::kBatch>(hp, ts, smem, h_full, h_empty,
-                                                                         abort_flag, pt);
+                                  : halo_produce_registers<Regs::kBatch, true>(hp, ts, smem, h_full, h_empty,
+                                                                               abort_flag, pt);
     if (!ok) raise_timeout(p, abort_flag);
   } else {
     // ------------------------------------------------------------ epilogue
