@@ -303,3 +303,47 @@ def test_in_kernel_resident_filter_needs_a_resident_halo_plan(ext):
         with pytest.raises(ext.I8ConvError) as e:
             ext.i8c_plan_layout(shape, 152, **opts)
         assert e.value.status == ext.I8C_ERR_UNSUPPORTED, opts
+
+
+def _random_shapes(seed, count):
+    """Seeded convolution shapes across the planner's ranges: channel counts
+    that are multiples of 32 (K also ragged), filters 1-9 taps a side,
+    strides 1-4, dilations 1-4, paddings up to the filter's reach, images
+    from a few pixels to a few hundred."""
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < count:
+        R, S = rng.randint(1, 9), rng.randint(1, 9)
+        sh, sw = rng.choice([1, 1, 1, 2, 2, 3, 4]), rng.choice([1, 1, 1, 2, 2, 3, 4])
+        dh, dw = rng.choice([1, 1, 2, 3, 4]), rng.choice([1, 1, 2, 3, 4])
+        ph, pw = rng.randint(0, (R - 1) * dh), rng.randint(0, (S - 1) * dw)
+        H, W = rng.randint(1, 160), rng.randint(1, 320)
+        N = rng.randint(1, 8)
+        C = 32 * rng.choice([1, 1, 2, 3, 4, 8, 16])
+        K = rng.choice([32, 64, 96, 128, 160, 256, 512, 24, 200])
+        shape = (N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw)
+        P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+        Q = (W + 2 * pw - dw * (S - 1) - 1) // sw + 1
+        if P >= 1 and Q >= 1:
+            out.append(shape)
+    return out
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13, 14])
+def test_random_shapes_every_plan_form_stays_in_bounds(ext, seed):
+    """Seeded random shapes through every plan form: every layout the planner
+    accepts passes the same bounds check as the fixed shapes (the planner
+    may refuse a form for a shape; it must never hand a kernel a layout whose
+    accesses leave their regions)."""
+    accepted = 0
+    for shape in _random_shapes(seed, 150):
+        if ext.i8c_supported(shape) != ext.I8C_OK:
+            continue
+        for opts in PLAN_FORMS:
+            L = _layout(ext, shape, opts)
+            if L is None:
+                continue
+            check_layout(shape, L)
+            accepted += 1
+    assert accepted >= 1000
