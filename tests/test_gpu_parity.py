@@ -665,3 +665,56 @@ def test_wide_patches_exact(shape, kw):
     y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **kw)
     assert np.array_equal(acc, acc_ref.astype(np.int32))
     assert np.array_equal(y, y_ref)
+
+
+def _random_small_shapes(seed, count):
+    """Seeded small convolutions across the planner's ranges (strides and
+    dilations 1-4, filters up to 7 taps a side, paddings up to the filter's
+    reach, ragged images, K a multiple of 32), sized for the oracle."""
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < count:
+        R, S = rng.randint(1, 7), rng.randint(1, 7)
+        sh, sw = rng.choice([1, 1, 2, 3, 4]), rng.choice([1, 1, 2, 3, 4])
+        if rng.random() < 0.4:  # stride 1 both ways: the transposed and stacked forms too
+            sh = sw = 1
+        dh, dw = rng.choice([1, 1, 2, 3]), rng.choice([1, 1, 2, 4])
+        ph, pw = rng.randint(0, (R - 1) * dh), rng.randint(0, (S - 1) * dw)
+        H, W = rng.randint(3, 30), rng.randint(3, 40)
+        N, C, K = rng.randint(1, 3), 32 * rng.randint(1, 3), 32 * rng.randint(1, 4)
+        P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+        Q = (W + 2 * pw - dw * (S - 1) - 1) // sw + 1
+        if P >= 1 and Q >= 1:
+            out.append((N, C, H, W, K, R, S, ph, pw, sh, sw, dh, dw))
+    return out
+
+
+RANDOM_FORMS = [{}, dict(kernel_variant=1), dict(kernel_variant=2), dict(kernel_variant=3),
+                dict(kernel_variant=4), dict(kernel_variant=5), dict(kernel_variant=6),
+                dict(kernel_variant=2, halo_loads=3), dict(tile_shape=3), dict(kernel_variant=2, halo_loads=1)]
+
+
+@pytest.mark.parametrize("shape", _random_small_shapes(2024, 24), ids=lambda s: "x".join(map(str, s)))
+def test_random_shapes_exact(shape):
+    """Seeded random small shapes on every kernel form the planner accepts for
+    them (auto, per-tap gather, halo, halo pairs, transposed tiles on single
+    CTAs and pairs, stacked taps, TMA-fed halos, 16x16 patches, staged
+    halos): int32 accumulators and int8 outputs bit-exact against the oracle;
+    forms the planner refuses are skipped."""
+    import int8_implicit_gemm_gb300 as ext
+    x, f = _data(shape, 31 + sum(shape))
+    y_ref, acc_ref = gpu_util.oracle_packed(shape, x, f, 2.0 ** -10)
+    ran = 0
+    for kw in RANDOM_FORMS:
+        try:
+            ext.Plan(shape, **kw).destroy()
+        except ext.I8ConvError as e:
+            if e.status == ext.I8C_ERR_UNSUPPORTED:
+                continue
+            raise
+        y, acc = gpu_util.gpu_run(shape, x, f, 2.0 ** -10, **kw)
+        assert np.array_equal(acc, acc_ref.astype(np.int32)), kw
+        assert np.array_equal(y, y_ref), kw
+        ran += 1
+    assert ran >= 2
