@@ -112,9 +112,10 @@ typedef struct {
                                 patch: two 16x8 sub-tiles on one halo, two MMAs per tap and K
                                 half (block_n <= 128, whole filter rows per filter stage,
                                 register or staged halo loads, no split tail; else
-                                I8C_ERR_UNSUPPORTED).  Auto takes 16x16 patches where they
-                                keep the filter resident (one output-channel tile) and the
-                                planner's cost model prefers them                          */
+                                I8C_ERR_UNSUPPORTED).  Auto takes 16x16 patches at block_n
+                                <= 64 where they keep the filter resident (one output-
+                                channel tile whose every stage fits) and the planner's cost
+                                model prefers them                                          */
   int32_t fused_filter;      /* where the int8 filter becomes the fp16 MMA operand:
                                 0 = auto (2 where the halo kernel keeps the whole filter
                                 resident in shared memory, else 3);
